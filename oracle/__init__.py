@@ -1,0 +1,172 @@
+"""CPU oracle for MXFP4 block-scaled quantization and GEMM (numpy front end over the C
+code in mxfp4_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the package's smoke check and by
+the benchmark's CPU-baseline leg, never by the product path.  It shares no code with the
+CUDA library.  The arithmetic and the passages it follows are documented in
+mxfp4_oracle.c; this module only marshals numpy arrays.
+
+Parity status: every function here is pinned by the oracle self-tests
+(tests/test_oracle_*.py) except the tensor-core scale layout, whose byte positions are a
+layout of this library's own choosing; that permutation is pinned on the CPU only as a
+bijection, and against the hardware by the GEMM parity tests.
+"""
+import ctypes
+import numpy as np
+
+from . import build as _build
+
+BLOCK = 32   # MXFP4_BLOCK_SIZE
+PAD = 128    # MXFP4_PADDING_ALIGN_SIZE
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        i64, u8, u16, f64 = ctypes.c_int64, ctypes.c_uint8, ctypes.c_uint16, ctypes.c_double
+        vp = ctypes.c_void_p
+        lib.oracle_bf16_to_f64.argtypes = [u16]
+        lib.oracle_bf16_to_f64.restype = f64
+        lib.oracle_e2m1_decode.argtypes = [u8]
+        lib.oracle_e2m1_decode.restype = f64
+        lib.oracle_e2m1_encode.argtypes = [f64]
+        lib.oracle_e2m1_encode.restype = u8
+        lib.oracle_e8m0_scale.argtypes = [f64]
+        lib.oracle_e8m0_scale.restype = u8
+        for fn in (lib.oracle_quantize_row, lib.oracle_quantize_col):
+            fn.argtypes = [vp, i64, i64, i64, vp, vp]
+            fn.restype = ctypes.c_int
+        lib.oracle_scale_to_tc.argtypes = [vp, i64, i64, vp]
+        lib.oracle_scale_to_tc.restype = None
+        lib.oracle_dequantize.argtypes = [vp, vp, i64, i64, vp]
+        lib.oracle_dequantize.restype = None
+        lib.oracle_gemm_f64.argtypes = [vp, vp, i64, i64, i64, i64, i64, vp, vp]
+        lib.oracle_gemm_f64.restype = None
+        lib.oracle_round_to_bf16.argtypes = [vp, vp, i64]
+        lib.oracle_round_to_bf16.restype = None
+        _lib = lib
+    return _lib
+
+
+def cdiv(a, b):
+    return (a + b - 1) // b
+
+
+def padded(n):
+    """Length of the packed dimension after padding to MXFP4_PADDING_ALIGN_SIZE."""
+    return cdiv(n, PAD) * PAD
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _bits(x):
+    x = np.asarray(x)
+    if x.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns (numpy uint16)")
+    return np.ascontiguousarray(x)
+
+
+# ---- scalar codecs -------------------------------------------------------------------
+def bf16_to_f64(bits):
+    return _load().oracle_bf16_to_f64(int(bits))
+
+
+def e2m1_decode(code):
+    return _load().oracle_e2m1_decode(int(code))
+
+
+def e2m1_encode(v):
+    return int(_load().oracle_e2m1_encode(float(v)))
+
+
+def e8m0_scale(amax):
+    return int(_load().oracle_e8m0_scale(float(amax)))
+
+
+# ---- quantizers ------------------------------------------------------------------------
+def quantize_row(x_bits):
+    """Row blob of X[M,K]: (q[M, Kp/2] u8, s[M, Kp/32] u8, plain scale layout)."""
+    x = _bits(x_bits)
+    M, K = x.shape
+    Kp = padded(K)
+    q = np.zeros((M, Kp // 2), np.uint8)
+    s = np.zeros((M, Kp // BLOCK), np.uint8)
+    if M and K and _load().oracle_quantize_row(_ptr(x), M, K, K, _ptr(q), _ptr(s)):
+        raise ValueError("oracle: non-finite input")
+    return q, s
+
+
+def quantize_col(x_bits):
+    """Col blob of X[M,K] = row blob of X^T: (q[K, Mp/2] u8, s[K, Mp/32] u8)."""
+    x = _bits(x_bits)
+    M, K = x.shape
+    Mp = padded(M)
+    q = np.zeros((K, Mp // 2), np.uint8)
+    s = np.zeros((K, Mp // BLOCK), np.uint8)
+    if M and K and _load().oracle_quantize_col(_ptr(x), M, K, K, _ptr(q), _ptr(s)):
+        raise ValueError("oracle: non-finite input")
+    return q, s
+
+
+def quantize_dual(x_bits):
+    """(row_q, row_s, col_q, col_s), the four outputs of the dual quantizer."""
+    rq, rs = quantize_row(x_bits)
+    cq, cs = quantize_col(x_bits)
+    return rq, rs, cq, cs
+
+
+def scale_to_tc(s_plain):
+    """Plain scale bytes [R, KB] -> tensor-core layout, flat u8 of ceil(R/128)*128*KB."""
+    s = np.ascontiguousarray(s_plain, dtype=np.uint8)
+    R, KB = s.shape
+    out = np.empty(padded(R) * KB, np.uint8)
+    _load().oracle_scale_to_tc(_ptr(s), R, KB, _ptr(out))
+    return out
+
+
+# ---- GEMM -------------------------------------------------------------------------------
+def dequantize(q, s):
+    """Blob (q[R, Kp/2], plain s[R, Kp/32]) -> fp64 [R, Kp]."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    R, half = q.shape
+    Kp = half * 2
+    assert s.shape == (R, Kp // BLOCK)
+    out = np.empty((R, Kp), np.float64)
+    _load().oracle_dequantize(_ptr(q), _ptr(s), R, Kp, _ptr(out))
+    return out
+
+
+def gemm_dequantized(a, b, rows=None, want_abs=True):
+    """C = A . B^T over fp64 dequantized operands A[M,Kp], B[N,Kp] (rows of C limited to
+    the range `rows` = (m0, m1) when given).  Returns (C, sum_k |a_k b_k|)."""
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    b = np.ascontiguousarray(b, dtype=np.float64)
+    M, Kp = a.shape
+    N, Kb = b.shape
+    assert Kb == Kp
+    m0, m1 = rows if rows is not None else (0, M)
+    c = np.empty((m1 - m0, N), np.float64)
+    cabs = np.empty((m1 - m0, N), np.float64) if want_abs else None
+    _load().oracle_gemm_f64(_ptr(a), _ptr(b), M, N, Kp, m0, m1, _ptr(c),
+                            _ptr(cabs) if want_abs else None)
+    return c, cabs
+
+
+def gemm(aq, a_s, bq, b_s, rows=None, want_abs=True):
+    """C[M,N] = A . B^T from two K-packed blobs in the plain scale layout."""
+    return gemm_dequantized(dequantize(aq, a_s), dequantize(bq, b_s), rows, want_abs)
+
+
+def round_to_bf16(x):
+    """fp64 -> bf16 bit patterns, one round-to-nearest-even."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, np.uint16)
+    _load().oracle_round_to_bf16(_ptr(x), _ptr(out), x.size)
+    return out

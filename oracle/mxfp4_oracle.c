@@ -1,0 +1,224 @@
+/*
+ * mxfp4_oracle.c -- plain, slow CPU oracle for MXFP4 block-scaled quantization and the
+ * block-scaled GEMM that consumes it.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or load this
+ * file: only the tests, the package's smoke check and the CPU-baseline leg of the
+ * benchmark use it.  It shares no code, header, table or constant with the CUDA
+ * library.
+ *
+ * What it computes, and the passages it follows:
+ *
+ *  - Element and scale formats: FP4 E2M1 elements packed two per byte
+ *    (torch.float4_e2m1fn_x2) and one E8M0 scale byte per block (torch.float8_e8m0fnu),
+ *    as the output dtypes of `_quantize_mxfp4_dual_fake` in primus_turbo_mxfp4_local.py
+ *    declare them.
+ *  - Block size 32 (MXFP4_BLOCK_SIZE) and padding of the packed dimension to a multiple
+ *    of 128 (MXFP4_PADDING_ALIGN_SIZE), primus_turbo_mxfp4_local.py, module constants and
+ *    the M_pad / N_pad arithmetic of `_quantize_mxfp4_dual_fake`.
+ *  - Row blob of X[R,K]: q[R, Kp/2], s[R, Kp/32]; col blob: the row blob of X^T
+ *    (same function, non-shuffled branch).
+ *  - The GEMM C = A . B^T over K-packed operands, the form the forward, dgrad and wgrad
+ *    calls of `MXFP4LinearFunction` in primus_turbo_mxfp4_local.py all take.
+ *
+ * The pages print no formula for the quantization itself.  The oracle follows the OCP
+ * Microscaling (MX) v1.0 rule for MXFP4:
+ *   scale exponent e = floor(log2(amax)) - 2   (2 = the largest E2M1 exponent),
+ *   clamped to the E8M0 range [-127, 127]; an all-zero block gets the byte 0x00;
+ *   element = round-to-nearest-even of v / 2^e onto {0, 0.5, 1, 1.5, 2, 3, 4, 6},
+ *   saturating at 6.
+ * Readings taken where that rule is silent (each is listed in the design notes):
+ *   - the sign of an element that rounds to zero is kept (-0 encodes as 0x8);
+ *   - padding elements are +0, so an all-padding block gets the byte 0x00;
+ *   - the low nibble of byte j holds element 2j, the high nibble element 2j+1;
+ *   - inputs must be finite; the quantizers return -1 on a NaN or infinity.
+ *
+ * Everything is computed in fp64, where every step above is exact.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define BLOCK 32
+#define PAD 128
+
+static int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+/* bf16 bit pattern -> double (exact: bf16 is the top half of an IEEE binary32). */
+double oracle_bf16_to_f64(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* E2M1 code (bit 3 sign, bits 2..1 exponent with bias 1, bit 0 mantissa) -> value. */
+double oracle_e2m1_decode(uint8_t code) {
+    int sign = (code >> 3) & 1;
+    int exp = (code >> 1) & 3;
+    int man = code & 1;
+    double mag = (exp == 0) ? 0.5 * man                       /* subnormal: 0 or 0.5 */
+                            : ldexp(1.0 + 0.5 * man, exp - 1); /* 1, 1.5, 2, 3, 4, 6 */
+    return sign ? -mag : mag;
+}
+
+/* Finite double -> E2M1 code: IEEE round-to-nearest-even onto the E2M1 grid, then
+ * saturation of anything above 6 to 6.  Within a binade the representable magnitudes
+ * are consecutive multiples of a quantum (0.5 below 2, 1 in [2,4), 2 in [4,8)), and an
+ * even multiple is an even code, so rounding v/quantum half-to-even rounds ties to the
+ * even code.  The sign bit is the sign of v, also when the magnitude rounds to 0. */
+uint8_t oracle_e2m1_encode(double v) {
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    double a = fabs(v);
+    double quantum = (a < 2.0) ? 0.5 : (a < 4.0) ? 1.0 : 2.0;
+    double r = nearbyint(a / quantum) * quantum; /* default rounding mode: ties-to-even */
+    if (r > 6.0) r = 6.0;
+    uint8_t mag;
+    if (r == 0.0) mag = 0;
+    else if (r == 0.5) mag = 1;
+    else if (r == 1.0) mag = 2;
+    else if (r == 1.5) mag = 3;
+    else if (r == 2.0) mag = 4;
+    else if (r == 3.0) mag = 5;
+    else if (r == 4.0) mag = 6;
+    else mag = 7; /* 6.0 */
+    return sign | mag;
+}
+
+/* Shared scale of a block whose largest magnitude is amax (finite, >= 0), as the E8M0
+ * byte (unbiased exponent + 127).  floor(log2(amax)) comes from frexp: amax = f * 2^E
+ * with f in [0.5, 1), so floor(log2(amax)) = E - 1. */
+uint8_t oracle_e8m0_scale(double amax) {
+    if (amax == 0.0) return 0;
+    int E;
+    frexp(amax, &E);
+    int e = (E - 1) - 2;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return (uint8_t)(e + 127);
+}
+
+/* Quantize one block of 32 values (padding already +0): writes 16 packed bytes and the
+ * scale byte.  Returns -1 if a value is not finite. */
+static int quantize_block(const double v[BLOCK], uint8_t q[BLOCK / 2], uint8_t* s) {
+    double amax = 0.0;
+    for (int i = 0; i < BLOCK; ++i) {
+        if (!isfinite(v[i])) return -1;
+        if (fabs(v[i]) > amax) amax = fabs(v[i]);
+    }
+    uint8_t byte = oracle_e8m0_scale(amax);
+    int e = (int)byte - 127;
+    for (int j = 0; j < BLOCK / 2; ++j) {
+        uint8_t lo = oracle_e2m1_encode(ldexp(v[2 * j], -e));
+        uint8_t hi = oracle_e2m1_encode(ldexp(v[2 * j + 1], -e));
+        q[j] = (uint8_t)(lo | (hi << 4));
+    }
+    *s = byte;
+    return 0;
+}
+
+/* Row blob of X[M,K] (bf16 bits, row pitch ldx elements): blocks of 32 run along K.
+ * q: [M, Kp/2] bytes, s: [M, Kp/32] bytes (plain layout).  Kp = ceil(K/128)*128. */
+int oracle_quantize_row(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                        uint8_t* s) {
+    int64_t Kp = cdiv64(K, PAD) * PAD, KB = Kp / BLOCK;
+    double v[BLOCK];
+    for (int64_t r = 0; r < M; ++r) {
+        for (int64_t b = 0; b < KB; ++b) {
+            for (int i = 0; i < BLOCK; ++i) {
+                int64_t k = b * BLOCK + i;
+                v[i] = (k < K) ? oracle_bf16_to_f64(x[r * ldx + k]) : 0.0;
+            }
+            if (quantize_block(v, q + r * (Kp / 2) + b * (BLOCK / 2), s + r * KB + b)) return -1;
+        }
+    }
+    return 0;
+}
+
+/* Col blob of X[M,K]: the row blob of X^T, i.e. blocks of 32 run along M.
+ * q: [K, Mp/2] bytes, s: [K, Mp/32] bytes (plain layout).  Mp = ceil(M/128)*128. */
+int oracle_quantize_col(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                        uint8_t* s) {
+    int64_t Mp = cdiv64(M, PAD) * PAD, MB = Mp / BLOCK;
+    double v[BLOCK];
+    for (int64_t k = 0; k < K; ++k) {
+        for (int64_t b = 0; b < MB; ++b) {
+            for (int i = 0; i < BLOCK; ++i) {
+                int64_t m = b * BLOCK + i;
+                v[i] = (m < M) ? oracle_bf16_to_f64(x[m * ldx + k]) : 0.0;
+            }
+            if (quantize_block(v, q + k * (Mp / 2) + b * (BLOCK / 2), s + k * MB + b)) return -1;
+        }
+    }
+    return 0;
+}
+
+/* Scale bytes of a blob with R rows and KB (a multiple of 4) blocks per row, from the
+ * plain layout s[R, KB] into the tensor-core layout: rows padded to a multiple of 128 and
+ * tiled in 128-row x 4-block atoms of 512 bytes, atoms ordered block-group-fastest; inside
+ * an atom, byte (r, kb) sits at (r % 32) * 16 + (r / 32) * 4 + kb, i.e. 32 lines of 16
+ * bytes.  Padding rows hold 0x00.  out must hold ceil(R/128)*128*KB bytes. */
+void oracle_scale_to_tc(const uint8_t* s, int64_t R, int64_t KB, uint8_t* out) {
+    int64_t Rp = cdiv64(R, PAD) * PAD;
+    memset(out, 0, (size_t)(Rp * KB));
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            int64_t atom = (r / 128) * (KB / 4) + kb / 4;
+            int64_t within = (r % 32) * 16 + ((r % 128) / 32) * 4 + (kb % 4);
+            out[atom * 512 + within] = s[r * KB + kb];
+        }
+}
+
+/* Dequantize a blob (plain scale layout) with R rows and Kp (multiple of 128) packed
+ * elements per row into out[R, Kp]: value = E2M1(code) * 2^(scale - 127). */
+void oracle_dequantize(const uint8_t* q, const uint8_t* s, int64_t R, int64_t Kp, double* out) {
+    int64_t KB = Kp / BLOCK;
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t k = 0; k < Kp; ++k) {
+            uint8_t byte = q[r * (Kp / 2) + k / 2];
+            uint8_t code = (k & 1) ? (byte >> 4) : (byte & 0xF);
+            out[r * Kp + k] = ldexp(oracle_e2m1_decode(code), (int)s[r * KB + k / BLOCK] - 127);
+        }
+}
+
+/* C[m,n] = sum_{k<Kp} A[m,k] * B[n,k] in fp64 over dequantized rows A[M,Kp], B[N,Kp]
+ * (both K-packed, the "TN" form), and cabs[m,n] = sum_k |A[m,k] * B[n,k]|, the scale the
+ * accuracy bound is stated against.  Either output may be NULL.  Only rows
+ * m in [m0, m1) of C are computed; c / cabs are indexed [m - m0, n]. */
+void oracle_gemm_f64(const double* a, const double* b, int64_t M, int64_t N, int64_t Kp,
+                     int64_t m0, int64_t m1, double* c, double* cabs) {
+    (void)M;
+    for (int64_t m = m0; m < m1; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, accabs = 0.0;
+            for (int64_t k = 0; k < Kp; ++k) {
+                double p = a[m * Kp + k] * b[n * Kp + k];
+                acc += p;
+                accabs += fabs(p);
+            }
+            if (c) c[(m - m0) * N + n] = acc;
+            if (cabs) cabs[(m - m0) * N + n] = accabs;
+        }
+}
+
+/* Round finite doubles to bf16 bit patterns, round-to-nearest-even, once.  bf16 keeps 8
+ * significant bits and the binary32 exponent range (normal down to 2^-126, subnormal
+ * spacing 2^-133); results beyond the largest finite value become infinity. */
+void oracle_round_to_bf16(const double* in, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) {
+        double x = in[i];
+        uint16_t sign = signbit(x) ? 0x8000 : 0;
+        double a = fabs(x);
+        if (a == 0.0) { out[i] = sign; continue; }
+        int E;
+        frexp(a, &E); /* a in [2^(E-1), 2^E) */
+        int e = E - 1;
+        double quantum = (e < -126) ? ldexp(1.0, -133) : ldexp(1.0, e - 7);
+        double r = nearbyint(a / quantum) * quantum;
+        if (r >= ldexp(1.0, 128)) { out[i] = sign | 0x7F80; continue; }
+        float f = (float)r; /* exact: r has at most 8 significant bits in bf16 range */
+        uint32_t u;
+        memcpy(&u, &f, sizeof u);
+        out[i] = sign | (uint16_t)(u >> 16);
+    }
+}
