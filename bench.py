@@ -1,0 +1,461 @@
+"""Benchmark of the GB300 MXFP4 linear hot path: one Flux-12B MLP up-projection training
+step (dual-quantize X, W, dY; fwd, dgrad and wgrad block-scaled GEMMs) per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--cpu-baseline-seconds S]
+
+Prints one JSON line (rank 0).  `value` is the step's GEMM work (3 x 2MNK flops) divided
+by the device time of the whole step, quantizers included, summed over all ranks' steps;
+per-kernel times, the GEMM roofline and the dual-quantizer bandwidth come with it.
+Under torchrun each rank runs its own replica of the step on its own GPU (the path has
+no exchange step), so scaling is weak.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP4 GEMM TFLOPS + dual-quant GB/s at Flux-12B shapes; % of roofline"
+DEFAULT_WORKLOAD = "flux12b_mlp_up_train_step_4608x12288x3072"
+L2_FLUSH_BYTES = 256 << 20       # > 2x the 129 MB L2
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # dense FP4 / dense bf16 tensor rate (nominal)
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "source": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mxfp4_block_scaled_quantize_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = t.get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.samples = []
+        self.proc = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [s for t, s in self.samples if self.window and self.window[0] - 0.15 <= t <= self.window[1] + 0.15]
+        if not rows:
+            rows = [s for _, s in self.samples[-3:]]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from mxfp4_block_scaled_quantize_gb300 import abi, workloads
+    from mxfp4_block_scaled_quantize_gb300.linear import MXFP4Linear
+    import __graft_entry__
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    abi.load()
+
+    wl = workloads.WORKLOADS[args.workload]
+    lin = wl.linears[0]
+    M, N, K = lin.M, lin.N, lin.K
+    t = wl.tensors(0)
+    x, w = t["X"].to(dev), t["W"].to(dev)
+    dy = t["dY"].to(dev) if lin.train else None
+    layer = MXFP4Linear(M, N, K, train=lin.train, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_k = layer.launches_per_step
+    names = (["quant_dual_X", "quant_dual_W", "gemm_fwd", "quant_dual_dY", "gemm_dgrad",
+              "gemm_wgrad"] if lin.train else ["quant_row_X", "quant_row_W", "gemm_fwd"])
+
+    def step_with_events(evs):
+        evs[0].record(stream)
+        layer.quantize_x(x)
+        evs[1].record(stream)
+        layer.quantize_w(w)
+        evs[2].record(stream)
+        layer.fwd_gemm()
+        evs[3].record(stream)
+        if lin.train:
+            layer.quantize_dy(dy)
+            evs[4].record(stream)
+            layer.dgrad_gemm()
+            evs[5].record(stream)
+            layer.wgrad_gemm()
+            evs[6].record(stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        layer.step(x, w, dy)
+    torch.cuda.synchronize()
+    if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
+        raise RuntimeError("device error word set during warm-up")
+
+    sampler = ClockSampler(local_rank)
+    if rank == 0:
+        sampler.start()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_k + 1)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t_start = time.time()
+    for k in range(args.steps):
+        flush.zero_()                      # evict L2 between timed steps (not timed)
+        step_with_events(events[k])
+    torch.cuda.synchronize()
+    t_end = time.time()
+    barrier()
+    sampler.mark(t_start, t_end)
+    clocks = sampler.stop() if rank == 0 else None
+    if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
+        raise RuntimeError("device error word set during the timed steps")
+
+    per_kernel = [[ev[i].elapsed_time(ev[i + 1]) for ev in events] for i in range(n_k)]
+    step_ms = [ev[0].elapsed_time(ev[n_k]) for ev in events]
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    # ---- end to end: inputs from pinned host memory, results back to pinned host memory
+    hx, hw = t["X"].pin_memory(), t["W"].pin_memory()
+    hdy = t["dY"].pin_memory() if lin.train else None
+    outs = [layer.y] + ([layer.dx, layer.dw] if lin.train else [])
+    houts = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(a.numel() * a.element_size() for a in (hx, hw, hdy) if a is not None)
+    d2h = sum(o.numel() * o.element_size() for o in houts)
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        x.copy_(hx, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        if lin.train:
+            dy.copy_(hdy, non_blocking=True)
+        layer.step(x, w, dy)
+        for o, ho in zip(outs, houts):
+            ho.copy_(o, non_blocking=True)
+    torch.cuda.synchronize()
+    e_ms = []
+    for _ in range(e2e_steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x.copy_(hx, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        if lin.train:
+            dy.copy_(hdy, non_blocking=True)
+        layer.step(x, w, dy)
+        for o, ho in zip(outs, houts):
+            ho.copy_(o, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e_ms.append(e0.elapsed_time(e1))
+    e2e_ms = statistics.mean(e_ms)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    if rank != 0:
+        return None
+
+    peaks = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
+    gemm_idx = [i for i, n in enumerate(names) if n.startswith("gemm")]
+    quant_idx = [i for i, n in enumerate(names) if n.startswith("quant")]
+    gemm_flops = 2 * M * N * K
+    gemm_ms = statistics.mean([v for i in gemm_idx for v in per_kernel[i]])
+    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
+
+    # algorithmic bytes of each quantizer launch (padding excluded)
+    shapes = {"X": (M, K), "W": (N, K), "dY": (M, N)}
+    bpe = 3.0625 if lin.train else 2.53125
+    kern = {}
+    for i, n in enumerate(names):
+        ms = statistics.mean(per_kernel[i])
+        ent = {"avg_us": round(ms * 1e3, 2), "min_us": round(min(per_kernel[i]) * 1e3, 2)}
+        if n.startswith("gemm"):
+            ent["tflops"] = round(gemm_flops / (ms * 1e-3) / 1e12, 1)
+            ent["frac_of_fp4_peak"] = round(ent["tflops"] / fp4_peak, 4)
+        else:
+            r, c = shapes[n.split("_")[-1]]
+            nbytes = r * c * bpe
+            ent["gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+            ent["frac_of_hbm"] = round(ent["gbs"] / peaks["hbm_gbs"], 4)
+        kern[n] = ent
+    q_bytes = sum(shapes[names[i].split("_")[-1]][0] * shapes[names[i].split("_")[-1]][1] * bpe
+                  for i in quant_idx)
+    q_ms = sum(statistics.mean(per_kernel[i]) for i in quant_idx)
+    quant_gbs = q_bytes / (q_ms * 1e-3) / 1e9
+
+    step_flops = lin.flops_step
+    value = world * step_flops * args.steps / (total_ms * 1e-3) / 1e12
+    e2e_value = world * step_flops / (e2e_ms * 1e-3) / 1e12
+    traffic = profiled_traffic("gemm_mxf4_kernel")
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp4_e2m1 (e8m0 block scales, fp32 accumulate, bf16 out)",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(0,1e-3) grads)",
+        "config": {"workload": args.workload, "M": M, "N": N, "K": K,
+                   "step": "dual-quant X,W; fwd; dual-quant dY; dgrad; wgrad" if lin.train
+                   else "row-quant X,W; fwd",
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_mxf4_kernel",
+                     "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak, 4),
+                     "traffic": traffic,
+                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x "
+                                    f"{NOMINAL_FP4_OVER_BF16:g} (nominal dense FP4/bf16 ratio)",
+                     "algorithmic_flops_per_launch": gemm_flops},
+        "quant_roofline": {"bound": "hbm", "achieved": round(quant_gbs, 1),
+                           "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                           "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
+                           "bytes_per_element": bpe, "peak_source": peaks["source"]},
+        "kernels": kern,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": n_k * args.steps,
+        "clocks": clocks,
+        "device": torch.cuda.get_device_name(dev),
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (cpu_baseline, and the reference arm)
+# ---------------------------------------------------------------------------------------
+def oracle_sample(workload_name, seconds):
+    """Times the oracle on slices of the workload and extrapolates one full step.
+
+    Sample: the oracle's dual (or row-only) quantizer on leading row slabs of X, W and dY,
+    and its fp64 GEMM on a block of output rows of each GEMM shape; each part is repeated
+    until it has run for about seconds/2.  Step time = per-element quantizer time x all
+    quantized elements + per-MAC GEMM time x all MACs of the step's GEMMs.
+    """
+    import numpy as np
+
+    import oracle
+    from mxfp4_block_scaled_quantize_gb300 import workloads
+
+    wl = workloads.WORKLOADS[workload_name]
+    lin = wl.linears[0]
+    M, N, K = lin.M, lin.N, lin.K
+    t = wl.tensors(0)
+    bits = {k: workloads.bf16_bits(v) for k, v in t.items()}
+    quant = oracle.quantize_dual if lin.train else oracle.quantize_row
+
+    q_elems = q_time = 0.0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds / 2:
+        for k in bits:
+            slab = np.ascontiguousarray(bits[k][:128])
+            s = time.perf_counter()
+            quant(slab)
+            q_time += time.perf_counter() - s
+            q_elems += slab.size
+    xq, xs = oracle.quantize_row(np.ascontiguousarray(bits["X"][:8]))
+    wq, ws = oracle.quantize_row(np.ascontiguousarray(bits["W"][:512]))
+    a = oracle.dequantize(xq, xs)
+    b = oracle.dequantize(wq, ws)
+    g_macs = g_time = 0.0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds / 2:
+        s = time.perf_counter()
+        oracle.gemm_dequantized(a, b, want_abs=False)
+        g_time += time.perf_counter() - s
+        g_macs += a.shape[0] * b.shape[0] * a.shape[1]
+    total_q = M * K + N * K + (M * N if lin.train else 0)
+    total_macs = M * N * K * (3 if lin.train else 1)
+    step_s = q_time / q_elems * total_q + g_time / g_macs * total_macs
+    return {
+        "step_seconds": step_s,
+        "value": lin.flops_step / step_s / 1e12,
+        "sample": (f"oracle {'dual' if lin.train else 'row-only'} quantizer on 128-row slabs of "
+                   f"X, W{', dY' if lin.train else ''} ({int(q_elems)} elements) and fp64 GEMM "
+                   f"on 8x512 output blocks at K={oracle.padded(K)} ({int(g_macs)} MACs); "
+                   f"one full step extrapolated per element / per MAC"),
+        "cores": 1,
+        "kind": "oracle",
+    }
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle.build
+    oracle.build.build()
+    per = max(2.0, args.cpu_baseline_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_sample(args.workload, 0.2)
+    vals = [oracle_sample(args.workload, per) for _ in range(args.steps)]
+    step_s = statistics.mean(v["step_seconds"] for v in vals)
+    value = vals[0]["value"] if len(vals) == 1 else statistics.mean(v["value"] for v in vals)
+    from mxfp4_block_scaled_quantize_gb300 import workloads
+    lin = workloads.WORKLOADS[args.workload].linears[0]
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "M": lin.M, "N": lin.N, "K": lin.K,
+                   "parallelism": "host cores of rank 0"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank, world, local_rank = dist_env()
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        base = oracle_sample(args.workload, args.cpu_baseline_seconds)
+        line["cpu_baseline"] = {"value": base["value"], "unit": "TFLOP/s", "cores": base["cores"],
+                                "kind": "oracle", "sample": base["sample"]}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,131 @@
+/*
+ * mxfp4.h -- C ABI of the GB300 (sm_103a) MXFP4 linear hot path.
+ *
+ * Three operations, all enqueued asynchronously on a caller stream:
+ *   mxfp4_quantize       row-only quantizer (forward-only regions)
+ *   mxfp4_quantize_dual  rowwise + columnwise quantizer from one read of the input
+ *   mxfp4_gemm           block-scaled MXF4 GEMM  C[M,N] = A[M,K] . B[N,K]^T
+ *
+ * Formats (primus_turbo_mxfp4_local.py, `_quantize_mxfp4_dual_fake`, non-shuffled
+ * branch, and module constants MXFP4_BLOCK_SIZE = 32, MXFP4_PADDING_ALIGN_SIZE = 128):
+ *   - Input: bf16 X[M,K], row-major with a row pitch of ldx elements.
+ *   - Kp = ceil(K/128)*128 and Mp = ceil(M/128)*128: only the packed dimension is padded.
+ *   - Row blob of X: elements q[M, Kp/2] (FP4 E2M1, two per byte, element 2j in the low
+ *     nibble of byte j) and one E8M0 scale byte per 32-element block along K.
+ *   - Col blob of X: the row blob of X^T, q[K, Mp/2] plus its scales.  It is what the
+ *     dgrad (dX = dY . W: B = col blob of W) and wgrad (dW = dY^T . X: A = col blob of
+ *     dY, B = col blob of X) GEMMs of `MXFP4LinearFunction.backward` consume.
+ *   - Padding elements are +0 and all-padding blocks have the scale byte 0x00.
+ *   - Quantization rule (OCP MX v1.0 for MXFP4; the pages print no formula): scale
+ *     exponent e = floor(log2(amax)) - 2 clamped to [-127, 127] (byte e + 127; an
+ *     all-zero block gets 0x00), element = round-to-nearest-even of v / 2^e onto
+ *     {0, 0.5, 1, 1.5, 2, 3, 4, 6}, saturating at 6, sign kept (also for zero).
+ *     Inputs must be finite; non-finite inputs give unspecified bytes.
+ *
+ * Scale layouts (mxfp4_scale_layout):
+ *   MXFP4_SCALE_PLAIN  s[R, KB] row-major, R = rows of the blob, KB = (packed dim)/32.
+ *                      Same shape as the pages' non-shuffled scale tensors.
+ *   MXFP4_SCALE_TC     the layout the tcgen05 block-scaled MMA reads: rows padded to a
+ *                      multiple of 128 (padding bytes 0x00), cut into 128-row x 4-block
+ *                      atoms of 512 bytes, atoms ordered block-group fastest
+ *                      (atom = (r/128) * (KB/4) + kb/4); in an atom byte (r, kb) is at
+ *                      (r%32)*16 + ((r%128)/32)*4 + kb%4.  Size ceil(R/128)*128*KB bytes.
+ *                      mxfp4_gemm requires this layout.  It replaces the pages'
+ *                      MI355X preshuffle, which needed extra shuffle launches per GEMM;
+ *                      here the quantizer writes it directly.
+ *
+ * Ownership: the caller allocates every buffer (use mxfp4_quantize_sizes); the library
+ * never allocates, frees or synchronizes on these calls.  Buffers must be device memory
+ * on the current device.
+ *
+ * Errors: argument, alignment and device checks run on the host before anything is
+ * enqueued and return a status without touching the buffers.  Every kernel wait is
+ * bounded; a wait that runs out records a device-side error word that
+ * mxfp4_last_device_error reports.  There is no fallback path: on an unsupported device
+ * the calls fail with MXFP4_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef MXFP4_GB300_H
+#define MXFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL selects the legacy default stream. */
+typedef struct CUstream_st* mxfp4_stream_t;
+
+typedef enum {
+    MXFP4_OK = 0,
+    MXFP4_ERR_INVALID_ARG = 1,        /* a size, pitch, pointer or enum is out of range   */
+    MXFP4_ERR_MISALIGNED = 2,         /* a pointer or pitch breaks the 16-byte rule       */
+    MXFP4_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3    */
+    MXFP4_ERR_CUDA = 4,               /* a CUDA runtime/driver call or a launch failed    */
+    MXFP4_ERR_TIMEOUT = 5             /* a kernel's bounded wait ran out (device word)    */
+} mxfp4_status;
+
+typedef enum { MXFP4_SCALE_PLAIN = 0, MXFP4_SCALE_TC = 1 } mxfp4_scale_layout;
+
+typedef enum { MXFP4_OUT_BF16 = 0, MXFP4_OUT_F32 = 1 } mxfp4_out_dtype;
+
+/* Bytes of the element buffer and of the scale buffer of one blob with `rows` rows and a
+ * packed dimension of logical length `k` (padded to Kp = ceil(k/128)*128):
+ * q_bytes = rows * Kp/2; s_bytes = rows * Kp/32 (PLAIN) or ceil(rows/128)*128 * Kp/32
+ * (TC).  For the row blob of X[M,K] pass (M, K); for the col blob pass (K, M).
+ * Either output pointer may be NULL.  rows, k >= 1, else MXFP4_ERR_INVALID_ARG. */
+mxfp4_status mxfp4_quantize_sizes(int64_t rows, int64_t k, mxfp4_scale_layout layout,
+                                  size_t* q_bytes, size_t* s_bytes);
+
+/* Row-only quantizer: the row blob of X (primus_turbo_mxfp4_local.py calls
+ * `quantize_mxfp4`; the row-only rationale is the "row-only packing" paragraph of Primus
+ * PR #1107: column blobs only feed backward, so forward-only regions skip them).
+ *   x      bf16 X[M,K], row pitch ldx elements (ldx >= K, ldx % 8 == 0), 16-byte aligned
+ *   q_row  out, M * Kp/2 bytes;  s_row  out, scale bytes in `layout`
+ * All of q_row and s_row (padding included) is written.  M, K >= 1. */
+mxfp4_status mxfp4_quantize(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row,
+                            void* s_row, mxfp4_scale_layout layout, mxfp4_stream_t stream);
+
+/* Dual quantizer: row blob and col blob of X from one read of X (primus_turbo_mxfp4_local.py,
+ * `_quantize_mxfp4_dual_op` with every recipe and shuffle flag off; outputs in the order
+ * row_q, row_s, col_q, col_s).
+ *   q_col  out, K * Mp/2 bytes;  s_col  out, col-blob scale bytes in `layout`
+ * Other arguments as mxfp4_quantize. */
+mxfp4_status mxfp4_quantize_dual(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                 void* q_row, void* s_row, void* q_col, void* s_col,
+                                 mxfp4_scale_layout layout, mxfp4_stream_t stream);
+
+/* Block-scaled GEMM C[M,N] = A . B^T over two K-packed blobs (the "TN" form that the
+ * forward, dgrad and wgrad `gemm_fp4_impl` calls of `MXFP4LinearFunction` reduce to):
+ *   a_q  A elements [M, Kp/2];  a_s  A scales, MXFP4_SCALE_TC layout for (M, K)
+ *   b_q  B elements [N, Kp/2];  b_s  B scales, MXFP4_SCALE_TC layout for (N, K)
+ *   K    logical reduction length (Kp = ceil(K/128)*128 is what the blobs hold; padding
+ *        is zero, so the sum over Kp equals the sum over K)
+ *   c    out, C[M,N] row-major with pitch ldc elements (ldc >= N), bf16 or fp32
+ * Products of the dequantized elements accumulate in fp32 on the tensor cores; bf16
+ * output is rounded once, to nearest even.  All pointers 16-byte aligned.  M, N, K >= 1.
+ */
+mxfp4_status mxfp4_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                        int64_t M, int64_t N, int64_t K, void* c, int64_t ldc,
+                        mxfp4_out_dtype out_dtype, mxfp4_stream_t stream);
+
+/* Synchronizes `stream`, then reads and clears the device error word of the current
+ * device: MXFP4_ERR_TIMEOUT if a bounded wait in any kernel of this library ran out
+ * since the last call, MXFP4_ERR_CUDA if the synchronization itself failed, else OK. */
+mxfp4_status mxfp4_last_device_error(mxfp4_stream_t stream);
+
+/* Diagnostic for the bounded-wait machinery: launches one warp that waits on a barrier
+ * nothing ever arrives at, with a limit of timeout_ns (1 .. 10^10 ns).  The wait runs out,
+ * the kernel records the error word and returns, so a following mxfp4_last_device_error
+ * must report MXFP4_ERR_TIMEOUT while the context stays usable. */
+mxfp4_status mxfp4_selftest_bounded_wait(int64_t timeout_ns, mxfp4_stream_t stream);
+
+/* Static, never NULL. */
+const char* mxfp4_status_string(mxfp4_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_GB300_H */

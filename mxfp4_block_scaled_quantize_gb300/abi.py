@@ -1,0 +1,182 @@
+"""Python binding of the C ABI in include/mxfp4.h (argument marshalling only).
+
+Every function named like a C entry point forwards to it through ctypes; buffers may be
+given as torch CUDA tensors or as raw device addresses (int).  PyTorch serves only as the
+allocator and the source of the current stream.  Nothing here computes: if the CUDA
+library is missing, loading raises -- there is no fallback path.
+"""
+import ctypes
+import os
+from typing import Optional, Tuple
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmxfp4_gb300.so")
+
+MXFP4_OK = 0
+MXFP4_ERR_INVALID_ARG = 1
+MXFP4_ERR_MISALIGNED = 2
+MXFP4_ERR_UNSUPPORTED_DEVICE = 3
+MXFP4_ERR_CUDA = 4
+MXFP4_ERR_TIMEOUT = 5
+
+MXFP4_SCALE_PLAIN = 0
+MXFP4_SCALE_TC = 1
+
+MXFP4_OUT_BF16 = 0
+MXFP4_OUT_F32 = 1
+
+EXPORTED = (
+    "mxfp4_quantize_sizes",
+    "mxfp4_quantize",
+    "mxfp4_quantize_dual",
+    "mxfp4_gemm",
+    "mxfp4_last_device_error",
+    "mxfp4_selftest_bounded_wait",
+    "mxfp4_status_string",
+)
+
+
+class Mxfp4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"CUDA library {path} not found: build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    i64, vp, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.mxfp4_quantize_sizes.argtypes = [i64, i64, i32, ctypes.POINTER(ctypes.c_size_t),
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    lib.mxfp4_quantize.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp]
+    lib.mxfp4_quantize_dual.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, vp]
+    lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
+    lib.mxfp4_last_device_error.argtypes = [vp]
+    lib.mxfp4_selftest_bounded_wait.argtypes = [i64, vp]
+    lib.mxfp4_status_string.argtypes = [i32]
+    lib.mxfp4_status_string.restype = ctypes.c_char_p
+    for name in EXPORTED[:-1]:
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def _ptr(buf) -> Optional[int]:
+    if buf is None:
+        return None
+    if isinstance(buf, int):
+        return buf
+    return buf.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str) -> None:
+    if status != MXFP4_OK:
+        raise Mxfp4Error(status, what)
+
+
+def status_string(status: int) -> str:
+    return load().mxfp4_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------------------------------
+# the C entry points
+# ---------------------------------------------------------------------------------------
+def mxfp4_quantize_sizes(rows: int, k: int, layout: int = MXFP4_SCALE_TC) -> Tuple[int, int]:
+    q = ctypes.c_size_t()
+    s = ctypes.c_size_t()
+    _check(load().mxfp4_quantize_sizes(rows, k, layout, ctypes.byref(q), ctypes.byref(s)),
+           "mxfp4_quantize_sizes")
+    return q.value, s.value
+
+
+def mxfp4_quantize(x, M, K, ldx, q_row, s_row, layout=MXFP4_SCALE_TC, stream=None) -> None:
+    _check(load().mxfp4_quantize(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(s_row), layout,
+                                 _stream(stream)), "mxfp4_quantize")
+
+
+def mxfp4_quantize_dual(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=MXFP4_SCALE_TC,
+                        stream=None) -> None:
+    _check(load().mxfp4_quantize_dual(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
+                                      _ptr(s_col), layout, _stream(stream)),
+           "mxfp4_quantize_dual")
+
+
+def mxfp4_gemm(a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype=MXFP4_OUT_BF16, stream=None) -> None:
+    _check(load().mxfp4_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, _ptr(c), ldc,
+                             out_dtype, _stream(stream)), "mxfp4_gemm")
+
+
+def mxfp4_last_device_error(stream=None) -> int:
+    """Returns the status (does not raise): MXFP4_ERR_TIMEOUT if a bounded wait ran out."""
+    return int(load().mxfp4_last_device_error(_stream(stream)))
+
+
+def mxfp4_selftest_bounded_wait(timeout_ns: int, stream=None) -> None:
+    _check(load().mxfp4_selftest_bounded_wait(timeout_ns, _stream(stream)),
+           "mxfp4_selftest_bounded_wait")
+
+
+def mxfp4_status_string(status: int) -> str:
+    return status_string(status)
+
+
+# ---------------------------------------------------------------------------------------
+# allocation helpers (torch as the allocator)
+# ---------------------------------------------------------------------------------------
+def alloc_blob(rows: int, k: int, layout: int = MXFP4_SCALE_TC, device="cuda"):
+    """Uninitialised (q, s) uint8 buffers for one blob of `rows` rows and packed length k;
+    q is shaped [rows, Kp/2], s is [rows, Kp/32] (plain) or flat (tensor-core layout)."""
+    import torch
+    qb, sb = mxfp4_quantize_sizes(rows, k, layout)
+    kp = (k + 127) // 128 * 128
+    q = torch.empty((rows, kp // 2), dtype=torch.uint8, device=device)
+    if layout == MXFP4_SCALE_PLAIN:
+        s = torch.empty((rows, kp // 32), dtype=torch.uint8, device=device)
+    else:
+        s = torch.empty((sb,), dtype=torch.uint8, device=device)
+    assert q.numel() == qb and s.numel() == sb
+    return q, s
+
+
+def quantize(x, dual: bool = True, layout: int = MXFP4_SCALE_TC, stream=None):
+    """bf16 X[M,K] (CUDA, row pitch a multiple of 8) -> (row_q, row_s[, col_q, col_s])."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    rq, rs = alloc_blob(M, K, layout, x.device)
+    if not dual:
+        mxfp4_quantize(x, M, K, x.stride(0), rq, rs, layout, stream)
+        return rq, rs
+    cq, cs = alloc_blob(K, M, layout, x.device)
+    mxfp4_quantize_dual(x, M, K, x.stride(0), rq, rs, cq, cs, layout, stream)
+    return rq, rs, cq, cs
+
+
+def gemm(a_q, a_s, b_q, b_s, M, N, K, out_dtype=None, out=None, stream=None):
+    """C[M,N] = A . B^T from two K-packed blobs with tensor-core-layout scales."""
+    import torch
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a_q.device)
+    code = MXFP4_OUT_F32 if out.dtype == torch.float32 else MXFP4_OUT_BF16
+    assert out.dtype in (torch.float32, torch.bfloat16) and out.stride(1) == 1
+    mxfp4_gemm(a_q, a_s, b_q, b_s, M, N, K, out, out.stride(0), code, stream)
+    return out

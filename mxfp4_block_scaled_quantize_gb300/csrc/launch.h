@@ -1,0 +1,65 @@
+// launch.h -- internal interface between the C ABI (api.cu) and the kernel translation
+// units (quantize.cu, gemm.cu).  Not installed; the public interface is include/mxfp4.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mxfp4 {
+
+// ---- quantizer -------------------------------------------------------------------------
+struct QuantArgs {
+    int64_t M, K;        // logical shape of X
+    int32_t tiles_m;     // ceil(M / 128)
+    int32_t tiles_k;     // ceil(K / 128)
+    uint8_t* q_row;      // [M, Kp/2]
+    uint8_t* s_row;      // row-blob scales
+    uint8_t* q_col;      // [K, Mp/2]   (dual only)
+    uint8_t* s_col;      // col-blob scales (dual only)
+    int64_t ldq_row;     // Kp / 2
+    int64_t ldq_col;     // Mp / 2
+    int64_t kb_row;      // Kp / 32
+    int64_t kb_col;      // Mp / 32
+    int32_t tc_layout;   // 1: tensor-core scale layout, 0: plain
+    uint32_t* err;       // device error word
+};
+
+// Shared memory one quantizer CTA needs, and how many CTAs share an SM.
+size_t quantize_smem_bytes();
+int quantize_ctas_per_sm();
+
+// xmap: bf16 X as a 2-D tensor {K, M} (innermost first), box {128, 128}, no swizzle,
+// out-of-bounds elements read as zero.
+cudaError_t launch_quantize(const CUtensorMap& xmap, const QuantArgs& a, bool dual, int grid,
+                            cudaStream_t stream);
+
+// ---- GEMM ------------------------------------------------------------------------------
+struct GemmArgs {
+    int64_t M, N;        // output shape
+    int32_t tiles_m;     // ceil(M / 128)
+    int32_t tiles_n;     // ceil(N / 256)
+    int32_t k_stages;    // ceil(Kp / 256): 256-element (128-byte) K steps
+    int32_t kb4;         // Kp / 128: 4-block scale groups per row (scale atoms along K)
+    int32_t groups_b;    // ceil(N / 128): 128-row scale groups of B
+    const uint8_t* a_s;  // A scales, tensor-core layout
+    const uint8_t* b_s;  // B scales, tensor-core layout
+    void* c;
+    int64_t ldc;
+    int32_t out_f32;     // 1: fp32 output, 0: bf16
+    uint32_t* err;
+};
+
+size_t gemm_smem_bytes();
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 256;
+
+// amap / bmap: the element blobs as 2-D u8 tensors {Kp/2, rows}, box {128, 128 | 256},
+// 128-byte swizzle, out-of-bounds bytes read as zero.
+cudaError_t launch_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const GemmArgs& g, int grid,
+                        cudaStream_t stream);
+
+// ---- diagnostics -----------------------------------------------------------------------
+cudaError_t launch_selftest_wait(uint32_t* err, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace mxfp4

@@ -1,0 +1,88 @@
+"""The MXFP4 linear layer's data path, Y = X . W^T, as a sequence of C-ABI calls.
+
+Follows the dataflow of `MXFP4LinearFunction` in primus_turbo_mxfp4_local.py with every
+quantization recipe flag off:
+  forward   dual-quantize X and W (row-only when no backward follows, the "row-only
+            packing" of Primus PR #1107), Y = X_row . W_row^T
+  backward  dual-quantize dY, dX = dY_row . (W_col)^T, dW = dY_col . (X_col)^T
+Only the column blobs of X and W need to live from forward to backward; bf16 X and W are
+not kept.  All buffers are allocated once (torch as the allocator) and reused, so a step
+is just six launches on one stream.
+"""
+import torch
+
+from . import abi
+
+
+class MXFP4Linear:
+    def __init__(self, M: int, N: int, K: int, train: bool = True, device="cuda",
+                 out_dtype=torch.bfloat16):
+        self.M, self.N, self.K, self.train = M, N, K, train
+        L = abi.MXFP4_SCALE_TC
+        self.x_row = abi.alloc_blob(M, K, L, device)
+        self.w_row = abi.alloc_blob(N, K, L, device)
+        self.y = torch.empty((M, N), dtype=out_dtype, device=device)
+        if train:
+            self.x_col = abi.alloc_blob(K, M, L, device)
+            self.w_col = abi.alloc_blob(K, N, L, device)
+            self.dy_row = abi.alloc_blob(M, N, L, device)
+            self.dy_col = abi.alloc_blob(N, M, L, device)
+            self.dx = torch.empty((M, K), dtype=out_dtype, device=device)
+            self.dw = torch.empty((N, K), dtype=out_dtype, device=device)
+
+    # -- steps a1..a4 of the path ---------------------------------------------------------
+    def quantize_x(self, x, stream=None):
+        M, K = self.M, self.K
+        if self.train:
+            abi.mxfp4_quantize_dual(x, M, K, x.stride(0), *self.x_row, *self.x_col,
+                                    abi.MXFP4_SCALE_TC, stream)
+        else:
+            abi.mxfp4_quantize(x, M, K, x.stride(0), *self.x_row, abi.MXFP4_SCALE_TC, stream)
+
+    def quantize_w(self, w, stream=None):
+        N, K = self.N, self.K
+        if self.train:
+            abi.mxfp4_quantize_dual(w, N, K, w.stride(0), *self.w_row, *self.w_col,
+                                    abi.MXFP4_SCALE_TC, stream)
+        else:
+            abi.mxfp4_quantize(w, N, K, w.stride(0), *self.w_row, abi.MXFP4_SCALE_TC, stream)
+
+    def quantize_dy(self, dy, stream=None):
+        abi.mxfp4_quantize_dual(dy, self.M, self.N, dy.stride(0), *self.dy_row, *self.dy_col,
+                                abi.MXFP4_SCALE_TC, stream)
+
+    # -- steps a5..a7 ---------------------------------------------------------------------
+    def fwd_gemm(self, stream=None):
+        abi.gemm(*self.x_row, *self.w_row, self.M, self.N, self.K, out=self.y, stream=stream)
+        return self.y
+
+    def dgrad_gemm(self, stream=None):
+        abi.gemm(*self.dy_row, *self.w_col, self.M, self.K, self.N, out=self.dx, stream=stream)
+        return self.dx
+
+    def wgrad_gemm(self, stream=None):
+        abi.gemm(*self.dy_col, *self.x_col, self.N, self.K, self.M, out=self.dw, stream=stream)
+        return self.dw
+
+    # -- a8: the whole step ---------------------------------------------------------------
+    def forward(self, x, w, stream=None):
+        self.quantize_x(x, stream)
+        self.quantize_w(w, stream)
+        return self.fwd_gemm(stream)
+
+    def backward(self, dy, stream=None):
+        assert self.train, "backward needs the column blobs of the dual quantizer"
+        self.quantize_dy(dy, stream)
+        return self.dgrad_gemm(stream), self.wgrad_gemm(stream)
+
+    def step(self, x, w, dy=None, stream=None):
+        y = self.forward(x, w, stream)
+        if not self.train:
+            return (y,)
+        dx, dw = self.backward(dy, stream)
+        return y, dx, dw
+
+    # launches per step (for the benchmark's launch count)
+    @property
+    def launches_per_step(self) -> int:
+        return 6 if self.train else 3

@@ -1,0 +1,69 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every
+function include/mxfp4.h declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from mxfp4_block_scaled_quantize_gb300 import abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return abi.load()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "mxfp4.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxfp4_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == sorted(abi.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", abi.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (mxfp4_[a-z_0-9]+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_sizes_match_the_shape_contract(lib):
+    # [4608, 3072] row blob and col blob, plain and tensor-core scale layouts
+    assert abi.mxfp4_quantize_sizes(4608, 3072, abi.MXFP4_SCALE_PLAIN) == (4608 * 1536, 4608 * 96)
+    assert abi.mxfp4_quantize_sizes(3072, 4600, abi.MXFP4_SCALE_PLAIN) == (3072 * 2304, 3072 * 144)
+    assert abi.mxfp4_quantize_sizes(4600, 3072, abi.MXFP4_SCALE_TC) == (4600 * 1536, 4608 * 96)
+    assert abi.mxfp4_quantize_sizes(1, 1, abi.MXFP4_SCALE_TC) == (64, 128 * 4)
+    for bad in ((0, 1, 0), (1, 0, 0), (-5, 8, 1), (8, 8, 2)):
+        with pytest.raises(abi.Mxfp4Error) as e:
+            abi.mxfp4_quantize_sizes(*bad)
+        assert e.value.status == abi.MXFP4_ERR_INVALID_ARG
+
+
+def test_argument_checks_precede_any_device_use(lib):
+    vp = ctypes.c_void_p
+    assert lib.mxfp4_quantize(None, 4, 4, 8, None, None, 0, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_quantize(16, 4, 16, 8, 32, 48, 0, None) == abi.MXFP4_ERR_INVALID_ARG  # ldx < K
+    assert lib.mxfp4_quantize(18, 4, 8, 8, 32, 48, 0, None) == abi.MXFP4_ERR_MISALIGNED
+    assert lib.mxfp4_quantize(16, 4, 6, 6, 32, 48, 0, None) == abi.MXFP4_ERR_MISALIGNED
+    assert lib.mxfp4_quantize_dual(16, 4, 8, 8, 32, 48, None, 64, 1, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_gemm(16, 32, 48, 64, 4, 4, 4, 80, 2, 0, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_gemm(16, 32, 48, 64, 4, 4, 4, 88, 4, 0, None) == abi.MXFP4_ERR_MISALIGNED
+    assert lib.mxfp4_selftest_bounded_wait(0, None) == abi.MXFP4_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert abi.status_string(code).startswith("MXFP4_")
+    assert "unknown" in abi.status_string(99)

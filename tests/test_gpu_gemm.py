@@ -1,0 +1,167 @@
+"""GPU parity of the block-scaled MXF4 GEMM (fwd, dgrad, wgrad) against the fp64 oracle.
+
+The GPU path quantizes bf16 inputs with its own kernels and multiplies on the tensor
+cores; the oracle quantizes the same bf16 inputs on the CPU and sums dequantized products
+in fp64.  Accuracy contract: see tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp4_block_scaled_quantize_gb300 import abi, workloads
+from mxfp4_block_scaled_quantize_gb300.linear import MXFP4Linear
+from parity import check_gemm
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+
+
+def pitched(x_cpu):
+    """CUDA copy of x with a row pitch rounded up to a multiple of 8 elements."""
+    M, K = x_cpu.shape
+    ld = (K + 7) // 8 * 8
+    wide = torch.zeros((M, ld), dtype=x_cpu.dtype, device="cuda")
+    wide[:, :K] = x_cpu.cuda()
+    return wide[:, :K]
+
+
+def gpu_gemm_from_bf16(a_cpu, b_cpu, out_dtype, ldc=None):
+    """Quantize A[M,K], B[N,K] (row blobs) on the GPU and return C = A.B^T."""
+    M, K = a_cpu.shape
+    N = b_cpu.shape[0]
+    aq, a_s = abi.quantize(pitched(a_cpu), dual=False)
+    bq, b_s = abi.quantize(pitched(b_cpu), dual=False)
+    ldc = ldc or N
+    out = torch.full((M, ldc), float("nan"), dtype=out_dtype, device="cuda")
+    abi.mxfp4_gemm(aq, a_s, bq, b_s, M, N, K, out, ldc,
+                   abi.MXFP4_OUT_F32 if out_dtype == torch.float32 else abi.MXFP4_OUT_BF16)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    return out
+
+
+def oracle_gemm_from_bf16(a_cpu, b_cpu, rows=None):
+    ab, bb = workloads.bf16_bits(a_cpu), workloads.bf16_bits(b_cpu)
+    if rows is not None:
+        ab = np.ascontiguousarray(ab[rows])
+    aq, a_s = oracle.quantize_row(ab)
+    bq, b_s = oracle.quantize_row(bb)
+    return oracle.gemm(aq, a_s, bq, b_s)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_tiny_config_step(out_dtype):
+    wl = workloads.TINY
+    lin = wl.linears[0]
+    t = wl.tensors(0)
+    layer = MXFP4Linear(lin.M, lin.N, lin.K, train=True, out_dtype=out_dtype)
+    y, dx, dw = layer.step(t["X"].cuda(), t["W"].cuda(), t["dY"].cuda())
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    X, W, DY = (oracle.quantize_dual(workloads.bf16_bits(t[k])) for k in ("X", "W", "dY"))
+    c, cabs = oracle.gemm(X[0], X[1], W[0], W[1])
+    check_gemm(y, c, cabs, "tiny fwd")
+    c, cabs = oracle.gemm(DY[0], DY[1], W[2], W[3])
+    check_gemm(dx, c, cabs, "tiny dgrad")
+    c, cabs = oracle.gemm(DY[2], DY[3], X[2], X[3])
+    check_gemm(dw, c, cabs, "tiny wgrad")
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 8, 32), (200, 300, 40), (129, 257, 384),
+                                   (128, 256, 256), (300, 520, 1000), (64, 1000, 4600),
+                                   (256, 128, 128), (384, 768, 640), (513, 255, 2048)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_ragged_shapes(M, N, K, out_dtype):
+    a = workloads.student_t3((M, K), 1.0, M + 3 * N + 7 * K)
+    b = workloads.normal((N, K), 0.5, M + 5 * N + 11 * K)
+    c_gpu = gpu_gemm_from_bf16(a, b, out_dtype)
+    c, cabs = oracle_gemm_from_bf16(a, b)
+    check_gemm(c_gpu, c, cabs, f"gemm {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_output_pitch_and_untouched_tail(out_dtype):
+    M, N, K = 200, 300, 512
+    a = workloads.normal((M, K), 1.0, 1)
+    b = workloads.normal((N, K), 1.0, 2)
+    ldc = N + 13                      # odd pitch: no vector stores possible
+    out = gpu_gemm_from_bf16(a, b, out_dtype, ldc=ldc)
+    assert torch.all(torch.isnan(out[:, N:].float()))   # columns past N untouched
+    c, cabs = oracle_gemm_from_bf16(a, b)
+    check_gemm(out[:, :N], c, cabs, "gemm ldc=N+13")
+
+
+def _sample_rows(M, n=12, seed=0):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([rng.choice(M, n, replace=False), [0, M - 1]]))
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_flux_qkv_forward_sampled(out_dtype):
+    wl = workloads.FLUX_QKV_FWD
+    lin = wl.linears[0]
+    t = wl.tensors(0)
+    layer = MXFP4Linear(lin.M, lin.N, lin.K, train=False, out_dtype=out_dtype)
+    (y,) = layer.step(t["X"].cuda(), t["W"].cuda())
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    rows = _sample_rows(lin.M)
+    c, cabs = oracle_gemm_from_bf16(t["X"], t["W"], rows)
+    check_gemm(y[torch.as_tensor(rows, device="cuda")], c, cabs, "flux qkv fwd")
+
+
+def test_flux_mlp_training_step_sampled():
+    wl = workloads.FLUX_MLP_STEP
+    lin = wl.linears[0]
+    t = wl.tensors(0)
+    layer = MXFP4Linear(lin.M, lin.N, lin.K, train=True)
+    y, dx, dw = layer.step(t["X"].cuda(), t["W"].cuda(), t["dY"].cuda())
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    xb, wb, dyb = (workloads.bf16_bits(t[k]) for k in ("X", "W", "dY"))
+    rows = _sample_rows(lin.M, 8, 1)
+    # fwd: rows of Y need X rows and all of W's row blob
+    aq, a_s = oracle.quantize_row(np.ascontiguousarray(xb[rows]))
+    wq, ws = oracle.quantize_row(wb)
+    c, cabs = oracle.gemm(aq, a_s, wq, ws)
+    check_gemm(y[torch.as_tensor(rows, device="cuda")], c, cabs, "mlp fwd")
+    # dgrad: rows of dX need dY rows and all of W's col blob
+    aq, a_s = oracle.quantize_row(np.ascontiguousarray(dyb[rows]))
+    wcq, wcs = oracle.quantize_col(wb)
+    c, cabs = oracle.gemm(aq, a_s, wcq, wcs)
+    check_gemm(dx[torch.as_tensor(rows, device="cuda")], c, cabs, "mlp dgrad")
+    # wgrad: rows n of dW need column n of dY (its col-blob row) and all of X's col blob
+    nrows = _sample_rows(lin.N, 8, 2)
+    aq, a_s = oracle.quantize_col(np.ascontiguousarray(dyb[:, nrows]))
+    xcq, xcs = oracle.quantize_col(xb)
+    c, cabs = oracle.gemm(aq, a_s, xcq, xcs)
+    check_gemm(dw[torch.as_tensor(nrows, device="cuda")], c, cabs, "mlp wgrad")
+
+
+def test_flux_linear2_forward_long_k_sampled():
+    lin = workloads.FLUX_SINGLE_BLOCK.linears[1]          # K = 15360
+    t = workloads.FLUX_SINGLE_BLOCK.tensors(1)
+    c_gpu = gpu_gemm_from_bf16(t["X"], t["W"], torch.bfloat16)
+    rows = _sample_rows(lin.M, 6, 3)
+    c, cabs = oracle_gemm_from_bf16(t["X"], t["W"], rows)
+    check_gemm(c_gpu[torch.as_tensor(rows, device="cuda")], c, cabs, "linear2 fwd")
+
+
+def test_gemm_argument_errors():
+    lib = abi.load()
+    q, s = abi.alloc_blob(128, 128)
+    c = torch.empty((128, 128), dtype=torch.bfloat16, device="cuda")
+    p = lambda t: t.data_ptr()
+    assert lib.mxfp4_gemm(p(q), p(s), p(q), p(s), 128, 128, 128, p(c), 64, 0, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_gemm(p(q), p(s), p(q), p(s), 128, 128, 0, p(c), 128, 0, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_gemm(p(q) + 8, p(s), p(q), p(s), 128, 128, 128, p(c), 128, 0, None) == abi.MXFP4_ERR_MISALIGNED
+    assert lib.mxfp4_gemm(p(q), p(s), p(q), p(s), 128, 128, 128, p(c), 128, 5, None) == abi.MXFP4_ERR_INVALID_ARG

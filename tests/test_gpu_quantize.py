@@ -1,0 +1,199 @@
+"""GPU parity of the MXFP4 quantizers (row-only and dual) against the CPU oracle.
+
+Every comparison is byte-for-byte, padding and both scale layouts included.  The inputs
+come from the seeded generators in mxfp4_block_scaled_quantize_gb300.workloads.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp4_block_scaled_quantize_gb300 import abi, workloads
+from parity import (assert_bytes_equal, check_quantized_full, check_quantized_sampled)
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+LAYOUTS = [abi.MXFP4_SCALE_PLAIN, abi.MXFP4_SCALE_TC]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    yield
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+
+
+def quant(x_cpu, dual, layout, ldx=None):
+    """Quantize a CPU bf16 tensor on the GPU (optionally from a wider row pitch)."""
+    M, K = x_cpu.shape
+    if ldx is not None and ldx != K:
+        wide = torch.zeros((M, ldx), dtype=torch.bfloat16)
+        wide[:, :K] = x_cpu
+        xg = wide.cuda()[:, :K]
+    else:
+        xg = x_cpu.cuda()
+    outs = abi.quantize(xg, dual=dual, layout=layout)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    return outs
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("name", ["X", "W", "dY"])
+def test_tiny_config_dual(name, layout):
+    t = workloads.TINY.tensors(0)[name]
+    check_quantized_full(t, quant(t, True, layout), layout, True, f"tiny {name}")
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_tiny_config_row_only(layout):
+    t = workloads.TINY.tensors(0)["X"]
+    check_quantized_full(t, quant(t, False, layout), layout, False, "tiny X row-only")
+
+
+def _bits_to_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(bits.astype(np.uint16).view(np.int16)).view(torch.bfloat16)
+
+
+def test_worked_examples():
+    with open(os.path.join(GOLDEN, "mx_worked_examples.json")) as f:
+        cases = json.load(f)["cases"]
+    rows = []
+    for case in cases:
+        vals = np.zeros(32, np.float32)
+        vals[:len(case["values"])] = case["values"]
+        rows.append((vals.view(np.uint32) >> 16).astype(np.uint16))
+    bits = np.stack(rows)                                  # one block per row
+    x = _bits_to_bf16(bits)
+    for layout in LAYOUTS:
+        outs = quant(x, True, layout)
+        check_quantized_full(x, outs, layout, True, "worked examples")
+        rq = outs[0].cpu().numpy()
+        rs = outs[1].cpu().numpy()
+        for i, case in enumerate(cases):
+            s = rs[i, 0] if layout == abi.MXFP4_SCALE_PLAIN else rs[(i % 32) * 16 + (i // 32) * 4]
+            assert s == case["scale"], case["name"]
+            codes = np.empty(32, np.uint8)
+            codes[0::2] = rq[i, :16] & 0xF
+            codes[1::2] = rq[i, :16] >> 4
+            assert list(codes[:len(case["codes"])]) == case["codes"], case["name"]
+
+
+@pytest.mark.parametrize("transpose", [False, True])
+def test_every_finite_bf16_pattern(transpose):
+    b = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    finite = (b & 0x7F80) != 0x7F80
+    b = np.where(finite, b, 0).astype(np.uint16)
+    # mix magnitudes inside blocks: permute with a fixed seed so blocks span many binades
+    rng = np.random.default_rng(7)
+    b = b[rng.permutation(b.size)].reshape(2048, 32)
+    if transpose:
+        b = np.ascontiguousarray(b.T)
+    x = _bits_to_bf16(b)
+    for layout in LAYOUTS:
+        check_quantized_full(x, quant(x, True, layout), layout, True, "all bf16 patterns")
+
+
+def _edge_input(M, K, seed):
+    x = workloads.student_t3((M, K), 1.0, seed)
+    return workloads.inject_edge_blocks(x, seed + 1)
+
+
+@pytest.mark.parametrize("M,K,ldx", [(1, 8, 8), (1, 32, 32), (32, 8, 16), (100, 40, 40),
+                                     (130, 200, 200), (257, 33, 40), (256, 512, 520),
+                                     (128, 128, 128), (129, 129, 136), (640, 384, 384),
+                                     (4600, 256, 256)])
+def test_ragged_shapes(M, K, ldx):
+    x = _edge_input(M, K, M * 7 + K)
+    for layout in LAYOUTS:
+        check_quantized_full(x, quant(x, True, layout, ldx), layout, True, f"dual {M}x{K}")
+        check_quantized_full(x, quant(x, False, layout, ldx), layout, False, f"row {M}x{K}")
+
+
+def test_row_only_equals_row_half_of_dual():
+    x = _edge_input(4608, 3072, 11)
+    r = quant(x, False, abi.MXFP4_SCALE_TC)
+    d = quant(x, True, abi.MXFP4_SCALE_TC)
+    assert torch.equal(r[0], d[0]) and torch.equal(r[1], d[1])
+
+
+def test_outputs_written_exactly():
+    """Guard bytes around every output stay untouched; padding is written (buffers start
+    as 0xA5 garbage)."""
+    M, K = 300, 200
+    x = _edge_input(M, K, 5).cuda()
+    guard = 4096
+    for layout in LAYOUTS:
+        sizes = [abi.mxfp4_quantize_sizes(M, K, layout), abi.mxfp4_quantize_sizes(K, M, layout)]
+        bufs = []
+        for qb, sb in sizes:
+            for nb in (qb, sb):
+                t = torch.full((nb + 2 * guard,), 0xA5, dtype=torch.uint8, device="cuda")
+                bufs.append(t)
+        views = [b[guard:-guard] for b in bufs]
+        abi.mxfp4_quantize_dual(x, M, K, K, views[0], views[1], views[2], views[3], layout)
+        torch.cuda.synchronize()
+        for b in bufs:
+            assert torch.all(b[:guard] == 0xA5) and torch.all(b[-guard:] == 0xA5)
+        Kp, Mp = oracle.padded(K), oracle.padded(M)
+        outs = [views[0].view(M, Kp // 2), views[1], views[2].view(K, Mp // 2), views[3]]
+        if layout == abi.MXFP4_SCALE_PLAIN:
+            outs[1] = outs[1].view(M, Kp // 32)
+            outs[3] = outs[3].view(K, Mp // 32)
+        check_quantized_full(x.cpu(), outs, layout, True, f"guarded layout {layout}")
+
+
+@pytest.mark.parametrize("M,K", [(4608, 3072), (4600, 3072), (4608, 12288), (18432, 3072),
+                                 (4600, 15360)])
+@pytest.mark.parametrize("scale", workloads.SWEEP_SCALE)
+def test_sweep_sampled(M, K, scale):
+    x = workloads.sweep_tensor(M, K, scale)
+    outs = quant(x, True, abi.MXFP4_SCALE_TC)
+    check_quantized_sampled(x, outs, True, f"sweep {M}x{K}x{scale}")
+
+
+def test_sweep_largest_sampled():
+    x = workloads.sweep_tensor(18432, 15360, 1.0)
+    outs = quant(x, True, abi.MXFP4_SCALE_TC)
+    check_quantized_sampled(x, outs, True, "sweep 18432x15360", n_rows=16, n_cols=16)
+
+
+@pytest.mark.parametrize("wname", ["flux12b_qkv_fwd_4608x9216x3072",
+                                   "flux12b_mlp_up_train_step_4608x12288x3072"])
+def test_flux_tensors_sampled(wname):
+    wl = workloads.WORKLOADS[wname]
+    t = wl.tensors(0)
+    dual = wl.linears[0].train
+    for name, x in t.items():
+        check_quantized_sampled(x, quant(x, dual, abi.MXFP4_SCALE_TC), dual, f"{wname} {name}")
+
+
+def test_argument_errors():
+    x = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    q, s = abi.alloc_blob(64, 64)
+    lib = abi.load()
+    st = lib.mxfp4_quantize(x.data_ptr() + 2, 64, 64, 64, q.data_ptr(), s.data_ptr(), 1, None)
+    assert st == abi.MXFP4_ERR_MISALIGNED
+    st = lib.mxfp4_quantize(x.data_ptr(), 64, 60, 60, q.data_ptr(), s.data_ptr(), 1, None)
+    assert st == abi.MXFP4_ERR_MISALIGNED          # row pitch not a multiple of 8
+    st = lib.mxfp4_quantize(x.data_ptr(), 64, 64, 32, q.data_ptr(), s.data_ptr(), 1, None)
+    assert st == abi.MXFP4_ERR_INVALID_ARG         # ldx < K
+    st = lib.mxfp4_quantize(x.data_ptr(), 0, 64, 64, q.data_ptr(), s.data_ptr(), 1, None)
+    assert st == abi.MXFP4_ERR_INVALID_ARG
+    st = lib.mxfp4_quantize(x.data_ptr(), 64, 64, 64, q.data_ptr(), s.data_ptr(), 7, None)
+    assert st == abi.MXFP4_ERR_INVALID_ARG
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    abi.mxfp4_selftest_bounded_wait(20_000_000)     # 20 ms
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_ERR_TIMEOUT
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK   # the word was cleared
+    t = workloads.TINY.tensors(0)["X"]
+    check_quantized_full(t, quant(t, True, abi.MXFP4_SCALE_TC), abi.MXFP4_SCALE_TC, True,
+                         "after timeout")
