@@ -37,6 +37,24 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def reduce_max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """Max of a per-rank float over all ranks of the default process group (the slowest
+    rank sets the job's time).  device: "cpu" for gloo, the rank's GPU for NCCL."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(step_flops: int, steps: int, max_total_ms: float, world: int) -> float:
+    """Weak scaling: every rank runs `steps` steps of the same workload; the job's
+    throughput is all ranks' work over the slowest rank's time."""
+    return world * step_flops * steps / (max_total_ms * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -209,11 +227,7 @@ def run_ours(args, rank, world, local_rank):
 
     per_kernel = [[ev[i].elapsed_time(ev[i + 1]) for ev in events] for i in range(n_k)]
     step_ms = [ev[0].elapsed_time(ev[n_k]) for ev in events]
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = reduce_max_over_ranks(sum(step_ms), world, dev)
 
     # ---- end to end: inputs from pinned host memory, results back to pinned host memory
     hx, hw = t["X"].pin_memory(), t["W"].pin_memory()
@@ -246,11 +260,7 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         e1.synchronize()
         e_ms.append(e0.elapsed_time(e1))
-    e2e_ms = statistics.mean(e_ms)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = reduce_max_over_ranks(statistics.mean(e_ms), world, dev)
 
     if rank != 0:
         return None
@@ -285,8 +295,8 @@ def run_ours(args, rank, world, local_rank):
     quant_gbs = q_bytes / (q_ms * 1e-3) / 1e9
 
     step_flops = lin.flops_step
-    value = world * step_flops * args.steps / (total_ms * 1e-3) / 1e12
-    e2e_value = world * step_flops / (e2e_ms * 1e-3) / 1e12
+    value = whole_job_tflops(step_flops, args.steps, total_ms, world)
+    e2e_value = whole_job_tflops(step_flops, 1, e2e_ms, world)
     traffic = profiled_traffic("gemm_mxf4_kernel")
 
     line = {

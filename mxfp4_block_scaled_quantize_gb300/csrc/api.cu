@@ -96,7 +96,7 @@ mxfp4_status quantize_common(const void* x, int64_t M, int64_t K, int64_t ldx, v
 
     CUtensorMap xmap;
     if (!encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
-                   static_cast<uint64_t>(ldx) * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   static_cast<uint64_t>(ldx) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return MXFP4_ERR_CUDA;
 
     mxfp4::QuantArgs a;

@@ -29,8 +29,8 @@ struct QuantArgs {
 size_t quantize_smem_bytes();
 int quantize_ctas_per_sm();
 
-// xmap: bf16 X as a 2-D tensor {K, M} (innermost first), box {128, 128}, no swizzle,
-// out-of-bounds elements read as zero.
+// xmap: bf16 X as a 2-D tensor {K, M} (innermost first), box {64, 128} with the 128-byte
+// swizzle (a 128 x 128 tile is two boxes), out-of-bounds elements read as zero.
 cudaError_t launch_quantize(const CUtensorMap& xmap, const QuantArgs& a, bool dual, int grid,
                             cudaStream_t stream);
 

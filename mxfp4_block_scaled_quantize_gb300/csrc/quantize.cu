@@ -10,13 +10,18 @@
 // saturated at 6 by the hardware conversion.  The power-of-two scaling is exact in fp32.
 //
 // Design: a persistent grid, one 128 x 128 bf16 tile (32 KB) per step.  One producer
-// thread streams tiles into a 3-stage shared-memory ring with TMA (out-of-bounds rows and
-// columns arrive as zeros, which is exactly the padding rule); 8 consumer warps quantize
-// each tile twice from shared memory -- rowwise with 16-byte vector reads and a 4-lane
-// shuffle amax, columnwise with each thread owning a column pair of one 32-row block --
-// so X is read from HBM once for both packings.  The scale bytes of a tile form exactly
-// one 512-byte atom of the tensor-core scale layout per packing; they are gathered in
-// shared memory and written with 16-byte stores.
+// thread streams tiles into a 3-stage shared-memory ring with TMA, as two 64-column boxes
+// with the 128-byte swizzle (out-of-bounds rows and columns arrive as zeros, which is
+// exactly the padding rule).  8 consumer warps quantize each tile twice from shared
+// memory, so X is read from HBM once for both packings:
+//   rowwise     one thread per 32-element block: four 16-byte reads, an abs-max tree of
+//               packed bf16 maxima, 16 packed fp32x2 multiplies, 16 conversions, one
+//               16-byte store of the codes;
+//   columnwise  one thread per column pair of a 32-row block: 32 4-byte reads, the same
+//               abs-max and conversions with the pair's two scales in one fp32x2 multiply.
+// The swizzle makes both access patterns bank-conflict free.  The scale bytes of a tile
+// form exactly one 512-byte atom of the tensor-core scale layout per packing; they are
+// gathered in shared memory and written with 16-byte stores.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -31,11 +36,10 @@ constexpr int kQConsumerWarps = 8;
 constexpr int kQConsumers = kQConsumerWarps * 32;
 constexpr int kQThreads = kQConsumers + 32;    // + one producer warp
 constexpr int kQTileBytes = kQT * kQT * 2;
-constexpr int kQRowPitch = kQT * 2;            // bytes per tile row in shared memory
 constexpr int kQCtasPerSm = 2;
 
 struct QuantSmem {
-    uint8_t tile[kQStages][kQTileBytes];
+    uint8_t tile[kQStages][kQTileBytes];       // per stage: two 64-column swizzled boxes
     uint8_t atom_row[2][512];
     uint8_t atom_col[2][512];
     uint64_t full[kQStages];
@@ -44,47 +48,104 @@ struct QuantSmem {
     int ok;
 };
 
-__device__ __forceinline__ float lo_f(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+constexpr int kQBoxBytes = kQT * 128;          // 128 rows x 64 bf16 columns
 
-// E8M0 byte of a block from the bit pattern of its largest magnitude (sign cleared).
+// Byte offset of (row r, 16-byte chunk j of the 128-byte box row) under the 128-byte
+// swizzle: chunk j of row r is stored at chunk j ^ (r % 8).
+__device__ __forceinline__ uint32_t swz(int r, int j) { return r * 128 + ((j ^ (r & 7)) << 4); }
+
+// E8M0 byte of a block from the bf16 bit pattern of its largest magnitude (sign ignored):
+// max(expfield - 2, 0).
 __device__ __forceinline__ uint32_t scale_byte(uint32_t amax_bits) {
-    const int ef = static_cast<int>(amax_bits >> 7);
-    return static_cast<uint32_t>(ef > 2 ? ef - 2 : 0);
+    const uint32_t ef = (amax_bits >> 7) & 0xFFu;
+    return max(ef, 2u) - 2u;
 }
 
 // 2^(127 - byte) as fp32: always a normal number for byte in [0, 252].
-__device__ __forceinline__ float inv_scale(uint32_t byte) { return __uint_as_float((254u - byte) << 23); }
+__device__ __forceinline__ uint32_t inv_scale_bits(uint32_t byte) { return (254u - byte) << 23; }
 
-// Two fp32 values -> one byte of two E2M1 codes, `lo` in the low nibble.
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
-    uint32_t r;
-    asm("{\n\t.reg .b8 t;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
-        "cvt.u32.u8 %0, t;\n\t}"
-        : "=r"(r)
-        : "f"(hi), "f"(lo));
-    return r;
+// Magnitude-wise max of two bf16x2 words (the result's signs are not meaningful).
+__device__ __forceinline__ uint32_t absmax2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
-// Sign bits of the two bf16 in w placed at bits 3 and 7 (the sign bits of the byte's two
-// nibbles): negative inputs that round to zero keep their sign as 0x8.
-__device__ __forceinline__ uint32_t sign_pair_lo_hi(uint32_t w) {
-    return ((w >> 12) & 0x8u) | ((w >> 24) & 0x80u);
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
 }
 
-template <bool kSignFix>
-__device__ __forceinline__ uint32_t encode8(const uint4& w, float s) {
-    uint32_t b0 = cvt_e2m1x2(hi_f(w.x) * s, lo_f(w.x) * s);
-    uint32_t b1 = cvt_e2m1x2(hi_f(w.y) * s, lo_f(w.y) * s);
-    uint32_t b2 = cvt_e2m1x2(hi_f(w.z) * s, lo_f(w.z) * s);
-    uint32_t b3 = cvt_e2m1x2(hi_f(w.w) * s, lo_f(w.w) * s);
-    uint32_t q = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-    if (kSignFix) {
-        q |= sign_pair_lo_hi(w.x) | (sign_pair_lo_hi(w.y) << 8) | (sign_pair_lo_hi(w.z) << 16) |
-             (sign_pair_lo_hi(w.w) << 24);
-    }
+// Four words of consecutive bf16 pairs (elements 2k in the low half) times the scale pair
+// `s2` -> four bytes of E2M1 codes, element 2k in the low nibble of byte k.
+__device__ __forceinline__ uint32_t encode8(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                            uint64_t s2) {
+    uint32_t q;
+    asm("{\n\t"
+        ".reg .b32 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+        ".reg .b64 x0, x1, x2, x3;\n\t"
+        ".reg .f32 a0, b0, a1, b1, a2, b2, a3, b3;\n\t"
+        ".reg .b8 t0, t1, t2, t3;\n\t"
+        "shl.b32 l0, %1, 16;\n\tand.b32 h0, %1, 0xFFFF0000;\n\t"
+        "shl.b32 l1, %2, 16;\n\tand.b32 h1, %2, 0xFFFF0000;\n\t"
+        "shl.b32 l2, %3, 16;\n\tand.b32 h2, %3, 0xFFFF0000;\n\t"
+        "shl.b32 l3, %4, 16;\n\tand.b32 h3, %4, 0xFFFF0000;\n\t"
+        "mov.b64 x0, {l0, h0};\n\tmov.b64 x1, {l1, h1};\n\t"
+        "mov.b64 x2, {l2, h2};\n\tmov.b64 x3, {l3, h3};\n\t"
+        "mul.rn.f32x2 x0, x0, %5;\n\tmul.rn.f32x2 x1, x1, %5;\n\t"
+        "mul.rn.f32x2 x2, x2, %5;\n\tmul.rn.f32x2 x3, x3, %5;\n\t"
+        "mov.b64 {a0, b0}, x0;\n\tmov.b64 {a1, b1}, x1;\n\t"
+        "mov.b64 {a2, b2}, x2;\n\tmov.b64 {a3, b3}, x3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, b0, a0;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, b1, a1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, b2, a2;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, b3, a3;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+        : "=r"(q)
+        : "r"(w0), "r"(w1), "r"(w2), "r"(w3), "l"(s2));
     return q;
+}
+
+// Eight words = rows 2j, 2j+1 (j = 0..3) of a column pair (column c0 in the low halves,
+// c1 in the high halves), times the pair's scales `s2` = {s(c0), s(c1)}: four bytes of
+// codes for c0 (*q0) and for c1 (*q1), row 2j in the low nibble of byte j.
+__device__ __forceinline__ void encode_cols8(const uint32_t* w, uint64_t s2, uint32_t* q0,
+                                             uint32_t* q1) {
+    asm("{\n\t"
+        ".reg .b32 l<8>, h<8>;\n\t"
+        ".reg .b64 x<8>;\n\t"
+        ".reg .f32 a<8>, b<8>;\n\t"
+        ".reg .b8 c<4>, d<4>;\n\t"
+        "shl.b32 l0, %2, 16;\n\tand.b32 h0, %2, 0xFFFF0000;\n\t"
+        "shl.b32 l1, %3, 16;\n\tand.b32 h1, %3, 0xFFFF0000;\n\t"
+        "shl.b32 l2, %4, 16;\n\tand.b32 h2, %4, 0xFFFF0000;\n\t"
+        "shl.b32 l3, %5, 16;\n\tand.b32 h3, %5, 0xFFFF0000;\n\t"
+        "shl.b32 l4, %6, 16;\n\tand.b32 h4, %6, 0xFFFF0000;\n\t"
+        "shl.b32 l5, %7, 16;\n\tand.b32 h5, %7, 0xFFFF0000;\n\t"
+        "shl.b32 l6, %8, 16;\n\tand.b32 h6, %8, 0xFFFF0000;\n\t"
+        "shl.b32 l7, %9, 16;\n\tand.b32 h7, %9, 0xFFFF0000;\n\t"
+        "mov.b64 x0, {l0, h0};\n\tmov.b64 x1, {l1, h1};\n\t"
+        "mov.b64 x2, {l2, h2};\n\tmov.b64 x3, {l3, h3};\n\t"
+        "mov.b64 x4, {l4, h4};\n\tmov.b64 x5, {l5, h5};\n\t"
+        "mov.b64 x6, {l6, h6};\n\tmov.b64 x7, {l7, h7};\n\t"
+        "mul.rn.f32x2 x0, x0, %10;\n\tmul.rn.f32x2 x1, x1, %10;\n\t"
+        "mul.rn.f32x2 x2, x2, %10;\n\tmul.rn.f32x2 x3, x3, %10;\n\t"
+        "mul.rn.f32x2 x4, x4, %10;\n\tmul.rn.f32x2 x5, x5, %10;\n\t"
+        "mul.rn.f32x2 x6, x6, %10;\n\tmul.rn.f32x2 x7, x7, %10;\n\t"
+        "mov.b64 {a0, b0}, x0;\n\tmov.b64 {a1, b1}, x1;\n\t"
+        "mov.b64 {a2, b2}, x2;\n\tmov.b64 {a3, b3}, x3;\n\t"
+        "mov.b64 {a4, b4}, x4;\n\tmov.b64 {a5, b5}, x5;\n\t"
+        "mov.b64 {a6, b6}, x6;\n\tmov.b64 {a7, b7}, x7;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c0, a1, a0;\n\tcvt.rn.satfinite.e2m1x2.f32 d0, b1, b0;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c1, a3, a2;\n\tcvt.rn.satfinite.e2m1x2.f32 d1, b3, b2;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c2, a5, a4;\n\tcvt.rn.satfinite.e2m1x2.f32 d2, b5, b4;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c3, a7, a6;\n\tcvt.rn.satfinite.e2m1x2.f32 d3, b7, b6;\n\t"
+        "mov.b32 %0, {c0, c1, c2, c3};\n\t"
+        "mov.b32 %1, {d0, d1, d2, d3};\n\t}"
+        : "=r"(*q0), "=r"(*q1)
+        : "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+          "l"(s2));
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -101,12 +162,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     return v;
 }
 
-template <bool kDual, bool kSignFix>
+template <bool kDual>
 __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantArgs p) {
     extern __shared__ uint8_t smem_raw[];
     QuantSmem& sm = *reinterpret_cast<QuantSmem*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -133,8 +194,10 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
                 if (!mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1, p.err, kErrQuantProducer, &sm.abort))
                     break;
                 const int tm = t / p.tiles_k, tk = t % p.tiles_k;
-                mbar_arrive_expect_tx(smem_addr(&sm.full[s]), kQTileBytes);
-                tma_load_2d(smem_addr(sm.tile[s]), &xmap, tk * kQT, tm * kQT, smem_addr(&sm.full[s]));
+                const uint32_t bar = smem_addr(&sm.full[s]);
+                mbar_arrive_expect_tx(bar, kQTileBytes);
+                tma_load_2d(smem_addr(sm.tile[s]), &xmap, tk * kQT, tm * kQT, bar);
+                tma_load_2d(smem_addr(sm.tile[s]) + kQBoxBytes, &xmap, tk * kQT + 64, tm * kQT, bar);
             }
             // Drain: every armed stage's copy has landed before this thread may leave.
             const int armed = it < kQStages ? it : kQStages;
@@ -162,53 +225,54 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
         const int64_t k0 = static_cast<int64_t>(tk) * kQT;
         const uint32_t tile = smem_addr(sm.tile[s]);
 
-        // ---- rowwise: 2048 chunks of 8 bf16; 4 consecutive chunks form one block
-#pragma unroll 2
-        for (int i = 0; i < (kQT * kQT / 8) / kQConsumers; ++i) {
-            const int id = i * kQConsumers + tid;
-            const int r = id >> 4, c = id & 15;
-            const uint4 w = lds128(tile + r * kQRowPitch + c * 16);
-            uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
-                                  __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
-            m = max(m & 0xFFFFu, m >> 16);
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+        // ---- rowwise: one thread per 32-element block; a quarter-warp covers 8 rows of
+        //      one block column, so its 16-byte reads hit 8 distinct swizzled chunks.
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int bid = i * kQConsumers + tid;
+            const int b = (bid >> 3) & 3;
+            const int r = (bid & 7) + ((bid >> 5) << 3);
+            const uint32_t box = tile + (b >> 1) * kQBoxBytes;
+            const int j0 = (b & 1) * 4;
+            const uint4 v0 = lds128(box + swz(r, j0 + 0));
+            const uint4 v1 = lds128(box + swz(r, j0 + 1));
+            const uint4 v2 = lds128(box + swz(r, j0 + 2));
+            const uint4 v3 = lds128(box + swz(r, j0 + 3));
+            uint32_t m = absmax2(absmax2(absmax2(v0.x, v0.y), absmax2(v0.z, v0.w)),
+                                 absmax2(absmax2(v1.x, v1.y), absmax2(v1.z, v1.w)));
+            m = absmax2(m, absmax2(absmax2(absmax2(v2.x, v2.y), absmax2(v2.z, v2.w)),
+                                   absmax2(absmax2(v3.x, v3.y), absmax2(v3.z, v3.w))));
+            m = absmax2(m, m >> 16);
             const uint32_t byte = scale_byte(m);
-            const uint32_t q = encode8<kSignFix>(w, inv_scale(byte));
+            const uint32_t inv = inv_scale_bits(byte);
+            const uint64_t s2 = pack2(inv, inv);
+            const uint4 q = make_uint4(encode8(v0.x, v0.y, v0.z, v0.w, s2), encode8(v1.x, v1.y, v1.z, v1.w, s2),
+                                       encode8(v2.x, v2.y, v2.z, v2.w, s2), encode8(v3.x, v3.y, v3.z, v3.w, s2));
             const int64_t row = m0 + r;
             if (row < p.M)
-                *reinterpret_cast<uint32_t*>(p.q_row + row * p.ldq_row + (k0 >> 1) + c * 4) = q;
-            if ((c & 3) == 0) {
-                const int cb = c >> 2;
-                const int pos = p.tc_layout ? ((r & 31) * 16 + (r >> 5) * 4 + cb) : (r * 4 + cb);
-                sm.atom_row[buf][pos] = static_cast<uint8_t>(byte);
-            }
+                *reinterpret_cast<uint4*>(p.q_row + row * p.ldq_row + ((k0 + 32 * b) >> 1)) = q;
+            const int pos = p.tc_layout ? ((r & 31) * 16 + (r >> 5) * 4 + b) : (r * 4 + b);
+            sm.atom_row[buf][pos] = static_cast<uint8_t>(byte);
         }
 
-        // ---- columnwise: thread owns columns (2pc, 2pc+1) of the 32-row block rb
+        // ---- columnwise: thread owns columns (2pc, 2pc+1) of the 32-row block rb; a warp
+        //      reads one whole 128-byte swizzled row per load.
         if (kDual) {
             const int pc = tid & 63, rb = tid >> 6;
+            const uint32_t box = tile + (pc >> 5) * kQBoxBytes;
+            const int jc = (pc & 31) >> 2;
+            const uint32_t inner = (pc & 3) * 4;
             uint32_t w[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) w[i] = lds32(tile + (rb * 32 + i) * kQRowPitch + pc * 4);
-            uint32_t m = 0;
+            for (int i = 0; i < 32; ++i) w[i] = lds32(box + swz(rb * 32 + i, jc) + inner);
+            uint32_t m = w[0];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) m = __vmaxu2(m, w[i] & 0x7FFF7FFFu);
-            const uint32_t byte0 = scale_byte(m & 0xFFFFu), byte1 = scale_byte(m >> 16);
-            const float s0 = inv_scale(byte0), s1 = inv_scale(byte1);
-            uint32_t q0[4] = {0, 0, 0, 0}, q1[4] = {0, 0, 0, 0};
+            for (int i = 1; i < 32; ++i) m = absmax2(m, w[i]);
+            const uint32_t byte0 = scale_byte(m), byte1 = scale_byte(m >> 16);
+            const uint64_t s2 = pack2(inv_scale_bits(byte0), inv_scale_bits(byte1));
+            uint32_t q0[4], q1[4];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const uint32_t a = w[2 * j], b = w[2 * j + 1];
-                uint32_t c0 = cvt_e2m1x2(lo_f(b) * s0, lo_f(a) * s0);
-                uint32_t c1 = cvt_e2m1x2(hi_f(b) * s1, hi_f(a) * s1);
-                if (kSignFix) {
-                    c0 |= ((a >> 12) & 0x8u) | ((b >> 8) & 0x80u);
-                    c1 |= ((a >> 28) & 0x8u) | ((b >> 24) & 0x80u);
-                }
-                q0[j >> 2] |= c0 << (8 * (j & 3));
-                q1[j >> 2] |= c1 << (8 * (j & 3));
-            }
+            for (int j = 0; j < 4; ++j) encode_cols8(&w[8 * j], s2, &q0[j], &q1[j]);
             const int64_t kc = k0 + 2 * pc;
             const int64_t off = (m0 + rb * 32) >> 1;
             if (kc < p.K)
@@ -257,26 +321,21 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     }
 }
 
-// Negative values that round to zero must come out as -0 (0x8).  Whether the hardware
-// conversion keeps that sign is checked by the parity tests; the explicit sign merge is
-// exact either way and is kept on.
-constexpr bool kSignFixDefault = true;
-
 }  // namespace
 
-size_t quantize_smem_bytes() { return sizeof(QuantSmem) + 128; }
+size_t quantize_smem_bytes() { return sizeof(QuantSmem) + 1024; }
 int quantize_ctas_per_sm() { return kQCtasPerSm; }
 
 cudaError_t launch_quantize(const CUtensorMap& xmap, const QuantArgs& a, bool dual, int grid,
                             cudaStream_t stream) {
     const size_t smem = quantize_smem_bytes();
     if (dual) {
-        auto k = quantize_kernel<true, kSignFixDefault>;
+        auto k = quantize_kernel<true>;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         k<<<grid, kQThreads, smem, stream>>>(xmap, a);
     } else {
-        auto k = quantize_kernel<false, kSignFixDefault>;
+        auto k = quantize_kernel<false>;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         k<<<grid, kQThreads, smem, stream>>>(xmap, a);
