@@ -67,10 +67,18 @@ def load_peaks():
                 "source": "fallback"}
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {
+    "gemm_mxf4_kernel": ("gemm.cu", "ptx.cuh", "launch.h"),
+    "quantize_kernel": ("quantize.cu", "ptx.cuh", "launch.h"),
+}
+
+
+def kernel_source_hash(kernel):
+    """Hash of the sources a kernel is built from (a profile taken on other sources is
+    stale)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mxfp4_block_scaled_quantize_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -86,7 +94,7 @@ def profiled_traffic(kernel):
     except (OSError, ValueError):
         return None
     ent = t.get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
