@@ -193,6 +193,18 @@ mxfp4_status mxfp4_gemm(const void* a_q, const void* a_s, const void* b_q, const
                    static_cast<uint64_t>(kp / 2), 128, mxfp4::kGemmBN, CU_TENSOR_MAP_SWIZZLE_128B))
         return MXFP4_ERR_CUDA;
 
+    // C goes out through TMA stores when its base and pitch allow a tensor map (16-byte
+    // aligned base, pitch a multiple of 16 bytes); otherwise with plain stores.
+    const int64_t esize = out_dtype == MXFP4_OUT_F32 ? 4 : 2;
+    CUtensorMap cmap;
+    std::memset(&cmap, 0, sizeof(cmap));
+    const bool c_tma = (ldc * esize) % 16 == 0 &&
+                       encode_2d(&cmap, out_dtype == MXFP4_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                 c, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                                 static_cast<uint64_t>(ldc * esize), static_cast<uint32_t>(64 / esize), 32,
+                                 CU_TENSOR_MAP_SWIZZLE_64B);
+
     mxfp4::GemmArgs g;
     g.M = M;
     g.N = N;
@@ -206,11 +218,12 @@ mxfp4_status mxfp4_gemm(const void* a_q, const void* a_s, const void* b_q, const
     g.c = c;
     g.ldc = ldc;
     g.out_f32 = out_dtype == MXFP4_OUT_F32 ? 1 : 0;
+    g.c_tma = c_tma ? 1 : 0;
     g.err = dev->err;
     const int64_t tiles = static_cast<int64_t>(g.tiles_m) * g.tiles_n;
     if (tiles > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;
     const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
-    return mxfp4::launch_gemm(amap, bmap, g, grid, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+    return mxfp4::launch_gemm(amap, bmap, cmap, g, grid, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MXFP4_OK
                : MXFP4_ERR_CUDA;
 }

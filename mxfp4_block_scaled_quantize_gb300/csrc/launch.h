@@ -47,6 +47,7 @@ struct GemmArgs {
     void* c;
     int64_t ldc;
     int32_t out_f32;     // 1: fp32 output, 0: bf16
+    int32_t c_tma;       // 1: cmap describes C (TMA stores), 0: plain stores
     uint32_t* err;
 };
 
@@ -55,9 +56,10 @@ constexpr int kGemmBM = 128;
 constexpr int kGemmBN = 256;
 
 // amap / bmap: the element blobs as 2-D u8 tensors {Kp/2, rows}, box {128, 128 | 256},
-// 128-byte swizzle, out-of-bounds bytes read as zero.
-cudaError_t launch_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const GemmArgs& g, int grid,
-                        cudaStream_t stream);
+// 128-byte swizzle, out-of-bounds bytes read as zero.  cmap (used when g.c_tma): C as a
+// 2-D {N, M} tensor of its output type, box {64 bytes of columns, 32 rows}, 64-byte swizzle.
+cudaError_t launch_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& cmap,
+                        const GemmArgs& g, int grid, cudaStream_t stream);
 
 // ---- diagnostics -----------------------------------------------------------------------
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t timeout_ns, cudaStream_t stream);

@@ -19,9 +19,9 @@
 //               16-byte store of the codes;
 //   columnwise  one thread per column pair of a 32-row block: 32 4-byte reads, the same
 //               abs-max and conversions with the pair's two scales in one fp32x2 multiply.
-// The swizzle makes both access patterns bank-conflict free.  The scale bytes of a tile
-// form exactly one 512-byte atom of the tensor-core scale layout per packing; they are
-// gathered in shared memory and written with 16-byte stores.
+// The swizzle makes both access patterns bank-conflict free.  Consumer warps never wait
+// for each other: each warp waits for the stage itself, stores its codes and scale bytes
+// straight to global memory, and releases the stage with its own barrier arrival.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -40,12 +40,9 @@ constexpr int kQCtasPerSm = 2;
 
 struct QuantSmem {
     uint8_t tile[kQStages][kQTileBytes];       // per stage: two 64-column swizzled boxes
-    uint8_t atom_row[2][512];
-    uint8_t atom_col[2][512];
     uint64_t full[kQStages];
-    uint64_t empty[kQStages];
+    uint64_t empty[kQStages];                  // one arrival per consumer warp
     int abort;
-    int ok;
 };
 
 constexpr int kQBoxBytes = kQT * 128;          // 128 rows x 64 bf16 columns
@@ -176,7 +173,7 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     if (tid == 0) {
         for (int s = 0; s < kQStages; ++s) {
             mbar_init(smem_addr(&sm.full[s]), 1);
-            mbar_init(smem_addr(&sm.empty[s]), 1);
+            mbar_init(smem_addr(&sm.empty[s]), kQConsumerWarps);
         }
         sm.abort = 0;
         fence_barrier_init();
@@ -210,20 +207,22 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     }
 
     // ------------------------------------------------------------------ consumers
+    const uint32_t lane = lane_id();
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
         const int s = it % kQStages;
         const uint32_t ph = (it / kQStages) & 1;
-        const int buf = it & 1;
-        if (tid == 0)
-            sm.ok = mbar_wait(smem_addr(&sm.full[s]), ph, p.err, kErrQuantConsumer, &sm.abort) ? 1 : 0;
-        named_barrier(1, kQConsumers);
-        if (!*reinterpret_cast<volatile int*>(&sm.ok)) break;
+        int ok = 0;
+        if (lane == 0) ok = mbar_wait(smem_addr(&sm.full[s]), ph, p.err, kErrQuantConsumer, &sm.abort) ? 1 : 0;
+        if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
 
         const int tm = t / p.tiles_k, tk = t % p.tiles_k;
         const int64_t m0 = static_cast<int64_t>(tm) * kQT;
         const int64_t k0 = static_cast<int64_t>(tk) * kQT;
         const uint32_t tile = smem_addr(sm.tile[s]);
+        // Tensor-core layout: this tile's scales are exactly one 512-byte atom per packing.
+        uint8_t* const atom_row = p.s_row + (static_cast<int64_t>(tm) * (p.kb_row >> 2) + tk) * 512;
+        uint8_t* const atom_col = kDual ? p.s_col + (static_cast<int64_t>(tk) * (p.kb_col >> 2) + tm) * 512 : nullptr;
 
         // ---- rowwise: one thread per 32-element block; a quarter-warp covers 8 rows of
         //      one block column, so its 16-byte reads hit 8 distinct swizzled chunks.
@@ -249,10 +248,12 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
             const uint4 q = make_uint4(encode8(v0.x, v0.y, v0.z, v0.w, s2), encode8(v1.x, v1.y, v1.z, v1.w, s2),
                                        encode8(v2.x, v2.y, v2.z, v2.w, s2), encode8(v3.x, v3.y, v3.z, v3.w, s2));
             const int64_t row = m0 + r;
-            if (row < p.M)
+            if (row < p.M) {
                 *reinterpret_cast<uint4*>(p.q_row + row * p.ldq_row + ((k0 + 32 * b) >> 1)) = q;
-            const int pos = p.tc_layout ? ((r & 31) * 16 + (r >> 5) * 4 + b) : (r * 4 + b);
-            sm.atom_row[buf][pos] = static_cast<uint8_t>(byte);
+                if (!p.tc_layout) p.s_row[row * p.kb_row + (k0 >> 5) + b] = static_cast<uint8_t>(byte);
+            }
+            // Padding rows of the tensor-core layout get their (zero) byte too.
+            if (p.tc_layout) atom_row[(r & 31) * 16 + (r >> 5) * 4 + b] = static_cast<uint8_t>(byte);
         }
 
         // ---- columnwise: thread owns columns (2pc, 2pc+1) of the 32-row block rb; a warp
@@ -275,49 +276,25 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
             for (int j = 0; j < 4; ++j) encode_cols8(&w[8 * j], s2, &q0[j], &q1[j]);
             const int64_t kc = k0 + 2 * pc;
             const int64_t off = (m0 + rb * 32) >> 1;
-            if (kc < p.K)
-                *reinterpret_cast<uint4*>(p.q_col + kc * p.ldq_col + off) =
-                    make_uint4(q0[0], q0[1], q0[2], q0[3]);
-            if (kc + 1 < p.K)
+            if (kc < p.K) {
+                *reinterpret_cast<uint4*>(p.q_col + kc * p.ldq_col + off) = make_uint4(q0[0], q0[1], q0[2], q0[3]);
+                if (!p.tc_layout) p.s_col[kc * p.kb_col + (m0 >> 5) + rb] = static_cast<uint8_t>(byte0);
+            }
+            if (kc + 1 < p.K) {
                 *reinterpret_cast<uint4*>(p.q_col + (kc + 1) * p.ldq_col + off) =
                     make_uint4(q1[0], q1[1], q1[2], q1[3]);
-            const int kl0 = 2 * pc, kl1 = 2 * pc + 1;
+                if (!p.tc_layout) p.s_col[(kc + 1) * p.kb_col + (m0 >> 5) + rb] = static_cast<uint8_t>(byte1);
+            }
             if (p.tc_layout) {
-                sm.atom_col[buf][(kl0 & 31) * 16 + (kl0 >> 5) * 4 + rb] = static_cast<uint8_t>(byte0);
-                sm.atom_col[buf][(kl1 & 31) * 16 + (kl1 >> 5) * 4 + rb] = static_cast<uint8_t>(byte1);
-            } else {
-                sm.atom_col[buf][kl0 * 4 + rb] = static_cast<uint8_t>(byte0);
-                sm.atom_col[buf][kl1 * 4 + rb] = static_cast<uint8_t>(byte1);
+                const int kl0 = 2 * pc, kl1 = 2 * pc + 1;
+                atom_col[(kl0 & 31) * 16 + (kl0 >> 5) * 4 + rb] = static_cast<uint8_t>(byte0);
+                atom_col[(kl1 & 31) * 16 + (kl1 >> 5) * 4 + rb] = static_cast<uint8_t>(byte1);
             }
         }
 
-        // All reads of the stage and all scale bytes of the tile are done.
-        named_barrier(1, kQConsumers);
-        if (tid == 0) mbar_arrive(smem_addr(&sm.empty[s]));
-
-        if (p.tc_layout) {
-            if (tid < 32) {
-                const int64_t atom = static_cast<int64_t>(tm) * (p.kb_row >> 2) + tk;
-                *reinterpret_cast<uint4*>(p.s_row + atom * 512 + tid * 16) =
-                    *reinterpret_cast<const uint4*>(&sm.atom_row[buf][tid * 16]);
-            } else if (kDual && tid < 64) {
-                const int64_t atom = static_cast<int64_t>(tk) * (p.kb_col >> 2) + tm;
-                *reinterpret_cast<uint4*>(p.s_col + atom * 512 + (tid - 32) * 16) =
-                    *reinterpret_cast<const uint4*>(&sm.atom_col[buf][(tid - 32) * 16]);
-            }
-        } else {
-            if (tid < kQT) {
-                const int64_t row = m0 + tid;
-                if (row < p.M)
-                    *reinterpret_cast<uint32_t*>(p.s_row + row * p.kb_row + (k0 >> 5)) =
-                        *reinterpret_cast<const uint32_t*>(&sm.atom_row[buf][tid * 4]);
-            } else if (kDual) {
-                const int64_t kr = k0 + (tid - kQT);
-                if (kr < p.K)
-                    *reinterpret_cast<uint32_t*>(p.s_col + kr * p.kb_col + (m0 >> 5)) =
-                        *reinterpret_cast<const uint32_t*>(&sm.atom_col[buf][(tid - kQT) * 4]);
-            }
-        }
+        // This warp is done with the stage.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[s]));
     }
 }
 
