@@ -220,12 +220,32 @@ mxfp4_status mxfp4_gemm(const void* a_q, const void* a_s, const void* b_q, const
     g.out_f32 = out_dtype == MXFP4_OUT_F32 ? 1 : 0;
     g.c_tma = c_tma ? 1 : 0;
     g.err = dev->err;
+    g.tiles_m2 = static_cast<int32_t>(cdiv(M, 256));
     const int64_t tiles = static_cast<int64_t>(g.tiles_m) * g.tiles_n;
     if (tiles > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    // More than one 128-row tile: 256 x 256 tiles on CTA pairs.
+    const int max_clusters = M > mxfp4::kGemmBM ? mxfp4::gemm_pair_max_clusters() : 0;
+    if (max_clusters > 0) {
+        CUtensorMap bmap2, sfamap, sfbmap;
+        if (!encode_2d(&bmap2, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_q, static_cast<uint64_t>(kp / 2),
+                       static_cast<uint64_t>(N), static_cast<uint64_t>(kp / 2), 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&sfamap, CU_TENSOR_MAP_DATA_TYPE_UINT64, a_s, static_cast<uint64_t>(g.kb4) * 64,
+                       static_cast<uint64_t>(cdiv(M, 128)), static_cast<uint64_t>(g.kb4) * 512, 128, 1,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !encode_2d(&sfbmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, b_s, static_cast<uint64_t>(g.kb4) * 64,
+                       static_cast<uint64_t>(cdiv(N, 128)), static_cast<uint64_t>(g.kb4) * 512, 128, 2,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+            return MXFP4_ERR_CUDA;
+        const int64_t pair_tiles = static_cast<int64_t>(g.tiles_m2) * g.tiles_n;
+        const int clusters = static_cast<int>(pair_tiles < max_clusters ? pair_tiles : max_clusters);
+        return mxfp4::launch_gemm_pair(amap, bmap2, cmap, sfamap, sfbmap, g, clusters, s) == cudaSuccess
+                   ? MXFP4_OK
+                   : MXFP4_ERR_CUDA;
+    }
     const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
-    return mxfp4::launch_gemm(amap, bmap, cmap, g, grid, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? MXFP4_OK
-               : MXFP4_ERR_CUDA;
+    return mxfp4::launch_gemm(amap, bmap, cmap, g, grid, s) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
 
 mxfp4_status mxfp4_last_device_error(mxfp4_stream_t stream) {

@@ -1,0 +1,362 @@
+// gemm_pair.cu -- the block-scaled MXF4 GEMM on CTA pairs (tcgen05 cta_group::2).
+//
+// Same operation and operands as gemm.cu (C = A . B^T on K-packed MXFP4 blobs with scales
+// in the tensor-core layout, fp32 accumulation, fp32 or bf16 out), for problems with more
+// than one 128-row tile.  A cluster of two CTAs on neighbouring SMs owns 256 x 256 output
+// tiles: each CTA holds the A rows of its own 128-row half and half of the tile's B rows,
+// and one 256 x 256 x 64 MMA issued by the even CTA reads both CTAs' shared memory.  Per
+// SM that is 35 KB of operands per 256-element K step instead of 51 KB for a 128 x 256
+// tile on one SM, so the same shared memory holds five stages instead of four and L2
+// feeds a third fewer bytes per flop.
+//
+// Layout facts this relies on (measured on the part: each CTA's scale copy lands in its
+// own TMEM from its own shared memory, and each SM reads all N B-scales from its own TMEM):
+//   - every CTA loads the A scales of its own rows and the B scales of all 256 tile rows;
+//   - all loads of a stage, from both CTAs, complete on the even CTA's `full` barrier;
+//   - the MMA's commit arrives on `empty` / `tmem_full` in both CTAs (multicast).
+//
+// Roles (both CTAs run the same code; `leader` is the even CTA):
+//   warp 0      producer, both CTAs: per K step, its A half (128 rows x 128 bytes), its B
+//               half (128 x 128), its A scales (1 KB) and all B scales (2 KB) by TMA.
+//   warp 1      TMEM allocation for the pair (512 columns, same address in both CTAs); in
+//               the leader, the MMA issuer (one elected lane of a converged warp).
+//   warp 2      leader only: waits on the barriers for the MMA warp, named-barrier hand-over.
+//   warps 3..10 epilogue, both CTAs: the CTA's own 128 accumulator rows, as in gemm.cu;
+//               each warp reports the accumulator read to the leader's `tmem_empty`.
+// Every mbarrier wait is bounded; on a timeout the CTA stops its loops, and both CTAs
+// still meet at the final cluster barrier, so neither leaves while the other may touch
+// its shared memory.
+#include <cuda_bf16.h>
+
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace mxfp4 {
+namespace {
+
+constexpr int BKB = 128;                  // bytes of K per stage (256 FP4 elements)
+constexpr int kStages = 5;
+constexpr int kABytes = 128 * BKB;        // this CTA's 128 A rows
+constexpr int kBBytes = 128 * BKB;        // this CTA's 128 of the tile's 256 B rows
+constexpr int kSfaBytes = 2 * 512;        // 2 scale atoms of this CTA's rows
+constexpr int kSfbBytes = 2 * 2 * 512;    // 2 atoms x both 128-row groups of B
+constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+constexpr int kEpiWarps = 8;
+constexpr int kEpi0 = 3;
+constexpr int kThreads = (kEpi0 + kEpiWarps) * 32;
+constexpr uint32_t kBarHandoff = 1;
+constexpr uint32_t kBarEpilogue = 2;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfTmemBase = 256;
+constexpr uint32_t kSfTmemPerStage = 24;
+constexpr int kOutRowBytes = 64;
+constexpr int kOutBytes = 32 * kOutRowBytes;
+
+struct PairSmem {
+    uint8_t a[kStages][kABytes];          // 1024-byte aligned (128-byte swizzle atoms)
+    uint8_t b[kStages][kBBytes];
+    uint8_t sfa[kStages][kSfaBytes];
+    uint8_t sfb[kStages][kSfbBytes];
+    uint8_t out[kEpiWarps][kOutBytes];
+    uint64_t full[kStages];               // used in the leader: both CTAs' bytes
+    uint64_t empty[kStages];              // each CTA: the leader's MMA commit
+    uint64_t tmem_full;                   // each CTA: the leader's commit after a tile
+    uint64_t tmem_empty;                  // used in the leader: 2 x kEpiWarps arrivals
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// tcgen05.mma kind::mxf4 instruction descriptor, M = 256 (the pair), N = 256.
+__device__ __forceinline__ uint32_t pair_idesc(uint32_t sf_id) {
+    uint32_t d = 0;
+    d |= sf_id << 4;
+    d |= 1u << 7;
+    d |= 1u << 10;
+    d |= static_cast<uint32_t>(256 >> 3) << 17;
+    d |= 1u << 23;
+    d |= static_cast<uint32_t>(256 >> 4) << 24;
+    d |= sf_id << 29;
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t j) {
+    return r * kOutRowBytes + ((j ^ ((r >> 1) & 3u)) << 4);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+                          const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap sfamap,
+                          const __grid_constant__ CUtensorMap sfbmap, const GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    PairSmem& sm = *reinterpret_cast<PairSmem*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const uint32_t lane = lane_id();
+    const uint32_t rank = cluster_cta_rank();
+    const bool leader = rank == 0;
+    const int cluster = blockIdx.x >> 1;
+    const int nclusters = gridDim.x >> 1;
+    const int num_tiles = g.tiles_m2 * g.tiles_n;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_addr(&sm.full[s]), 1);
+            mbar_init(smem_addr(&sm.empty[s]), 1);
+        }
+        mbar_init(smem_addr(&sm.tmem_full), 1);
+        mbar_init(smem_addr(&sm.tmem_empty), 2 * kEpiWarps);
+        mbar_init(smem_addr(&sm.drain), 1);
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(&sm.tmem_base), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();   // both CTAs' barriers exist before anything signals across
+    tc_fence_after_sync();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensormap(&amap);
+            prefetch_tensormap(&bmap);
+            prefetch_tensormap(&sfamap);
+            prefetch_tensormap(&sfbmap);
+            const uint64_t pol = l2_policy_evict_last();
+            int it = 0;
+            bool ok = true;
+            for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+                const int mt2 = t % g.tiles_m2, nt = t / g.tiles_m2;
+                const int arow = mt2 * 256 + static_cast<int>(rank) * 128;
+                const int brow = nt * 256 + static_cast<int>(rank) * 128;
+                for (int ks = 0; ks < g.k_stages; ++ks, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    if (!mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1, g.err, kErrGemmProducer, &sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(smem_addr(&sm.full[s]), 2 * kStageBytes);
+                    const uint32_t bar = cluster_map(smem_addr(&sm.full[s]), 0);
+                    tma_load_2d_pair(smem_addr(sm.a[s]), &amap, ks * BKB, arow, bar, pol);
+                    tma_load_2d_pair(smem_addr(sm.b[s]), &bmap, ks * BKB, brow, bar, pol);
+                    // Scale maps count 8-byte units: 2 atoms = 128 units per K step.
+                    tma_load_2d_pair(smem_addr(sm.sfa[s]), &sfamap, ks * 128, 2 * mt2 + static_cast<int>(rank),
+                                     bar, pol);
+                    tma_load_2d_pair(smem_addr(sm.sfb[s]), &sfbmap, ks * 128, 2 * nt, bar, pol);
+                }
+            }
+            // Drain (leader): every armed stage, both CTAs' bytes, has landed.
+            if (leader) {
+                const int armed = it < kStages ? it : kStages;
+                for (int i = 1; i <= armed; ++i) {
+                    const int j = it - i;
+                    mbar_wait_quiet(smem_addr(&sm.full[j % kStages]), (j / kStages) & 1, kWaitLimitNs);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (leader) {
+            int it = 0;
+            bool ok = true;
+            for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+                for (int ks = 0; ks < g.k_stages; ++ks, ++it) {
+                    if (!named_barrier_and(kBarHandoff, 64, true)) {
+                        ok = false;
+                        break;
+                    }
+                    if (elect_one()) {
+                        tc_fence_after_sync();
+                        const int s = it % kStages;
+                        const int natoms = min(2, g.kb4 - 2 * ks);
+                        const uint32_t sf = tmem + kSfTmemBase + s * kSfTmemPerStage;
+                        const uint32_t sfa_s = smem_addr(sm.sfa[s]);
+                        const uint32_t sfb_s = smem_addr(sm.sfb[s]);
+                        for (int a = 0; a < natoms; ++a) {
+                            tc_cp_32x128b_warpx4_pair(sf + a * 4, smem_desc(sfa_s + a * 512, 0, 128, 0));
+                            tc_cp_32x128b_warpx4_pair(sf + 8 + a * 8, smem_desc(sfb_s + a * 512, 0, 128, 0));
+                            tc_cp_32x128b_warpx4_pair(sf + 8 + a * 8 + 4,
+                                                      smem_desc(sfb_s + 1024 + a * 512, 0, 128, 0));
+                        }
+                        const uint64_t adesc = smem_desc(smem_addr(sm.a[s]), 16, 1024, 2);
+                        const uint64_t bdesc = smem_desc(smem_addr(sm.b[s]), 16, 1024, 2);
+                        for (int j = 0; j < natoms * 2; ++j) {
+                            const uint32_t sf_id = (j & 1) * 2;
+                            tc_mma_mxf4_pair(tmem, adesc + 2 * j, bdesc + 2 * j, pair_idesc(sf_id),
+                                             sf + (j >> 1) * 4, sf + 8 + (j >> 1) * 8, (ks | j) != 0);
+                        }
+                        tc_commit_pair_multicast(smem_addr(&sm.empty[s]), 3);
+                        if (ks == g.k_stages - 1) tc_commit_pair_multicast(smem_addr(&sm.tmem_full), 3);
+                    }
+                }
+            }
+            if (elect_one()) {
+                tc_commit_pair_multicast(smem_addr(&sm.drain), 1);
+                if (!mbar_wait_quiet(smem_addr(&sm.drain), 0, kWaitLimitNs)) atomicOr(g.err, kErrGemmDrain);
+            }
+            __syncwarp();
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------------ MMA waiter
+        if (leader) {
+            int it = 0, tl = 0;
+            bool ok = true;
+            for (int t = cluster; t < num_tiles && ok; t += nclusters, ++tl) {
+                for (int ks = 0; ks < g.k_stages; ++ks, ++it) {
+                    int w = 1;
+                    if (lane == 0) {
+                        if (ks == 0 && tl > 0)
+                            w = mbar_wait(smem_addr(&sm.tmem_empty), (tl - 1) & 1, g.err, kErrGemmMma, &sm.abort);
+                        if (w)
+                            w = mbar_wait(smem_addr(&sm.full[it % kStages]), (it / kStages) & 1, g.err,
+                                          kErrGemmMma, &sm.abort);
+                    }
+                    if (!named_barrier_and(kBarHandoff, 64, __shfl_sync(0xFFFFFFFFu, w, 0) != 0)) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------------ epilogue
+        const int q = warp & 3;
+        const int h = (warp - kEpi0) >> 2;
+        const uint32_t obuf = smem_addr(sm.out[warp - kEpi0]);
+        const uint64_t pol = l2_policy_evict_first();
+        const uint32_t leader_tmem_empty = cluster_map(smem_addr(&sm.tmem_empty), 0);
+        if (g.c_tma && lane == 0) prefetch_tensormap(&cmap);
+        int tl = 0;
+        for (int t = cluster; t < num_tiles; t += nclusters, ++tl) {
+            int okw = 1;
+            if (warp == kEpi0 && lane == 0)
+                okw = mbar_wait(smem_addr(&sm.tmem_full), tl & 1, g.err, kErrGemmEpilogue, &sm.abort);
+            if (!named_barrier_and(kBarEpilogue, kEpiWarps * 32, __shfl_sync(0xFFFFFFFFu, okw, 0) != 0)) break;
+            tc_fence_after_sync();
+            uint32_t v[4][32];
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
+            tc_ld_32x32b_x32(taddr + 0, v[0]);
+            tc_ld_32x32b_x32(taddr + 32, v[1]);
+            tc_ld_32x32b_x32(taddr + 64, v[2]);
+            tc_ld_32x32b_x32(taddr + 96, v[3]);
+            tc_wait_ld();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+
+            const int mt2 = t % g.tiles_m2, nt = t / g.tiles_m2;
+            const int64_t row0 = static_cast<int64_t>(mt2) * 256 + rank * 128 + q * 32;
+            const int64_t col0 = static_cast<int64_t>(nt) * 256 + h * 128;
+            if (row0 >= g.M || col0 >= g.N) continue;
+            if (g.c_tma) {
+                const int per = g.out_f32 ? 16 : 32;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    if (c * per >= 128 || col0 + c * per >= g.N) break;
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                    uint32_t w[16];
+                    if (g.out_f32) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = v[(c >> 1) & 3][(c & 1) * 16 + i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[c & 3][2 * i], v[c & 3][2 * i + 1]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        sts128(obuf + swz64(lane, j), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d_hint(&cmap, static_cast<int32_t>(col0 + c * per), static_cast<int32_t>(row0),
+                                          obuf, pol);
+                        bulk_commit_group();
+                    }
+                }
+                continue;
+            }
+            const int64_t row = row0 + lane;
+            if (row >= g.M) continue;
+            if (!g.out_f32) {
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g.c) + row * g.ldc + col0;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = __float2bfloat16_rn(__uint_as_float(v[c4][j]));
+            } else {
+                float* dst = reinterpret_cast<float*>(g.c) + row * g.ldc + col0;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = __uint_as_float(v[c4][j]);
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();   // no CTA leaves or frees TMEM while its peer may still use it
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t gemm_pair_smem_bytes() { return sizeof(PairSmem) + 1024; }
+
+int gemm_pair_max_clusters() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] > 0) return cached[dev];
+    const size_t smem = gemm_pair_smem_bytes();
+    if (cudaFuncSetAttribute(gemm_mxf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel, &cfg) != cudaSuccess) return 0;
+    cached[dev] = n;
+    return n;
+}
+
+cudaError_t launch_gemm_pair(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& cmap,
+                             const CUtensorMap& sfamap, const CUtensorMap& sfbmap, const GemmArgs& g,
+                             int clusters, cudaStream_t stream) {
+    const size_t smem = gemm_pair_smem_bytes();
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_mxf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    gemm_mxf4_pair_kernel<<<2 * clusters, kThreads, smem, stream>>>(amap, bmap, cmap, sfamap, sfbmap, g);
+    return cudaGetLastError();
+}
+
+}  // namespace mxfp4

@@ -39,6 +39,7 @@ struct GemmArgs {
     int64_t M, N;        // output shape
     int32_t tiles_m;     // ceil(M / 128)
     int32_t tiles_n;     // ceil(N / 256)
+    int32_t tiles_m2;    // ceil(M / 256): row tiles of the CTA-pair kernel
     int32_t k_stages;    // ceil(Kp / 256): 256-element (128-byte) K steps
     int32_t kb4;         // Kp / 128: 4-block scale groups per row (scale atoms along K)
     int32_t groups_b;    // ceil(N / 128): 128-row scale groups of B
@@ -60,6 +61,15 @@ constexpr int kGemmBN = 256;
 // 2-D {N, M} tensor of its output type, box {64 bytes of columns, 32 rows}, 64-byte swizzle.
 cudaError_t launch_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& cmap,
                         const GemmArgs& g, int grid, cudaStream_t stream);
+
+// The CTA-pair kernel (gemm_pair.cu): 256 x 256 tiles on clusters of two CTAs.  sfamap /
+// sfbmap: the A / B scale blobs as 2-D u64 tensors {Kp/128 * 64, ceil(rows/128)} (one row
+// per 128-row group of atoms), boxes {128, 1} / {128, 2}.  `clusters` CTA pairs.
+size_t gemm_pair_smem_bytes();
+int gemm_pair_max_clusters();   // co-resident clusters of the pair kernel, 0 if none
+cudaError_t launch_gemm_pair(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& cmap,
+                             const CUtensorMap& sfamap, const CUtensorMap& sfbmap, const GemmArgs& g,
+                             int clusters, cudaStream_t stream);
 
 // ---- diagnostics -----------------------------------------------------------------------
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t timeout_ns, cudaStream_t stream);
