@@ -131,6 +131,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync_all();   // both CTAs' barriers exist before anything signals across
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
+    grid_launch_dependents();
+    grid_wait_prerequisites();
 
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
@@ -355,8 +357,17 @@ cudaError_t launch_gemm_pair(const CUtensorMap& amap, const CUtensorMap& bmap, c
     cudaError_t e =
         cudaFuncSetAttribute(gemm_mxf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    gemm_mxf4_pair_kernel<<<2 * clusters, kThreads, smem, stream>>>(amap, bmap, cmap, sfamap, sfbmap, g);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, amap, bmap, cmap, sfamap, sfbmap, g);
 }
 
 }  // namespace mxfp4

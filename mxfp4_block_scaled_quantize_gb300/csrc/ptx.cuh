@@ -36,6 +36,19 @@ __device__ __forceinline__ uint64_t globaltimer() {
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
 // ---------------------------------------------------------------------------------------
+// Programmatic dependent launch: kernels of the path run back to back in one stream; each
+// lets the next one launch at once and waits, before touching global memory, until the
+// kernels before it have finished and their writes are visible.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_wait_prerequisites() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

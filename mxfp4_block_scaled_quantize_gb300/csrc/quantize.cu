@@ -179,6 +179,8 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
         fence_barrier_init();
     }
     __syncthreads();
+    grid_launch_dependents();
+    grid_wait_prerequisites();
 
     if (warp == kQConsumerWarps) {
         // ------------------------------------------------------------- producer (TMA)
@@ -306,18 +308,20 @@ int quantize_ctas_per_sm() { return kQCtasPerSm; }
 cudaError_t launch_quantize(const CUtensorMap& xmap, const QuantArgs& a, bool dual, int grid,
                             cudaStream_t stream) {
     const size_t smem = quantize_smem_bytes();
-    if (dual) {
-        auto k = quantize_kernel<true>;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        k<<<grid, kQThreads, smem, stream>>>(xmap, a);
-    } else {
-        auto k = quantize_kernel<false>;
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        k<<<grid, kQThreads, smem, stream>>>(xmap, a);
-    }
-    return cudaGetLastError();
+    auto k = dual ? quantize_kernel<true> : quantize_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kQThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, xmap, a);
 }
 
 }  // namespace mxfp4
