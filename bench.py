@@ -185,6 +185,13 @@ def run_ours(args, rank, world, local_rank):
     dy = t["dY"].to(dev) if lin.train else None
     layer = MXFP4Linear(M, N, K, train=lin.train, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_src = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # Write a buffer larger than L2, then read another one: no input of the step is left
+        # in L2, and neither is a dirty line whose write-back would land in the next step.
+        flush.zero_()
+        flush_src.sum()
     stream = torch.cuda.current_stream(dev)
     n_k = layer.launches_per_step
     names = (["quant_dual_X", "quant_dual_W", "gemm_fwd", "quant_dual_dY", "gemm_dgrad",
@@ -211,7 +218,7 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         layer.step(x, w, dy)
     torch.cuda.synchronize()
     if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
@@ -235,7 +242,7 @@ def run_ours(args, rank, world, local_rank):
     t_start = time.time()
     head_start()
     for k in range(args.steps):
-        flush.zero_()
+        flush_l2()
         step_events[k][0].record(stream)
         layer.step(x, w, dy)
         step_events[k][1].record(stream)
@@ -247,7 +254,7 @@ def run_ours(args, rank, world, local_rank):
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_k + 1)] for _ in range(args.steps)]
     head_start()
     for k in range(args.steps):
-        flush.zero_()
+        flush_l2()
         step_with_events(events[k])
     torch.cuda.synchronize()
     t_end2 = time.time()
@@ -348,7 +355,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": args.workload, "M": M, "N": N, "K": K,
                    "step": "dual-quant X,W; fwd; dual-quant dY; dgrad; wgrad" if lin.train
                    else "row-quant X,W; fwd",
-                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then "
+                         f"{L2_FLUSH_BYTES >> 20} MiB read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "kernel": gemm_kernel,
                      "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1),
