@@ -76,6 +76,25 @@ def test_tiny_config_step(out_dtype):
     check_gemm(dw, c, cabs, "tiny wgrad")
 
 
+def test_step_from_host_matches_device_step():
+    # The overlapped host-buffer step (copy streams + kernel stream) gives the same bytes as
+    # the plain device step, twice in a row (buffers reused across steps).
+    lin = workloads.Linear("host", 384, 640, 512, True)
+    wl = workloads.Workload("host", "host-buffer step", [lin], base_seed=11)
+    t = wl.tensors(0)
+    ref = MXFP4Linear(lin.M, lin.N, lin.K, train=True)
+    want = [o.cpu() for o in ref.step(t["X"].cuda(), t["W"].cuda(), t["dY"].cuda())]
+    layer = MXFP4Linear(lin.M, lin.N, lin.K, train=True)
+    hx, hw, hdy = (t[k].pin_memory() for k in ("X", "W", "dY"))
+    for _ in range(2):
+        outs = [torch.full(o.shape, float("nan"), dtype=o.dtype).pin_memory() for o in want]
+        layer.step_host(hx, hw, hdy, *outs)
+        torch.cuda.synchronize()
+        assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+        for got, exp in zip(outs, want):
+            assert torch.equal(got.view(torch.int16), exp.view(torch.int16))
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 8, 32), (200, 300, 40), (129, 257, 384),
                                    (128, 256, 256), (300, 520, 1000), (64, 1000, 4600),
                                    (256, 128, 128), (384, 768, 640), (513, 255, 2048)])
