@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_wait_ld();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&sm.tmem_empty));
+            if (lane == 0) mbar_arrive_relaxed(smem_addr(&sm.tmem_empty));
 
             const int mt = t % g.tiles_m, nt = t / g.tiles_m;
             const int64_t row0 = static_cast<int64_t>(mt) * BM + q * 32;

@@ -262,7 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tc_wait_ld();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(leader_tmem_empty);
+            if (lane == 0) mbar_arrive_cluster_relaxed(leader_tmem_empty);
 
             const int mt2 = t % g.tiles_m2, nt = t / g.tiles_m2;
             const int64_t row0 = static_cast<int64_t>(mt2) * 256 + rank * 128 + q * 32;
