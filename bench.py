@@ -194,24 +194,22 @@ def run_ours(args, rank, world, local_rank):
         flush_src.sum()
     stream = torch.cuda.current_stream(dev)
     n_k = layer.launches_per_step
-    names = (["quant_dual_X", "quant_dual_W", "gemm_fwd", "quant_dual_dY", "gemm_dgrad",
-              "gemm_wgrad"] if lin.train else ["quant_row_X", "quant_row_W", "gemm_fwd"])
+    names = (["quant_dual_XW", "gemm_fwd", "quant_dual_dY", "gemm_dgrad", "gemm_wgrad"]
+             if lin.train else ["quant_row_XW", "gemm_fwd"])
 
     def step_with_events(evs):
         evs[0].record(stream)
-        layer.quantize_x(x)
+        layer.quantize_xw(x, w)
         evs[1].record(stream)
-        layer.quantize_w(w)
-        evs[2].record(stream)
         layer.fwd_gemm()
-        evs[3].record(stream)
+        evs[2].record(stream)
         if lin.train:
             layer.quantize_dy(dy)
-            evs[4].record(stream)
+            evs[3].record(stream)
             layer.dgrad_gemm()
-            evs[5].record(stream)
+            evs[4].record(stream)
             layer.wgrad_gemm()
-            evs[6].record(stream)
+            evs[5].record(stream)
 
     def barrier():
         if world > 1:
@@ -303,7 +301,7 @@ def run_ours(args, rank, world, local_rank):
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
 
     # algorithmic bytes of each quantizer launch (padding excluded)
-    shapes = {"X": (M, K), "W": (N, K), "dY": (M, N)}
+    elems = {"XW": M * K + N * K, "dY": M * N}   # elements each quantizer launch reads
     bpe = 3.0625 if lin.train else 2.53125
     kern = {}
     for i, n in enumerate(names):
@@ -313,13 +311,11 @@ def run_ours(args, rank, world, local_rank):
             ent["tflops"] = round(gemm_flops / (ms * 1e-3) / 1e12, 1)
             ent["frac_of_fp4_peak"] = round(ent["tflops"] / fp4_peak, 4)
         else:
-            r, c = shapes[n.split("_")[-1]]
-            nbytes = r * c * bpe
+            nbytes = elems[n.split("_")[-1]] * bpe
             ent["gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
             ent["frac_of_hbm"] = round(ent["gbs"] / peaks["hbm_gbs"], 4)
         kern[n] = ent
-    q_bytes = sum(shapes[names[i].split("_")[-1]][0] * shapes[names[i].split("_")[-1]][1] * bpe
-                  for i in quant_idx)
+    q_bytes = sum(elems[names[i].split("_")[-1]] * bpe for i in quant_idx)
     q_ms = sum(statistics.mean(per_kernel[i]) for i in quant_idx)
     quant_gbs = q_bytes / (q_ms * 1e-3) / 1e9
 

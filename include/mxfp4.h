@@ -96,6 +96,32 @@ mxfp4_status mxfp4_quantize_dual(const void* x, int64_t M, int64_t K, int64_t ld
                                  void* q_row, void* s_row, void* q_col, void* s_col,
                                  mxfp4_scale_layout layout, mxfp4_stream_t stream);
 
+/* One tensor of a batched quantization: bf16 x[rows, k] with row pitch ldx elements and
+ * its output buffers, as for mxfp4_quantize / mxfp4_quantize_dual (q_col and s_col are
+ * read only for the dual quantizer). */
+typedef struct {
+    const void* x;
+    int64_t rows;
+    int64_t k;
+    int64_t ldx;
+    void* q_row;
+    void* s_row;
+    void* q_col;
+    void* s_col;
+} mxfp4_quantize_task;
+
+#define MXFP4_MAX_BATCH 4
+
+/* Quantizes 1..MXFP4_MAX_BATCH independent tensors in one launch, each with exactly the
+ * output of mxfp4_quantize (dual == 0) or mxfp4_quantize_dual (dual != 0).  Same
+ * operation as those two (the per-tensor `quantize_mxfp4` / `_quantize_mxfp4_dual_op`
+ * calls of primus_turbo_mxfp4_local.py); one launch lets a small tensor share the GPU with
+ * a large one instead of paying its own ramp-up and tail (the forward step quantizes X and
+ * W together).  Tasks must not overlap in memory.  Every task is checked before anything
+ * runs: the first failing task's status is returned and nothing is launched. */
+mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* tasks, int32_t dual,
+                                  mxfp4_scale_layout layout, mxfp4_stream_t stream);
+
 /* Block-scaled GEMM C[M,N] = A . B^T over two K-packed blobs (the "TN" form that the
  * forward, dgrad and wgrad `gemm_fp4_impl` calls of `MXFP4LinearFunction` reduce to):
  *   a_q  A elements [M, Kp/2];  a_s  A scales, MXFP4_SCALE_TC layout for (M, K)

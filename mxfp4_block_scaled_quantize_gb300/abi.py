@@ -25,10 +25,20 @@ MXFP4_SCALE_TC = 1
 MXFP4_OUT_BF16 = 0
 MXFP4_OUT_F32 = 1
 
+MXFP4_MAX_BATCH = 4
+
+
+class QuantizeTask(ctypes.Structure):
+    """mxfp4_quantize_task of include/mxfp4.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("ldx", ctypes.c_int64), ("q_row", ctypes.c_void_p), ("s_row", ctypes.c_void_p),
+                ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p)]
+
 EXPORTED = (
     "mxfp4_quantize_sizes",
     "mxfp4_quantize",
     "mxfp4_quantize_dual",
+    "mxfp4_quantize_batch",
     "mxfp4_gemm",
     "mxfp4_last_device_error",
     "mxfp4_selftest_bounded_wait",
@@ -60,6 +70,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                          ctypes.POINTER(ctypes.c_size_t)]
     lib.mxfp4_quantize.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp]
     lib.mxfp4_quantize_dual.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, vp]
+    lib.mxfp4_quantize_batch.argtypes = [i32, ctypes.POINTER(QuantizeTask), i32, i32, vp]
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_last_device_error.argtypes = [vp]
     lib.mxfp4_selftest_bounded_wait.argtypes = [i64, vp]
@@ -118,6 +129,17 @@ def mxfp4_quantize_dual(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=MXFP4_S
     _check(load().mxfp4_quantize_dual(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
                                       _ptr(s_col), layout, _stream(stream)),
            "mxfp4_quantize_dual")
+
+
+def mxfp4_quantize_batch(tasks, dual: bool, layout=MXFP4_SCALE_TC, stream=None) -> None:
+    """tasks: sequence of (x, rows, k, ldx, q_row, s_row, q_col, s_col); q_col / s_col may
+    be None for the row-only quantizer."""
+    arr = (QuantizeTask * max(1, len(tasks)))()
+    for i, (x, rows, k, ldx, q_row, s_row, q_col, s_col) in enumerate(tasks):
+        arr[i] = QuantizeTask(_ptr(x), rows, k, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
+                              _ptr(s_col))
+    _check(load().mxfp4_quantize_batch(len(tasks), arr, int(bool(dual)), layout, _stream(stream)),
+           "mxfp4_quantize_batch")
 
 
 def mxfp4_gemm(a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype=MXFP4_OUT_BF16, stream=None) -> None:

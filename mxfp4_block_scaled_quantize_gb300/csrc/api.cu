@@ -81,25 +81,27 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uin
     return r == CUDA_SUCCESS;
 }
 
-mxfp4_status quantize_common(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* s_row,
-                             void* q_col, void* s_col, mxfp4_scale_layout layout, bool dual,
-                             cudaStream_t stream) {
+// Argument checks of one quantization task (no device needed).
+mxfp4_status quantize_check(const void* x, int64_t M, int64_t K, int64_t ldx, const void* q_row,
+                            const void* s_row, const void* q_col, const void* s_col, mxfp4_scale_layout layout,
+                            bool dual) {
     if (x == nullptr || q_row == nullptr || s_row == nullptr) return MXFP4_ERR_INVALID_ARG;
     if (dual && (q_col == nullptr || s_col == nullptr)) return MXFP4_ERR_INVALID_ARG;
     if (M < 1 || K < 1 || M > kMaxDim || K > kMaxDim || ldx < K || ldx > kMaxDim) return MXFP4_ERR_INVALID_ARG;
     if (layout != MXFP4_SCALE_PLAIN && layout != MXFP4_SCALE_TC) return MXFP4_ERR_INVALID_ARG;
     if (!aligned16(x) || (ldx % 8) != 0 || !aligned16(q_row) || !aligned16(s_row)) return MXFP4_ERR_MISALIGNED;
     if (dual && (!aligned16(q_col) || !aligned16(s_col))) return MXFP4_ERR_MISALIGNED;
-    DeviceState* dev = nullptr;
-    mxfp4_status st = device_ready(&dev);
-    if (st != MXFP4_OK) return st;
+    return MXFP4_OK;
+}
 
-    CUtensorMap xmap;
-    if (!encode_2d(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
-                   static_cast<uint64_t>(ldx) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+// Fills slot j of the batch (tensor map and arguments) for a checked task.
+mxfp4_status quantize_task(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* s_row,
+                           void* q_col, void* s_col, mxfp4_scale_layout layout, DeviceState* dev,
+                           mxfp4::QuantBatch* b, int j) {
+    if (!encode_2d(&b->maps[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(K),
+                   static_cast<uint64_t>(M), static_cast<uint64_t>(ldx) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return MXFP4_ERR_CUDA;
-
-    mxfp4::QuantArgs a;
+    mxfp4::QuantArgs& a = b->args[j];
     a.M = M;
     a.K = K;
     a.tiles_m = static_cast<int32_t>(cdiv(M, 128));
@@ -114,11 +116,34 @@ mxfp4_status quantize_common(const void* x, int64_t M, int64_t K, int64_t ldx, v
     a.kb_col = pad128(M) / 32;
     a.tc_layout = layout == MXFP4_SCALE_TC ? 1 : 0;
     a.err = dev->err;
-    const int64_t tiles = static_cast<int64_t>(a.tiles_m) * a.tiles_k;
-    if (tiles > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;
+    const int64_t before = j > 0 ? b->tile_end[j - 1] : 0;
+    const int64_t end = before + static_cast<int64_t>(a.tiles_m) * a.tiles_k;
+    if (end > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;
+    b->tile_end[j] = static_cast<int32_t>(end);
+    b->count = j + 1;
+    return MXFP4_OK;
+}
+
+mxfp4_status launch_batch(const mxfp4::QuantBatch& b, bool dual, DeviceState* dev, cudaStream_t stream) {
+    const int64_t tiles = b.tile_end[b.count - 1];
     const int64_t cap = static_cast<int64_t>(dev->sms) * mxfp4::quantize_ctas_per_sm();
     const int grid = static_cast<int>(tiles < cap ? tiles : cap);
-    return mxfp4::launch_quantize(xmap, a, dual, grid, stream) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+    return mxfp4::launch_quantize(b, dual, grid, stream) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
+mxfp4_status quantize_common(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* s_row,
+                             void* q_col, void* s_col, mxfp4_scale_layout layout, bool dual,
+                             cudaStream_t stream) {
+    mxfp4_status st = quantize_check(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, dual);
+    if (st != MXFP4_OK) return st;
+    DeviceState* dev = nullptr;
+    st = device_ready(&dev);
+    if (st != MXFP4_OK) return st;
+    mxfp4::QuantBatch b;
+    std::memset(&b, 0, sizeof(b));
+    st = quantize_task(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, dev, &b, 0);
+    if (st != MXFP4_OK) return st;
+    return launch_batch(b, dual, dev, stream);
 }
 
 __global__ void selftest_wait_kernel(uint32_t* err, uint64_t limit_ns) {
@@ -171,6 +196,29 @@ mxfp4_status mxfp4_quantize_dual(const void* x, int64_t M, int64_t K, int64_t ld
                                  void* q_col, void* s_col, mxfp4_scale_layout layout, mxfp4_stream_t stream) {
     return quantize_common(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, true,
                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* tasks, int32_t dual,
+                                  mxfp4_scale_layout layout, mxfp4_stream_t stream) {
+    if (count < 1 || count > MXFP4_MAX_BATCH || tasks == nullptr) return MXFP4_ERR_INVALID_ARG;
+    const bool d = dual != 0;
+    for (int j = 0; j < count; ++j) {
+        const mxfp4_quantize_task& t = tasks[j];
+        const mxfp4_status st = quantize_check(t.x, t.rows, t.k, t.ldx, t.q_row, t.s_row, t.q_col, t.s_col,
+                                               layout, d);
+        if (st != MXFP4_OK) return st;
+    }
+    DeviceState* dev = nullptr;
+    mxfp4_status st = device_ready(&dev);
+    if (st != MXFP4_OK) return st;
+    mxfp4::QuantBatch b;
+    std::memset(&b, 0, sizeof(b));
+    for (int j = 0; j < count; ++j) {
+        const mxfp4_quantize_task& t = tasks[j];
+        st = quantize_task(t.x, t.rows, t.k, t.ldx, t.q_row, t.s_row, t.q_col, t.s_col, layout, dev, &b, j);
+        if (st != MXFP4_OK) return st;
+    }
+    return launch_batch(b, d, dev, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mxfp4_status mxfp4_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s, int64_t M, int64_t N,

@@ -25,14 +25,23 @@ struct QuantArgs {
     uint32_t* err;       // device error word
 };
 
+// Up to kMaxQuantTasks independent tensors quantized by one launch; tile t of the launch
+// belongs to the first task j with t < tile_end[j].  maps[j]: bf16 X of task j as a 2-D
+// tensor {K, M} (innermost first), box {64, 128} with the 128-byte swizzle (a 128 x 128
+// tile is two boxes), out-of-bounds elements read as zero.
+constexpr int kMaxQuantTasks = 4;
+struct QuantBatch {
+    CUtensorMap maps[kMaxQuantTasks];
+    QuantArgs args[kMaxQuantTasks];
+    int32_t tile_end[kMaxQuantTasks];
+    int32_t count;
+};
+
 // Shared memory one quantizer CTA needs, and how many CTAs share an SM.
 size_t quantize_smem_bytes();
 int quantize_ctas_per_sm();
 
-// xmap: bf16 X as a 2-D tensor {K, M} (innermost first), box {64, 128} with the 128-byte
-// swizzle (a 128 x 128 tile is two boxes), out-of-bounds elements read as zero.
-cudaError_t launch_quantize(const CUtensorMap& xmap, const QuantArgs& a, bool dual, int grid,
-                            cudaStream_t stream);
+cudaError_t launch_quantize(const QuantBatch& b, bool dual, int grid, cudaStream_t stream);
 
 // ---- GEMM ------------------------------------------------------------------------------
 struct GemmArgs {

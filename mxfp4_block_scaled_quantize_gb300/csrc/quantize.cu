@@ -166,14 +166,22 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 
 template <bool kDual>
 __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
-    quantize_kernel(const __grid_constant__ CUtensorMap xmap, const QuantArgs p) {
+    quantize_kernel(const __grid_constant__ QuantBatch P) {
     extern __shared__ uint8_t smem_raw[];
     QuantSmem& sm = *reinterpret_cast<QuantSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int num_tiles = p.tiles_m * p.tiles_k;
+    const int num_tiles = P.tile_end[P.count - 1];
+    uint32_t* const err = P.args[0].err;
+    // Task of launch tile t, and t's index within that task.
+    auto task_of = [&](int t, int* local) {
+        int j = 0;
+        while (j + 1 < P.count && t >= P.tile_end[j]) ++j;
+        *local = t - (j > 0 ? P.tile_end[j - 1] : 0);
+        return j;
+    };
 
     if (tid == 0) {
         for (int s = 0; s < kQStages; ++s) {
@@ -190,18 +198,21 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     if (warp == kQConsumerWarps) {
         // ------------------------------------------------------------- producer (TMA)
         if (lane_id() == 0) {
-            prefetch_tensormap(&xmap);
+            for (int j = 0; j < P.count; ++j) prefetch_tensormap(&P.maps[j]);
             int it = 0;
             for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
                 const int s = it % kQStages;
                 const uint32_t ph = (it / kQStages) & 1;
-                if (!mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1, p.err, kErrQuantProducer, &sm.abort))
+                if (!mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1, err, kErrQuantProducer, &sm.abort))
                     break;
-                const int tm = t / p.tiles_k, tk = t % p.tiles_k;
+                int lt;
+                const int j = task_of(t, &lt);
+                const int tm = lt / P.args[j].tiles_k, tk = lt % P.args[j].tiles_k;
+                const CUtensorMap* xmap = &P.maps[j];
                 const uint32_t bar = smem_addr(&sm.full[s]);
                 mbar_arrive_expect_tx(bar, kQTileBytes);
-                tma_load_2d(smem_addr(sm.tile[s]), &xmap, tk * kQT, tm * kQT, bar);
-                tma_load_2d(smem_addr(sm.tile[s]) + kQBoxBytes, &xmap, tk * kQT + 64, tm * kQT, bar);
+                tma_load_2d(smem_addr(sm.tile[s]), xmap, tk * kQT, tm * kQT, bar);
+                tma_load_2d(smem_addr(sm.tile[s]) + kQBoxBytes, xmap, tk * kQT + 64, tm * kQT, bar);
             }
             // Drain: every armed stage's copy has landed before this thread may leave.
             const int armed = it < kQStages ? it : kQStages;
@@ -220,10 +231,12 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
         const int s = it % kQStages;
         const uint32_t ph = (it / kQStages) & 1;
         int ok = 0;
-        if (lane == 0) ok = mbar_wait(smem_addr(&sm.full[s]), ph, p.err, kErrQuantConsumer, &sm.abort) ? 1 : 0;
+        if (lane == 0) ok = mbar_wait(smem_addr(&sm.full[s]), ph, err, kErrQuantConsumer, &sm.abort) ? 1 : 0;
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
 
-        const int tm = t / p.tiles_k, tk = t % p.tiles_k;
+        int lt;
+        const QuantArgs& p = P.args[task_of(t, &lt)];
+        const int tm = lt / p.tiles_k, tk = lt % p.tiles_k;
         const int64_t m0 = static_cast<int64_t>(tm) * kQT;
         const int64_t k0 = static_cast<int64_t>(tk) * kQT;
         const uint32_t tile = smem_addr(sm.tile[s]);
@@ -330,8 +343,7 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
 size_t quantize_smem_bytes() { return sizeof(QuantSmem) + 1024; }
 int quantize_ctas_per_sm() { return kQCtasPerSm; }
 
-cudaError_t launch_quantize(const CUtensorMap& xmap, const QuantArgs& a, bool dual, int grid,
-                            cudaStream_t stream) {
+cudaError_t launch_quantize(const QuantBatch& b, bool dual, int grid, cudaStream_t stream) {
     const size_t smem = quantize_smem_bytes();
     auto k = dual ? quantize_kernel<true> : quantize_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -346,7 +358,7 @@ cudaError_t launch_quantize(const CUtensorMap& xmap, const QuantArgs& a, bool du
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, xmap, a);
+    return cudaLaunchKernelEx(&cfg, k, b);
 }
 
 }  // namespace mxfp4

@@ -61,6 +61,18 @@ def test_argument_checks_precede_any_device_use(lib):
     assert lib.mxfp4_gemm(16, 32, 48, 64, 4, 4, 4, 80, 2, 0, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_gemm(16, 32, 48, 64, 4, 4, 4, 88, 4, 0, None) == abi.MXFP4_ERR_MISALIGNED
     assert lib.mxfp4_selftest_bounded_wait(0, None) == abi.MXFP4_ERR_INVALID_ARG
+    # batch: task count, task array, and each task's own checks
+    T = abi.QuantizeTask
+    good = T(16, 4, 8, 8, 32, 48, 64, 80)
+    arr = (T * 5)(*([good] * 5))
+    assert lib.mxfp4_quantize_batch(0, arr, 1, 1, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_quantize_batch(5, arr, 1, 1, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_quantize_batch(1, None, 1, 1, None) == abi.MXFP4_ERR_INVALID_ARG
+    bad = (T * 2)(good, T(16, 4, 8, 8, 32, 48, None, 80))          # dual without q_col
+    assert lib.mxfp4_quantize_batch(2, bad, 1, 1, None) == abi.MXFP4_ERR_INVALID_ARG
+    bad = (T * 2)(good, T(18, 4, 8, 8, 32, 48, 64, 80))            # x not 16-byte aligned
+    assert lib.mxfp4_quantize_batch(2, bad, 1, 1, None) == abi.MXFP4_ERR_MISALIGNED
+    assert lib.mxfp4_quantize_batch(1, arr, 1, 2, None) == abi.MXFP4_ERR_INVALID_ARG  # layout
 
 
 def test_status_strings(lib):

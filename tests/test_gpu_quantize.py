@@ -116,6 +116,32 @@ def test_ragged_shapes(M, K, ldx):
         check_quantized_full(x, quant(x, False, layout, ldx), layout, False, f"row {M}x{K}")
 
 
+@pytest.mark.parametrize("dual", [True, False])
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_batch_equals_single_calls(dual, layout):
+    # One launch over 1..4 tensors of different shapes (ragged edges, a pitched input) gives
+    # each tensor the bytes its own call gives.
+    shapes = [(300, 200, 200), (129, 1000, 1008), (1, 40, 40), (640, 384, 392)]
+    xs = [_edge_input(M, K, 31 * i + M) for i, (M, K, _) in enumerate(shapes)]
+    singles = [quant(x, dual, layout, ldx) for x, (_, _, ldx) in zip(xs, shapes)]
+    for n in (1, 2, 4):
+        tasks, outs = [], []
+        for x, (M, K, ldx) in zip(xs[:n], shapes[:n]):
+            wide = torch.zeros((M, ldx), dtype=torch.bfloat16)
+            wide[:, :K] = x
+            xg = wide.cuda()
+            rq, rs = abi.alloc_blob(M, K, layout)
+            cq, cs = abi.alloc_blob(K, M, layout) if dual else (None, None)
+            tasks.append((xg, M, K, ldx, rq, rs, cq, cs))
+            outs.append((rq, rs, cq, cs) if dual else (rq, rs))
+        abi.mxfp4_quantize_batch(tasks, dual, layout)
+        torch.cuda.synchronize()
+        assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+        for got, want in zip(outs, singles):
+            for g, w in zip(got, want):
+                assert torch.equal(g.cpu(), w.cpu())
+
+
 def test_row_only_equals_row_half_of_dual():
     x = _edge_input(4608, 3072, 11)
     r = quant(x, False, abi.MXFP4_SCALE_TC)
