@@ -194,7 +194,7 @@ def run_ours(args, rank, world, local_rank):
         flush_src.sum()
     stream = torch.cuda.current_stream(dev)
     n_k = layer.launches_per_step
-    names = (["quant_dual_XW", "gemm_fwd", "quant_dual_dY", "gemm_dgrad", "gemm_wgrad"]
+    names = (["quant_dual_XW", "gemm_fwd", "quant_dual_dY", "gemm_dgrad_wgrad"]
              if lin.train else ["quant_row_XW", "gemm_fwd"])
 
     def step_with_events(evs):
@@ -206,10 +206,8 @@ def run_ours(args, rank, world, local_rank):
         if lin.train:
             layer.quantize_dy(dy)
             evs[3].record(stream)
-            layer.dgrad_gemm()
+            layer.bwd_gemms()
             evs[4].record(stream)
-            layer.wgrad_gemm()
-            evs[5].record(stream)
 
     def barrier():
         if world > 1:
@@ -296,8 +294,10 @@ def run_ours(args, rank, world, local_rank):
     fp4_peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
     gemm_idx = [i for i, n in enumerate(names) if n.startswith("gemm")]
     quant_idx = [i for i, n in enumerate(names) if n.startswith("quant")]
-    gemm_flops = 2 * M * N * K
-    gemm_ms = statistics.mean([v for i in gemm_idx for v in per_kernel[i]])
+    # algorithmic flops of each GEMM launch: the forward GEMM, and dgrad + wgrad together
+    launch_flops = {"gemm_fwd": 2 * M * N * K, "gemm_dgrad_wgrad": 4 * M * N * K}
+    gemm_flops = sum(launch_flops[names[i]] for i in gemm_idx) / len(gemm_idx)   # per launch
+    gemm_ms = statistics.mean([v for i in gemm_idx for v in per_kernel[i]])      # per launch
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
 
     # algorithmic bytes of each quantizer launch (padding excluded)
@@ -308,7 +308,7 @@ def run_ours(args, rank, world, local_rank):
         ms = statistics.mean(per_kernel[i])
         ent = {"avg_us": round(ms * 1e3, 2), "min_us": round(min(per_kernel[i]) * 1e3, 2)}
         if n.startswith("gemm"):
-            ent["tflops"] = round(gemm_flops / (ms * 1e-3) / 1e12, 1)
+            ent["tflops"] = round(launch_flops[n] / (ms * 1e-3) / 1e12, 1)
             ent["frac_of_fp4_peak"] = round(ent["tflops"] / fp4_peak, 4)
         else:
             nbytes = elems[n.split("_")[-1]] * bpe
@@ -350,7 +350,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": traffic,
                      "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x "
                                     f"{NOMINAL_FP4_OVER_BF16:g} (nominal dense FP4/bf16 ratio)",
-                     "algorithmic_flops_per_launch": gemm_flops},
+                     "algorithmic_flops_per_launch": int(gemm_flops)},
         "quant_roofline": {"bound": "hbm", "achieved": round(quant_gbs, 1),
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": round(quant_gbs / peaks["hbm_gbs"], 4),

@@ -136,6 +136,29 @@ mxfp4_status mxfp4_gemm(const void* a_q, const void* a_s, const void* b_q, const
                         int64_t M, int64_t N, int64_t K, void* c, int64_t ldc,
                         mxfp4_out_dtype out_dtype, mxfp4_stream_t stream);
 
+/* One GEMM of a batch: the arguments of mxfp4_gemm. */
+typedef struct {
+    const void* a_q;
+    const void* a_s;
+    const void* b_q;
+    const void* b_s;
+    int64_t M;
+    int64_t N;
+    int64_t K;
+    void* c;
+    int64_t ldc;
+    mxfp4_out_dtype out_dtype;
+} mxfp4_gemm_task;
+
+/* 1..MXFP4_MAX_BATCH independent GEMMs, each with exactly the result its own mxfp4_gemm
+ * call gives (the dgrad and wgrad `gemm_fp4_impl` calls of
+ * `MXFP4LinearFunction.backward` read the same quantized dY and run back to back).  The
+ * problems with more than one 128-row tile share one launch, whose CTA pairs walk the
+ * tiles of all of them, so neither pays its own ramp-up and tail.  Outputs must not
+ * overlap each other or any input.  Every task is checked before anything runs: the first
+ * failing task's status is returned and nothing is launched. */
+mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4_stream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the device error word of the current
  * device: MXFP4_ERR_TIMEOUT if a bounded wait in any kernel of this library ran out
  * since the last call, MXFP4_ERR_CUDA if the synchronization itself failed, else OK. */

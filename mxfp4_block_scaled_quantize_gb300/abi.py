@@ -28,6 +28,14 @@ MXFP4_OUT_F32 = 1
 MXFP4_MAX_BATCH = 4
 
 
+class GemmTask(ctypes.Structure):
+    """mxfp4_gemm_task of include/mxfp4.h."""
+    _fields_ = [("a_q", ctypes.c_void_p), ("a_s", ctypes.c_void_p), ("b_q", ctypes.c_void_p),
+                ("b_s", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("c", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+                ("out_dtype", ctypes.c_int)]
+
+
 class QuantizeTask(ctypes.Structure):
     """mxfp4_quantize_task of include/mxfp4.h."""
     _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("k", ctypes.c_int64),
@@ -40,6 +48,7 @@ EXPORTED = (
     "mxfp4_quantize_dual",
     "mxfp4_quantize_batch",
     "mxfp4_gemm",
+    "mxfp4_gemm_batch",
     "mxfp4_last_device_error",
     "mxfp4_selftest_bounded_wait",
     "mxfp4_status_string",
@@ -72,6 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_quantize_dual.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, vp]
     lib.mxfp4_quantize_batch.argtypes = [i32, ctypes.POINTER(QuantizeTask), i32, i32, vp]
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
+    lib.mxfp4_gemm_batch.argtypes = [i32, ctypes.POINTER(GemmTask), vp]
     lib.mxfp4_last_device_error.argtypes = [vp]
     lib.mxfp4_selftest_bounded_wait.argtypes = [i64, vp]
     lib.mxfp4_status_string.argtypes = [i32]
@@ -145,6 +155,14 @@ def mxfp4_quantize_batch(tasks, dual: bool, layout=MXFP4_SCALE_TC, stream=None) 
 def mxfp4_gemm(a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype=MXFP4_OUT_BF16, stream=None) -> None:
     _check(load().mxfp4_gemm(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, _ptr(c), ldc,
                              out_dtype, _stream(stream)), "mxfp4_gemm")
+
+
+def mxfp4_gemm_batch(tasks, stream=None) -> None:
+    """tasks: sequence of (a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype)."""
+    arr = (GemmTask * max(1, len(tasks)))()
+    for i, (a_q, a_s, b_q, b_s, M, N, K, c, ldc, od) in enumerate(tasks):
+        arr[i] = GemmTask(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, _ptr(c), ldc, od)
+    _check(load().mxfp4_gemm_batch(len(tasks), arr, _stream(stream)), "mxfp4_gemm_batch")
 
 
 def mxfp4_last_device_error(stream=None) -> int:

@@ -162,6 +162,80 @@ __global__ void selftest_wait_kernel(uint32_t* err, uint64_t limit_ns) {
     __syncwarp();
 }
 
+// Argument checks of one GEMM (no device needed).
+mxfp4_status gemm_check(const mxfp4_gemm_task& t) {
+    if (!t.a_q || !t.a_s || !t.b_q || !t.b_s || !t.c) return MXFP4_ERR_INVALID_ARG;
+    if (t.M < 1 || t.N < 1 || t.K < 1 || t.M > kMaxDim || t.N > kMaxDim || t.K > kMaxDim)
+        return MXFP4_ERR_INVALID_ARG;
+    if (t.ldc < t.N || t.ldc > kMaxDim) return MXFP4_ERR_INVALID_ARG;
+    if (t.out_dtype != MXFP4_OUT_BF16 && t.out_dtype != MXFP4_OUT_F32) return MXFP4_ERR_INVALID_ARG;
+    if (!aligned16(t.a_q) || !aligned16(t.a_s) || !aligned16(t.b_q) || !aligned16(t.b_s) || !aligned16(t.c))
+        return MXFP4_ERR_MISALIGNED;
+    const int64_t tiles = cdiv(t.M, mxfp4::kGemmBM) * cdiv(t.N, mxfp4::kGemmBN);
+    if (tiles > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;
+    return MXFP4_OK;
+}
+
+// Kernel arguments and the A, B (box of b_rows rows) and C tensor maps of a checked GEMM.
+// C goes out through TMA stores when its pitch allows a tensor map (a multiple of 16
+// bytes; the base is 16-byte aligned by the checks); otherwise with plain stores.
+mxfp4_status gemm_fill(const mxfp4_gemm_task& t, DeviceState* dev, mxfp4::GemmArgs* g, CUtensorMap* amap,
+                       CUtensorMap* bmap, CUtensorMap* cmap, uint32_t b_rows) {
+    const int64_t kp = pad128(t.K);
+    if (!encode_2d(amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.a_q, static_cast<uint64_t>(kp / 2),
+                   static_cast<uint64_t>(t.M), static_cast<uint64_t>(kp / 2), 128, mxfp4::kGemmBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(bmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, t.b_q, static_cast<uint64_t>(kp / 2),
+                   static_cast<uint64_t>(t.N), static_cast<uint64_t>(kp / 2), 128, b_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return MXFP4_ERR_CUDA;
+    const int64_t esize = t.out_dtype == MXFP4_OUT_F32 ? 4 : 2;
+    std::memset(cmap, 0, sizeof(*cmap));
+    const bool c_tma = (t.ldc * esize) % 16 == 0 &&
+                       encode_2d(cmap, t.out_dtype == MXFP4_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                                     : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                 t.c, static_cast<uint64_t>(t.N), static_cast<uint64_t>(t.M),
+                                 static_cast<uint64_t>(t.ldc * esize), static_cast<uint32_t>(64 / esize), 32,
+                                 CU_TENSOR_MAP_SWIZZLE_64B);
+    g->M = t.M;
+    g->N = t.N;
+    g->tiles_m = static_cast<int32_t>(cdiv(t.M, mxfp4::kGemmBM));
+    g->tiles_n = static_cast<int32_t>(cdiv(t.N, mxfp4::kGemmBN));
+    g->tiles_m2 = static_cast<int32_t>(cdiv(t.M, 256));
+    g->k_stages = static_cast<int32_t>(cdiv(kp, 256));
+    g->kb4 = static_cast<int32_t>(kp / 128);
+    g->groups_b = static_cast<int32_t>(cdiv(t.N, 128));
+    g->a_s = static_cast<const uint8_t*>(t.a_s);
+    g->b_s = static_cast<const uint8_t*>(t.b_s);
+    g->c = t.c;
+    g->ldc = t.ldc;
+    g->out_f32 = t.out_dtype == MXFP4_OUT_F32 ? 1 : 0;
+    g->c_tma = c_tma ? 1 : 0;
+    g->err = dev->err;
+    return MXFP4_OK;
+}
+
+// Appends a checked GEMM to the CTA-pair batch (B box 128 rows, scale maps).
+mxfp4_status gemm_fill_pair(const mxfp4_gemm_task& t, DeviceState* dev, mxfp4::GemmPairBatch* b) {
+    const int j = b->count;
+    mxfp4::GemmArgs& g = b->args[j];
+    mxfp4_status st = gemm_fill(t, dev, &g, &b->amap[j], &b->bmap[j], &b->cmap[j], 128);
+    if (st != MXFP4_OK) return st;
+    if (!encode_2d(&b->sfamap[j], CU_TENSOR_MAP_DATA_TYPE_UINT64, t.a_s, static_cast<uint64_t>(g.kb4) * 64,
+                   static_cast<uint64_t>(cdiv(t.M, 128)), static_cast<uint64_t>(g.kb4) * 512, 128, 1,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&b->sfbmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT64, t.b_s, static_cast<uint64_t>(g.kb4) * 64,
+                   static_cast<uint64_t>(cdiv(t.N, 128)), static_cast<uint64_t>(g.kb4) * 512, 128, 2,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        return MXFP4_ERR_CUDA;
+    const int64_t before = j > 0 ? b->tile_end[j - 1] : 0;
+    const int64_t end = before + static_cast<int64_t>(g.tiles_m2) * g.tiles_n;
+    if (end > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;
+    b->tile_end[j] = static_cast<int32_t>(end);
+    b->count = j + 1;
+    return MXFP4_OK;
+}
+
 }  // namespace
 
 namespace mxfp4 {
@@ -223,77 +297,46 @@ mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* task
 
 mxfp4_status mxfp4_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s, int64_t M, int64_t N,
                         int64_t K, void* c, int64_t ldc, mxfp4_out_dtype out_dtype, mxfp4_stream_t stream) {
-    if (!a_q || !a_s || !b_q || !b_s || !c) return MXFP4_ERR_INVALID_ARG;
-    if (M < 1 || N < 1 || K < 1 || M > kMaxDim || N > kMaxDim || K > kMaxDim) return MXFP4_ERR_INVALID_ARG;
-    if (ldc < N || ldc > kMaxDim) return MXFP4_ERR_INVALID_ARG;
-    if (out_dtype != MXFP4_OUT_BF16 && out_dtype != MXFP4_OUT_F32) return MXFP4_ERR_INVALID_ARG;
-    if (!aligned16(a_q) || !aligned16(a_s) || !aligned16(b_q) || !aligned16(b_s) || !aligned16(c))
-        return MXFP4_ERR_MISALIGNED;
+    const mxfp4_gemm_task t{a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype};
+    return mxfp4_gemm_batch(1, &t, stream);
+}
+
+mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4_stream_t stream) {
+    if (count < 1 || count > MXFP4_MAX_BATCH || tasks == nullptr) return MXFP4_ERR_INVALID_ARG;
+    for (int j = 0; j < count; ++j) {
+        const mxfp4_status st = gemm_check(tasks[j]);
+        if (st != MXFP4_OK) return st;
+    }
     DeviceState* dev = nullptr;
     mxfp4_status st = device_ready(&dev);
     if (st != MXFP4_OK) return st;
-
-    const int64_t kp = pad128(K);
-    CUtensorMap amap, bmap;
-    if (!encode_2d(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_q, static_cast<uint64_t>(kp / 2), static_cast<uint64_t>(M),
-                   static_cast<uint64_t>(kp / 2), 128, mxfp4::kGemmBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&bmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_q, static_cast<uint64_t>(kp / 2), static_cast<uint64_t>(N),
-                   static_cast<uint64_t>(kp / 2), 128, mxfp4::kGemmBN, CU_TENSOR_MAP_SWIZZLE_128B))
-        return MXFP4_ERR_CUDA;
-
-    // C goes out through TMA stores when its base and pitch allow a tensor map (16-byte
-    // aligned base, pitch a multiple of 16 bytes); otherwise with plain stores.
-    const int64_t esize = out_dtype == MXFP4_OUT_F32 ? 4 : 2;
-    CUtensorMap cmap;
-    std::memset(&cmap, 0, sizeof(cmap));
-    const bool c_tma = (ldc * esize) % 16 == 0 &&
-                       encode_2d(&cmap, out_dtype == MXFP4_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                                 c, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
-                                 static_cast<uint64_t>(ldc * esize), static_cast<uint32_t>(64 / esize), 32,
-                                 CU_TENSOR_MAP_SWIZZLE_64B);
-
-    mxfp4::GemmArgs g;
-    g.M = M;
-    g.N = N;
-    g.tiles_m = static_cast<int32_t>(cdiv(M, mxfp4::kGemmBM));
-    g.tiles_n = static_cast<int32_t>(cdiv(N, mxfp4::kGemmBN));
-    g.k_stages = static_cast<int32_t>(cdiv(kp, 256));
-    g.kb4 = static_cast<int32_t>(kp / 128);
-    g.groups_b = static_cast<int32_t>(cdiv(N, 128));
-    g.a_s = static_cast<const uint8_t*>(a_s);
-    g.b_s = static_cast<const uint8_t*>(b_s);
-    g.c = c;
-    g.ldc = ldc;
-    g.out_f32 = out_dtype == MXFP4_OUT_F32 ? 1 : 0;
-    g.c_tma = c_tma ? 1 : 0;
-    g.err = dev->err;
-    g.tiles_m2 = static_cast<int32_t>(cdiv(M, 256));
-    const int64_t tiles = static_cast<int64_t>(g.tiles_m) * g.tiles_n;
-    if (tiles > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    // More than one 128-row tile: 256 x 256 tiles on CTA pairs.
-    const int max_clusters = M > mxfp4::kGemmBM ? mxfp4::gemm_pair_max_clusters() : 0;
-    if (max_clusters > 0) {
-        CUtensorMap bmap2, sfamap, sfbmap;
-        if (!encode_2d(&bmap2, CU_TENSOR_MAP_DATA_TYPE_UINT8, b_q, static_cast<uint64_t>(kp / 2),
-                       static_cast<uint64_t>(N), static_cast<uint64_t>(kp / 2), 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&sfamap, CU_TENSOR_MAP_DATA_TYPE_UINT64, a_s, static_cast<uint64_t>(g.kb4) * 64,
-                       static_cast<uint64_t>(cdiv(M, 128)), static_cast<uint64_t>(g.kb4) * 512, 128, 1,
-                       CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !encode_2d(&sfbmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, b_s, static_cast<uint64_t>(g.kb4) * 64,
-                       static_cast<uint64_t>(cdiv(N, 128)), static_cast<uint64_t>(g.kb4) * 512, 128, 2,
-                       CU_TENSOR_MAP_SWIZZLE_NONE))
-            return MXFP4_ERR_CUDA;
-        const int64_t pair_tiles = static_cast<int64_t>(g.tiles_m2) * g.tiles_n;
-        const int clusters = static_cast<int>(pair_tiles < max_clusters ? pair_tiles : max_clusters);
-        return mxfp4::launch_gemm_pair(amap, bmap2, cmap, sfamap, sfbmap, g, clusters, s) == cudaSuccess
-                   ? MXFP4_OK
-                   : MXFP4_ERR_CUDA;
+    // Problems of more than one 128-row tile share one CTA-pair launch; the others run on
+    // the one-CTA kernel, one launch each.
+    const int max_clusters = mxfp4::gemm_pair_max_clusters();
+    mxfp4::GemmPairBatch b;
+    std::memset(&b, 0, sizeof(b));
+    for (int j = 0; j < count; ++j) {
+        const mxfp4_gemm_task& t = tasks[j];
+        if (t.M > mxfp4::kGemmBM && max_clusters > 0) {
+            st = gemm_fill_pair(t, dev, &b);
+        } else {
+            mxfp4::GemmArgs g;
+            CUtensorMap amap, bmap, cmap;
+            st = gemm_fill(t, dev, &g, &amap, &bmap, &cmap, mxfp4::kGemmBN);
+            if (st == MXFP4_OK) {
+                const int64_t tiles = static_cast<int64_t>(g.tiles_m) * g.tiles_n;
+                const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
+                st = mxfp4::launch_gemm(amap, bmap, cmap, g, grid, s) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+            }
+        }
+        if (st != MXFP4_OK) return st;
     }
-    const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
-    return mxfp4::launch_gemm(amap, bmap, cmap, g, grid, s) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+    if (b.count == 0) return MXFP4_OK;
+    const int64_t pair_tiles = b.tile_end[b.count - 1];
+    const int clusters = static_cast<int>(pair_tiles < max_clusters ? pair_tiles : max_clusters);
+    return mxfp4::launch_gemm_pair(b, clusters, s) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
 
 mxfp4_status mxfp4_last_device_error(mxfp4_stream_t stream) {

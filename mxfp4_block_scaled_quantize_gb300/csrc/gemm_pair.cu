@@ -94,10 +94,12 @@ __device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t j) {
     return r * kOutRowBytes + ((j ^ ((r >> 1) & 3u)) << 4);
 }
 
+// kBatched = false: one problem (P.count == 1); its arguments stay constant-bank operands,
+// which the batched form's run-time problem index turns into registers (measured: the
+// forward GEMM spilled and lost 4 us in the batched form).
+template <bool kBatched>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gemm_mxf4_pair_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
-                          const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap sfamap,
-                          const __grid_constant__ CUtensorMap sfbmap, const GemmArgs g) {
+    gemm_mxf4_pair_kernel(const __grid_constant__ GemmPairBatch P) {
     extern __shared__ uint8_t smem_raw[];
     PairSmem& sm = *reinterpret_cast<PairSmem*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -109,7 +111,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     const int cluster = blockIdx.x >> 1;
     const int nclusters = gridDim.x >> 1;
-    const int num_tiles = g.tiles_m2 * g.tiles_n;
+    const int num_tiles = P.tile_end[P.count - 1];
+    uint32_t* const err = P.args[0].err;
+    // Problem of launch tile t, and t's index within that problem.
+    auto task_of = [&](int t, int* local) {
+        if (!kBatched) {
+            *local = t;
+            return 0;
+        }
+        int j = 0;
+        while (j + 1 < P.count && t >= P.tile_end[j]) ++j;
+        *local = t - (j > 0 ? P.tile_end[j - 1] : 0);
+        return j;
+    };
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -137,15 +151,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
         if (lane == 0) {
-            prefetch_tensormap(&amap);
-            prefetch_tensormap(&bmap);
-            prefetch_tensormap(&sfamap);
-            prefetch_tensormap(&sfbmap);
+            for (int j = 0; j < P.count; ++j) {
+                prefetch_tensormap(&P.amap[j]);
+                prefetch_tensormap(&P.bmap[j]);
+                prefetch_tensormap(&P.sfamap[j]);
+                prefetch_tensormap(&P.sfbmap[j]);
+            }
             const uint64_t pol = l2_policy_evict_last();
             int it = 0;
             bool ok = true;
             for (int t = cluster; t < num_tiles && ok; t += nclusters) {
-                const int mt2 = t % g.tiles_m2, nt = t / g.tiles_m2;
+                int lt;
+                const int j = task_of(t, &lt);
+                const GemmArgs& g = P.args[j];
+                const int mt2 = lt % g.tiles_m2, nt = lt / g.tiles_m2;
                 const int arow = mt2 * 256 + static_cast<int>(rank) * 128;
                 const int brow = nt * 256 + static_cast<int>(rank) * 128;
                 for (int ks = 0; ks < g.k_stages; ++ks, ++it) {
@@ -157,12 +176,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     if (leader) mbar_arrive_expect_tx(smem_addr(&sm.full[s]), 2 * kStageBytes);
                     const uint32_t bar = cluster_map(smem_addr(&sm.full[s]), 0);
-                    tma_load_2d_pair(smem_addr(sm.a[s]), &amap, ks * BKB, arow, bar, pol);
-                    tma_load_2d_pair(smem_addr(sm.b[s]), &bmap, ks * BKB, brow, bar, pol);
+                    tma_load_2d_pair(smem_addr(sm.a[s]), &P.amap[j], ks * BKB, arow, bar, pol);
+                    tma_load_2d_pair(smem_addr(sm.b[s]), &P.bmap[j], ks * BKB, brow, bar, pol);
                     // Scale maps count 8-byte units: 2 atoms = 128 units per K step.
-                    tma_load_2d_pair(smem_addr(sm.sfa[s]), &sfamap, ks * 128, 2 * mt2 + static_cast<int>(rank),
+                    tma_load_2d_pair(smem_addr(sm.sfa[s]), &P.sfamap[j], ks * 128, 2 * mt2 + static_cast<int>(rank),
                                      bar, pol);
-                    tma_load_2d_pair(smem_addr(sm.sfb[s]), &sfbmap, ks * 128, 2 * nt, bar, pol);
+                    tma_load_2d_pair(smem_addr(sm.sfb[s]), &P.sfbmap[j], ks * 128, 2 * nt, bar, pol);
                 }
             }
             // Drain (leader): every armed stage, both CTAs' bytes, has landed.
@@ -180,6 +199,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+                int lt;
+                const GemmArgs& g = P.args[task_of(t, &lt)];
                 for (int ks = 0; ks < g.k_stages; ++ks, ++it) {
                     if (!named_barrier_and(kBarHandoff, 64, true)) {
                         ok = false;
@@ -212,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             if (elect_one()) {
                 tc_commit_pair_multicast(smem_addr(&sm.drain), 1);
-                if (!mbar_wait_quiet(smem_addr(&sm.drain), 0, kWaitLimitNs)) atomicOr(g.err, kErrGemmDrain);
+                if (!mbar_wait_quiet(smem_addr(&sm.drain), 0, kWaitLimitNs)) atomicOr(err, kErrGemmDrain);
             }
             __syncwarp();
         }
@@ -222,6 +243,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int it = 0, tl = 0;
             bool ok = true;
             for (int t = cluster; t < num_tiles && ok; t += nclusters, ++tl) {
+                int lt;
+                const GemmArgs& g = P.args[task_of(t, &lt)];
                 for (int ks = 0; ks < g.k_stages; ++ks, ++it) {
                     int w = 1;
                     if (lane == 0) {
@@ -245,12 +268,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t obuf = smem_addr(sm.out[warp - kEpi0]);
         const uint64_t pol = l2_policy_evict_first();
         const uint32_t leader_tmem_empty = cluster_map(smem_addr(&sm.tmem_empty), 0);
-        if (g.c_tma && lane == 0) prefetch_tensormap(&cmap);
+        if (lane == 0)
+            for (int j = 0; j < P.count; ++j)
+                if (P.args[j].c_tma) prefetch_tensormap(&P.cmap[j]);
         int tl = 0;
         for (int t = cluster; t < num_tiles; t += nclusters, ++tl) {
             int okw = 1;
             if (warp == kEpi0 && lane == 0)
-                okw = mbar_wait(smem_addr(&sm.tmem_full), tl & 1, g.err, kErrGemmEpilogue, &sm.abort);
+                okw = mbar_wait(smem_addr(&sm.tmem_full), tl & 1, err, kErrGemmEpilogue, &sm.abort);
             if (!named_barrier_and(kBarEpilogue, kEpiWarps * 32, __shfl_sync(0xFFFFFFFFu, okw, 0) != 0)) break;
             tc_fence_after_sync();
             uint32_t v[4][32];
@@ -264,7 +289,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster_relaxed(leader_tmem_empty);
 
-            const int mt2 = t % g.tiles_m2, nt = t / g.tiles_m2;
+            int lt;
+            const int pj = task_of(t, &lt);
+            const GemmArgs& g = P.args[pj];
+            const int mt2 = lt % g.tiles_m2, nt = lt / g.tiles_m2;
             const int64_t row0 = static_cast<int64_t>(mt2) * 256 + rank * 128 + q * 32;
             const int64_t col0 = static_cast<int64_t>(nt) * 256 + h * 128;
             if (row0 >= g.M || col0 >= g.N) continue;
@@ -289,7 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d_hint(&cmap, static_cast<int32_t>(col0 + c * per), static_cast<int32_t>(row0),
+                        tma_store_2d_hint(&P.cmap[pj], static_cast<int32_t>(col0 + c * per), static_cast<int32_t>(row0),
                                           obuf, pol);
                         bulk_commit_group();
                     }
@@ -337,7 +365,7 @@ int gemm_pair_max_clusters() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev] > 0) return cached[dev];
     const size_t smem = gemm_pair_smem_bytes();
-    if (cudaFuncSetAttribute(gemm_mxf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(gemm_mxf4_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -345,17 +373,15 @@ int gemm_pair_max_clusters() {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel<true>, &cfg) != cudaSuccess) return 0;
     cached[dev] = n;
     return n;
 }
 
-cudaError_t launch_gemm_pair(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& cmap,
-                             const CUtensorMap& sfamap, const CUtensorMap& sfbmap, const GemmArgs& g,
-                             int clusters, cudaStream_t stream) {
+cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream) {
     const size_t smem = gemm_pair_smem_bytes();
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_mxf4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = b.count > 1 ? gemm_mxf4_pair_kernel<true> : gemm_mxf4_pair_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -367,7 +393,7 @@ cudaError_t launch_gemm_pair(const CUtensorMap& amap, const CUtensorMap& bmap, c
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_mxf4_pair_kernel, amap, bmap, cmap, sfamap, sfbmap, g);
+    return cudaLaunchKernelEx(&cfg, kernel, b);
 }
 
 }  // namespace mxfp4

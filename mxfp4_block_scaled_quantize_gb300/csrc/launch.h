@@ -71,14 +71,26 @@ constexpr int kGemmBN = 256;
 cudaError_t launch_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& cmap,
                         const GemmArgs& g, int grid, cudaStream_t stream);
 
-// The CTA-pair kernel (gemm_pair.cu): 256 x 256 tiles on clusters of two CTAs.  sfamap /
-// sfbmap: the A / B scale blobs as 2-D u64 tensors {Kp/128 * 64, ceil(rows/128)} (one row
-// per 128-row group of atoms), boxes {128, 1} / {128, 2}.  `clusters` CTA pairs.
+// The CTA-pair kernel (gemm_pair.cu): 256 x 256 tiles on clusters of two CTAs, over up to
+// kMaxGemmTasks independent problems in one launch (tile t belongs to the first problem j
+// with t < tile_end[j]).  Per problem: amap / bmap as for launch_gemm but with a B box of
+// 128 rows; sfamap / sfbmap: the A / B scale blobs as 2-D u64 tensors
+// {Kp/128 * 64, ceil(rows/128)} (one row per 128-row group of atoms), boxes {128, 1} /
+// {128, 2}; cmap as for launch_gemm.  `clusters` CTA pairs.
+constexpr int kMaxGemmTasks = 4;
+struct GemmPairBatch {
+    CUtensorMap amap[kMaxGemmTasks];
+    CUtensorMap bmap[kMaxGemmTasks];
+    CUtensorMap cmap[kMaxGemmTasks];
+    CUtensorMap sfamap[kMaxGemmTasks];
+    CUtensorMap sfbmap[kMaxGemmTasks];
+    GemmArgs args[kMaxGemmTasks];
+    int32_t tile_end[kMaxGemmTasks];
+    int32_t count;
+};
 size_t gemm_pair_smem_bytes();
 int gemm_pair_max_clusters();   // co-resident clusters of the pair kernel, 0 if none
-cudaError_t launch_gemm_pair(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& cmap,
-                             const CUtensorMap& sfamap, const CUtensorMap& sfbmap, const GemmArgs& g,
-                             int clusters, cudaStream_t stream);
+cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream);
 
 // ---- diagnostics -----------------------------------------------------------------------
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t timeout_ns, cudaStream_t stream);

@@ -64,6 +64,15 @@ class MXFP4Linear:
         abi.gemm(*self.dy_col, *self.x_col, self.N, self.K, self.M, out=self.dw, stream=stream)
         return self.dw
 
+    def bwd_gemms(self, stream=None):
+        """dgrad and wgrad in one launch (they read the same dY blobs)."""
+        code = abi.MXFP4_OUT_F32 if self.dx.dtype == torch.float32 else abi.MXFP4_OUT_BF16
+        abi.mxfp4_gemm_batch([
+            (*self.dy_row, *self.w_col, self.M, self.K, self.N, self.dx, self.dx.stride(0), code),
+            (*self.dy_col, *self.x_col, self.N, self.K, self.M, self.dw, self.dw.stride(0), code),
+        ], stream)
+        return self.dx, self.dw
+
     # -- a8: the whole step ---------------------------------------------------------------
     def quantize_xw(self, x, w, stream=None):
         """X and W in one launch (steps a1-a4 for both)."""
@@ -83,7 +92,7 @@ class MXFP4Linear:
     def backward(self, dy, stream=None):
         assert self.train, "backward needs the column blobs of the dual quantizer"
         self.quantize_dy(dy, stream)
-        return self.dgrad_gemm(stream), self.wgrad_gemm(stream)
+        return self.bwd_gemms(stream)
 
     def step(self, x, w, dy=None, stream=None):
         y = self.forward(x, w, stream)
@@ -139,14 +148,13 @@ class MXFP4Linear:
         if self.train:
             compute.wait_event(ready[2])
             self.quantize_dy(self._dy)
-            # wgrad first: its result (N x K) is the larger one to send back, so it starts
-            # back while dgrad runs and the step ends on the smaller dX copy.
-            send_back(self.wgrad_gemm(), hdw)
-            send_back(self.dgrad_gemm(), hdx)
+            self.bwd_gemms()
+            send_back(self.dw, hdw)
+            send_back(self.dx, hdx)
         compute.wait_stream(d2h)
         compute.wait_stream(h2d)
 
     # launches per step (for the benchmark's launch count)
     @property
     def launches_per_step(self) -> int:
-        return 5 if self.train else 2
+        return 4 if self.train else 2

@@ -73,6 +73,18 @@ def test_argument_checks_precede_any_device_use(lib):
     bad = (T * 2)(good, T(18, 4, 8, 8, 32, 48, 64, 80))            # x not 16-byte aligned
     assert lib.mxfp4_quantize_batch(2, bad, 1, 1, None) == abi.MXFP4_ERR_MISALIGNED
     assert lib.mxfp4_quantize_batch(1, arr, 1, 2, None) == abi.MXFP4_ERR_INVALID_ARG  # layout
+    G = abi.GemmTask
+    g_ok = G(16, 32, 48, 64, 4, 4, 4, 80, 4, 0)
+    garr = (G * 5)(*([g_ok] * 5))
+    assert lib.mxfp4_gemm_batch(0, garr, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_gemm_batch(5, garr, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_gemm_batch(1, None, None) == abi.MXFP4_ERR_INVALID_ARG
+    gbad = (G * 2)(g_ok, G(16, 32, 48, 64, 4, 4, 4, 80, 2, 0))     # ldc < N
+    assert lib.mxfp4_gemm_batch(2, gbad, None) == abi.MXFP4_ERR_INVALID_ARG
+    gbad = (G * 2)(g_ok, G(16, 32, 48, 64, 4, 4, 4, 88, 4, 0))     # c not 16-byte aligned
+    assert lib.mxfp4_gemm_batch(2, gbad, None) == abi.MXFP4_ERR_MISALIGNED
+    gbad = (G * 1)(G(16, 32, 48, 64, 4, 4, 4, 80, 4, 7))           # out dtype
+    assert lib.mxfp4_gemm_batch(1, gbad, None) == abi.MXFP4_ERR_INVALID_ARG
 
 
 def test_status_strings(lib):

@@ -107,6 +107,37 @@ def test_ragged_shapes(M, N, K, out_dtype):
     check_gemm(c_gpu, c, cabs, f"gemm {M}x{N}x{K}")
 
 
+def test_batch_equals_single_calls():
+    # One batched call over 1..4 problems (CTA-pair and one-CTA shapes, ragged edges, bf16
+    # and fp32 outputs, a pitched output) gives each problem exactly its own call's bytes.
+    probs = [(384, 768, 640, torch.bfloat16, 768), (129, 257, 384, torch.float32, 260),
+             (64, 1000, 4600, torch.bfloat16, 1000), (513, 255, 2048, torch.float32, 256)]
+    ins, singles = [], []
+    for i, (M, N, K, od, ldc) in enumerate(probs):
+        a = workloads.student_t3((M, K), 1.0, 101 + i)
+        b = workloads.normal((N, K), 0.5, 201 + i)
+        aq, a_s = abi.quantize(pitched(a), dual=False)
+        bq, b_s = abi.quantize(pitched(b), dual=False)
+        code = abi.MXFP4_OUT_F32 if od == torch.float32 else abi.MXFP4_OUT_BF16
+        ins.append((aq, a_s, bq, b_s, M, N, K, code))
+        ref = torch.full((M, ldc), float("nan"), dtype=od, device="cuda")
+        abi.mxfp4_gemm(aq, a_s, bq, b_s, M, N, K, ref, ldc, code)
+        singles.append(ref)
+    torch.cuda.synchronize()
+    for n in (1, 2, 4):
+        outs, tasks = [], []
+        for (aq, a_s, bq, b_s, M, N, K, code), ref in zip(ins[:n], singles[:n]):
+            out = torch.full(ref.shape, float("nan"), dtype=ref.dtype, device="cuda")
+            tasks.append((aq, a_s, bq, b_s, M, N, K, out, out.stride(0), code))
+            outs.append(out)
+        abi.mxfp4_gemm_batch(tasks)
+        torch.cuda.synchronize()
+        assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+        for out, ref in zip(outs, singles):
+            # byte-identical, the pitch tail (never written) included
+            assert torch.equal(out.view(torch.uint8).cpu(), ref.view(torch.uint8).cpu())
+
+
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_output_pitch_and_untouched_tail(out_dtype):
     M, N, K = 200, 300, 512
