@@ -7,7 +7,8 @@ quantization recipe flag off:
   backward  dual-quantize dY, dX = dY_row . (W_col)^T, dW = dY_col . (X_col)^T
 Only the column blobs of X and W need to live from forward to backward; bf16 X and W are
 not kept.  All buffers are allocated once (torch as the allocator) and reused, so a step
-is just six launches on one stream.
+is four launches on one stream: X and W quantized together, the forward GEMM, dY, and
+dgrad with wgrad in one GEMM launch.
 """
 import torch
 
