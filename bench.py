@@ -69,8 +69,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {
-    "gemm_mxf4_kernel": ("gemm.cu", "ptx.cuh", "launch.h"),
-    "gemm_mxf4_pair_kernel": ("gemm_pair.cu", "ptx.cuh", "launch.h"),
+    "gemm_mxf4_kernel": ("gemm.cu", "epilogue.cuh", "ptx.cuh", "launch.h"),
+    "gemm_mxf4_pair_kernel": ("gemm_pair.cu", "epilogue.cuh", "ptx.cuh", "launch.h"),
     "quantize_kernel": ("quantize.cu", "ptx.cuh", "launch.h"),
 }
 
@@ -184,6 +184,7 @@ def run_ours(args, rank, world, local_rank):
     x, w = t["X"].to(dev), t["W"].to(dev)
     dy = t["dY"].to(dev) if lin.train else None
     layer = MXFP4Linear(M, N, K, train=lin.train, device=dev)
+    bias = (workloads.normal((N,), 0.02, 977).to(dev) if args.bias else None)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_src = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
@@ -201,7 +202,7 @@ def run_ours(args, rank, world, local_rank):
         evs[0].record(stream)
         layer.quantize_xw(x, w)
         evs[1].record(stream)
-        layer.fwd_gemm()
+        layer.fwd_gemm(bias=bias)
         evs[2].record(stream)
         if lin.train:
             layer.quantize_dy(dy)
@@ -215,7 +216,7 @@ def run_ours(args, rank, world, local_rank):
 
     for _ in range(args.warmup):
         flush_l2()
-        layer.step(x, w, dy)
+        layer.step(x, w, dy, bias=bias)
     torch.cuda.synchronize()
     if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
         raise RuntimeError("device error word set during warm-up")
@@ -240,7 +241,7 @@ def run_ours(args, rank, world, local_rank):
     for k in range(args.steps):
         flush_l2()
         step_events[k][0].record(stream)
-        layer.step(x, w, dy)
+        layer.step(x, w, dy, bias=bias)
         step_events[k][1].record(stream)
     torch.cuda.synchronize()
     t_end = time.time()
@@ -275,13 +276,13 @@ def run_ours(args, rank, world, local_rank):
     d2h = sum(o.numel() * o.element_size() for o in houts if o is not None)
     e2e_steps = max(3, min(args.steps, 20))
     for _ in range(2):
-        layer.step_host(hx, hw, hdy, *houts)
+        layer.step_host(hx, hw, hdy, *houts, bias=bias)
     torch.cuda.synchronize()
     e_ms = []
     for _ in range(e2e_steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        layer.step_host(hx, hw, hdy, *houts)
+        layer.step_host(hx, hw, hdy, *houts, bias=bias)
         e1.record(stream)
         e1.synchronize()
         e_ms.append(e0.elapsed_time(e1))
@@ -339,7 +340,8 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "fp4_e2m1 (e8m0 block scales, fp32 accumulate, bf16 out)",
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(0,1e-3) grads)",
         "config": {"workload": args.workload, "M": M, "N": N, "K": K,
-                   "step": "dual-quant X,W; fwd; dual-quant dY; dgrad; wgrad" if lin.train
+                   "step": ("dual-quant X,W; fwd" + (" + bias" if args.bias else "") +
+                            "; dual-quant dY; dgrad; wgrad") if lin.train
                    else "row-quant X,W; fwd",
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then "
                          f"{L2_FLUSH_BYTES >> 20} MiB read)",
@@ -467,6 +469,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--bias", action="store_true",
+                    help="the forward adds the layer's bf16 bias inside the GEMM (the "
+                         "`output + bias` that follows the GEMM in the layer's forward)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -136,7 +136,21 @@ mxfp4_status mxfp4_gemm(const void* a_q, const void* a_s, const void* b_q, const
                         int64_t M, int64_t N, int64_t K, void* c, int64_t ldc,
                         mxfp4_out_dtype out_dtype, mxfp4_stream_t stream);
 
-/* One GEMM of a batch: the arguments of mxfp4_gemm. */
+/* mxfp4_gemm followed by the layer's bias add, in the same launch: the `output + bias`
+ * of `_forward_impl` in MXFP4ColumnParallelLinear / MXFP4RowParallelLinear
+ * (primus_turbo_mxfp4_local.py), which adds the bf16 bias vector to every row of the GEMM
+ * output.  C[m,n] = out(out(A.B^T [m,n]) + bias[n]) with the same two roundings as the
+ * unfused pair of operations: out() rounds to the output dtype to nearest even, and the
+ * add itself is done in fp32 (bf16 output: the GEMM result is rounded to bf16 first;
+ * fp32 output: the fp32 sum).
+ *   bias  bf16[N], 16-byte aligned, not NULL (MXFP4_ERR_INVALID_ARG); read only.
+ * Everything else as mxfp4_gemm. */
+mxfp4_status mxfp4_gemm_bias(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                             int64_t M, int64_t N, int64_t K, const void* bias, void* c,
+                             int64_t ldc, mxfp4_out_dtype out_dtype, mxfp4_stream_t stream);
+
+/* One GEMM of a batch: the arguments of mxfp4_gemm, and an optional bias (NULL: none;
+ * otherwise as for mxfp4_gemm_bias). */
 typedef struct {
     const void* a_q;
     const void* a_s;
@@ -148,6 +162,7 @@ typedef struct {
     void* c;
     int64_t ldc;
     mxfp4_out_dtype out_dtype;
+    const void* bias;
 } mxfp4_gemm_task;
 
 /* 1..MXFP4_MAX_BATCH independent GEMMs, each with exactly the result its own mxfp4_gemm

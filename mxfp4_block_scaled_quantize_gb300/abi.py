@@ -33,7 +33,7 @@ class GemmTask(ctypes.Structure):
     _fields_ = [("a_q", ctypes.c_void_p), ("a_s", ctypes.c_void_p), ("b_q", ctypes.c_void_p),
                 ("b_s", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
                 ("K", ctypes.c_int64), ("c", ctypes.c_void_p), ("ldc", ctypes.c_int64),
-                ("out_dtype", ctypes.c_int)]
+                ("out_dtype", ctypes.c_int), ("bias", ctypes.c_void_p)]
 
 
 class QuantizeTask(ctypes.Structure):
@@ -48,6 +48,7 @@ EXPORTED = (
     "mxfp4_quantize_dual",
     "mxfp4_quantize_batch",
     "mxfp4_gemm",
+    "mxfp4_gemm_bias",
     "mxfp4_gemm_batch",
     "mxfp4_last_device_error",
     "mxfp4_selftest_bounded_wait",
@@ -81,6 +82,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_quantize_dual.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, vp]
     lib.mxfp4_quantize_batch.argtypes = [i32, ctypes.POINTER(QuantizeTask), i32, i32, vp]
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
+    lib.mxfp4_gemm_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i32, vp]
     lib.mxfp4_gemm_batch.argtypes = [i32, ctypes.POINTER(GemmTask), vp]
     lib.mxfp4_last_device_error.argtypes = [vp]
     lib.mxfp4_selftest_bounded_wait.argtypes = [i64, vp]
@@ -157,11 +159,19 @@ def mxfp4_gemm(a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype=MXFP4_OUT_BF16, st
                              out_dtype, _stream(stream)), "mxfp4_gemm")
 
 
+def mxfp4_gemm_bias(a_q, a_s, b_q, b_s, M, N, K, bias, c, ldc, out_dtype=MXFP4_OUT_BF16,
+                    stream=None) -> None:
+    _check(load().mxfp4_gemm_bias(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, _ptr(bias),
+                                  _ptr(c), ldc, out_dtype, _stream(stream)), "mxfp4_gemm_bias")
+
+
 def mxfp4_gemm_batch(tasks, stream=None) -> None:
-    """tasks: sequence of (a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype)."""
+    """tasks: sequence of (a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype[, bias])."""
     arr = (GemmTask * max(1, len(tasks)))()
-    for i, (a_q, a_s, b_q, b_s, M, N, K, c, ldc, od) in enumerate(tasks):
-        arr[i] = GemmTask(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, _ptr(c), ldc, od)
+    for i, t in enumerate(tasks):
+        a_q, a_s, b_q, b_s, M, N, K, c, ldc, od = t[:10]
+        bias = t[10] if len(t) > 10 else None
+        arr[i] = GemmTask(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, _ptr(c), ldc, od, _ptr(bias))
     _check(load().mxfp4_gemm_batch(len(tasks), arr, _stream(stream)), "mxfp4_gemm_batch")
 
 
@@ -211,12 +221,17 @@ def quantize(x, dual: bool = True, layout: int = MXFP4_SCALE_TC, stream=None):
     return rq, rs, cq, cs
 
 
-def gemm(a_q, a_s, b_q, b_s, M, N, K, out_dtype=None, out=None, stream=None):
-    """C[M,N] = A . B^T from two K-packed blobs with tensor-core-layout scales."""
+def gemm(a_q, a_s, b_q, b_s, M, N, K, out_dtype=None, out=None, stream=None, bias=None):
+    """C[M,N] = A . B^T (+ bias[N], a contiguous bf16 vector, when given) from two K-packed
+    blobs with tensor-core-layout scales."""
     import torch
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a_q.device)
     code = MXFP4_OUT_F32 if out.dtype == torch.float32 else MXFP4_OUT_BF16
     assert out.dtype in (torch.float32, torch.bfloat16) and out.stride(1) == 1
-    mxfp4_gemm(a_q, a_s, b_q, b_s, M, N, K, out, out.stride(0), code, stream)
+    if bias is None:
+        mxfp4_gemm(a_q, a_s, b_q, b_s, M, N, K, out, out.stride(0), code, stream)
+    else:
+        assert bias.dtype == torch.bfloat16 and bias.is_contiguous() and bias.numel() == N
+        mxfp4_gemm_bias(a_q, a_s, b_q, b_s, M, N, K, bias, out, out.stride(0), code, stream)
     return out

@@ -169,7 +169,8 @@ mxfp4_status gemm_check(const mxfp4_gemm_task& t) {
         return MXFP4_ERR_INVALID_ARG;
     if (t.ldc < t.N || t.ldc > kMaxDim) return MXFP4_ERR_INVALID_ARG;
     if (t.out_dtype != MXFP4_OUT_BF16 && t.out_dtype != MXFP4_OUT_F32) return MXFP4_ERR_INVALID_ARG;
-    if (!aligned16(t.a_q) || !aligned16(t.a_s) || !aligned16(t.b_q) || !aligned16(t.b_s) || !aligned16(t.c))
+    if (!aligned16(t.a_q) || !aligned16(t.a_s) || !aligned16(t.b_q) || !aligned16(t.b_s) || !aligned16(t.c) ||
+        (t.bias != nullptr && !aligned16(t.bias)))
         return MXFP4_ERR_MISALIGNED;
     const int64_t tiles = cdiv(t.M, mxfp4::kGemmBM) * cdiv(t.N, mxfp4::kGemmBN);
     if (tiles > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;
@@ -211,6 +212,7 @@ mxfp4_status gemm_fill(const mxfp4_gemm_task& t, DeviceState* dev, mxfp4::GemmAr
     g->ldc = t.ldc;
     g->out_f32 = t.out_dtype == MXFP4_OUT_F32 ? 1 : 0;
     g->c_tma = c_tma ? 1 : 0;
+    g->bias = static_cast<const uint16_t*>(t.bias);
     g->err = dev->err;
     return MXFP4_OK;
 }
@@ -297,7 +299,15 @@ mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* task
 
 mxfp4_status mxfp4_gemm(const void* a_q, const void* a_s, const void* b_q, const void* b_s, int64_t M, int64_t N,
                         int64_t K, void* c, int64_t ldc, mxfp4_out_dtype out_dtype, mxfp4_stream_t stream) {
-    const mxfp4_gemm_task t{a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype};
+    const mxfp4_gemm_task t{a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype, nullptr};
+    return mxfp4_gemm_batch(1, &t, stream);
+}
+
+mxfp4_status mxfp4_gemm_bias(const void* a_q, const void* a_s, const void* b_q, const void* b_s, int64_t M,
+                             int64_t N, int64_t K, const void* bias, void* c, int64_t ldc, mxfp4_out_dtype out_dtype,
+                             mxfp4_stream_t stream) {
+    if (bias == nullptr) return MXFP4_ERR_INVALID_ARG;
+    const mxfp4_gemm_task t{a_q, a_s, b_q, b_s, M, N, K, c, ldc, out_dtype, bias};
     return mxfp4_gemm_batch(1, &t, stream);
 }
 

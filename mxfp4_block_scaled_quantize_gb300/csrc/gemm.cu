@@ -34,6 +34,7 @@
 // Every wait is bounded (see ptx.cuh); a wait that runs out stops the CTA cleanly.
 #include <cuda_bf16.h>
 
+#include "epilogue.cuh"
 #include "launch.h"
 #include "ptx.cuh"
 
@@ -86,11 +87,6 @@ __device__ __forceinline__ uint32_t mma_idesc(uint32_t sf_id) {
     d |= static_cast<uint32_t>(BM >> 4) << 24;
     d |= sf_id << 29;                         // A scale-factor byte selector
     return d;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
-    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -283,13 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) bulk_wait_read_all();   // the buffer's previous store has read it
                     __syncwarp();
                     uint32_t w[16];
-                    if (g.out_f32) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) w[i] = v[(c >> 1) & 3][(c & 1) * 16 + i];
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[c & 3][2 * i], v[c & 3][2 * i + 1]);
-                    }
+                    if (g.out_f32)
+                        convert_piece<true>(&v[(c >> 1) & 3][(c & 1) * 16], g.bias, col0 + c * per, g.N, w);
+                    else
+                        convert_piece<false>(v[c & 3], g.bias, col0 + c * per, g.N, w);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         sts128(obuf + swz64(lane, j), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
@@ -311,14 +304,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = __float2bfloat16_rn(__uint_as_float(v[c4][j]));
+                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = out_bf16(v[c4][j], g.bias, col0 + c4 * 32 + j);
             } else {
                 float* dst = reinterpret_cast<float*>(g.c) + row * g.ldc + col0;
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = __uint_as_float(v[c4][j]);
+                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = out_f32(v[c4][j], g.bias, col0 + c4 * 32 + j);
             }
         }
         // Every TMA store of this warp is complete before the CTA may leave.

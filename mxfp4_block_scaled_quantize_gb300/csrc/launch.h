@@ -58,6 +58,7 @@ struct GemmArgs {
     int64_t ldc;
     int32_t out_f32;     // 1: fp32 output, 0: bf16
     int32_t c_tma;       // 1: cmap describes C (TMA stores), 0: plain stores
+    const uint16_t* bias;  // bf16 bias[N] added to every row (16-byte aligned), or null
     uint32_t* err;
 };
 

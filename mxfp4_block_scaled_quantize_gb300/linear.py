@@ -53,8 +53,10 @@ class MXFP4Linear:
                                 abi.MXFP4_SCALE_TC, stream)
 
     # -- steps a5..a7 ---------------------------------------------------------------------
-    def fwd_gemm(self, stream=None):
-        abi.gemm(*self.x_row, *self.w_row, self.M, self.N, self.K, out=self.y, stream=stream)
+    def fwd_gemm(self, stream=None, bias=None):
+        """Y = X . W^T, plus the layer's bf16 bias[N] fused into the GEMM's output when given
+        (the `output + bias` that follows the GEMM in `_forward_impl`)."""
+        abi.gemm(*self.x_row, *self.w_row, self.M, self.N, self.K, out=self.y, stream=stream, bias=bias)
         return self.y
 
     def dgrad_gemm(self, stream=None):
@@ -86,24 +88,24 @@ class MXFP4Linear:
                      (w, N, K, w.stride(0), *self.w_row, None, None)]
         abi.mxfp4_quantize_batch(tasks, self.train, abi.MXFP4_SCALE_TC, stream)
 
-    def forward(self, x, w, stream=None):
+    def forward(self, x, w, stream=None, bias=None):
         self.quantize_xw(x, w, stream)
-        return self.fwd_gemm(stream)
+        return self.fwd_gemm(stream, bias)
 
     def backward(self, dy, stream=None):
         assert self.train, "backward needs the column blobs of the dual quantizer"
         self.quantize_dy(dy, stream)
         return self.bwd_gemms(stream)
 
-    def step(self, x, w, dy=None, stream=None):
-        y = self.forward(x, w, stream)
+    def step(self, x, w, dy=None, stream=None, bias=None):
+        y = self.forward(x, w, stream, bias)
         if not self.train:
             return (y,)
         dx, dw = self.backward(dy, stream)
         return y, dx, dw
 
     # -- the step from pinned host buffers to pinned host buffers --------------------------
-    def step_host(self, hx, hw, hdy=None, hy=None, hdx=None, hdw=None):
+    def step_host(self, hx, hw, hdy=None, hy=None, hdx=None, hdw=None, bias=None):
         """One step with bf16 inputs in pinned host memory and results copied back to pinned
         host memory.  Host-to-device copies run on one copy stream, device-to-host copies on
         another, and the kernels on the current stream; each kernel waits only for the copy
@@ -145,7 +147,7 @@ class MXFP4Linear:
         compute.wait_event(ready[0])
         compute.wait_event(ready[1])
         self.quantize_xw(self._x, self._w)
-        send_back(self.fwd_gemm(), hy)
+        send_back(self.fwd_gemm(bias=bias), hy)
         if self.train:
             compute.wait_event(ready[2])
             self.quantize_dy(self._dy)

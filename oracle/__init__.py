@@ -7,7 +7,8 @@ CUDA library.  The arithmetic and the passages it follows are documented in
 mxfp4_oracle.c; this module only marshals numpy arrays.
 
 Parity status: every function here is pinned by the oracle self-tests
-(tests/test_oracle_*.py) except the tensor-core scale layout, whose byte positions are a
+(tests/test_oracle_*.py; the bias add against torch's own CPU elementwise add, the
+operation the layer performs) except the tensor-core scale layout, whose byte positions are a
 layout of this library's own choosing; that permutation is pinned on the CPU only as a
 bijection, and against the hardware by the GEMM parity tests.
 """
@@ -48,6 +49,9 @@ def _load():
         lib.oracle_gemm_f64.restype = None
         lib.oracle_round_to_bf16.argtypes = [vp, vp, i64]
         lib.oracle_round_to_bf16.restype = None
+        for fn in (lib.oracle_bias_add_bf16, lib.oracle_bias_add_f32):
+            fn.argtypes = [vp, vp, i64, i64, vp]
+            fn.restype = None
         _lib = lib
     return _lib
 
@@ -169,4 +173,29 @@ def round_to_bf16(x):
     x = np.ascontiguousarray(x, dtype=np.float64)
     out = np.empty(x.shape, np.uint16)
     _load().oracle_round_to_bf16(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def round_to_f32(x):
+    """fp64 -> binary32, one round-to-nearest-even (numpy's cast)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float32)
+
+
+def bias_add(y, bias_bits):
+    """The layer's `output + bias` after the GEMM: y is the GEMM output already in its
+    dtype (bf16 bit patterns as uint16 [M, N], or float32 [M, N]), bias_bits the bf16 bias
+    [N] as uint16.  Returns the same dtype as y."""
+    bias_bits = np.ascontiguousarray(bias_bits, dtype=np.uint16)
+    if y.dtype == np.uint16:
+        y = np.ascontiguousarray(y)
+        M, N = y.shape
+        assert bias_bits.shape == (N,)
+        out = np.empty((M, N), np.uint16)
+        _load().oracle_bias_add_bf16(_ptr(y), _ptr(bias_bits), M, N, _ptr(out))
+        return out
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    M, N = y.shape
+    assert bias_bits.shape == (N,)
+    out = np.empty((M, N), np.float32)
+    _load().oracle_bias_add_f32(_ptr(y), _ptr(bias_bits), M, N, _ptr(out))
     return out

@@ -222,3 +222,34 @@ void oracle_round_to_bf16(const double* in, uint16_t* out, int64_t n) {
         out[i] = sign | (uint16_t)(u >> 16);
     }
 }
+
+/* The layer's bias add after the GEMM: `output + bias` in `_forward_impl` of
+ * MXFP4ColumnParallelLinear / MXFP4RowParallelLinear (primus_turbo_mxfp4_local.py), where
+ * `output` is the GEMM result already in the output dtype and `bias` a bf16 vector added
+ * to every row.  Computed the way an elementwise add of those dtypes is defined: both
+ * operands widened exactly to binary32, one binary32 addition (round to nearest even),
+ * and for a bf16 result one more round-to-nearest-even to bf16.  y and out are [M, N]
+ * row-major; bias is [N]. */
+static float bf16_bits_to_f32(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+void oracle_bias_add_bf16(const uint16_t* y, const uint16_t* bias, int64_t M, int64_t N, uint16_t* out) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            volatile float s = bf16_bits_to_f32(y[m * N + n]) + bf16_bits_to_f32(bias[n]);
+            double d = (double)s;
+            oracle_round_to_bf16(&d, &out[m * N + n], 1);
+        }
+}
+
+void oracle_bias_add_f32(const float* y, const uint16_t* bias, int64_t M, int64_t N, float* out) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            volatile float s = y[m * N + n] + bf16_bits_to_f32(bias[n]);
+            out[m * N + n] = s;
+        }
+}

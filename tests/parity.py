@@ -134,3 +134,44 @@ def oracle_gemm_rows(a_q, a_s_plain, b_q, b_s_plain, rows):
     a = oracle.dequantize(a_q[rows], a_s_plain[rows])
     b = oracle.dequantize(b_q, b_s_plain)
     return oracle.gemm_dequantized(a, b)
+
+
+def _bf16_from_key(k: np.ndarray) -> np.ndarray:
+    k = np.asarray(k, np.int64)
+    return np.where(k >= 0, k, 0x8000 | (-k)).astype(np.uint16)
+
+
+def check_gemm_bias(c_gpu: torch.Tensor, c_ref: np.ndarray, cabs: np.ndarray, bias_bits: np.ndarray,
+                    what: str) -> dict:
+    """GEMM output with the fused bias add (the layer's `output + bias`).  The oracle applies
+    its bias add to its own GEMM result in the output dtype:
+      - fp32: |gpu - oracle| <= 1e-5 * sum|ab| + one fp32 spacing at the result;
+      - bf16: the GPU value is the oracle's bias add of the oracle's bf16 GEMM output or of
+        one of its two bf16 neighbours (the GEMM is allowed 1 ulp), or, where the GEMM
+        nearly cancels, within 1e-5 * sum|ab| plus two bf16 ulps of the fp64 value."""
+    bias_vals = (bias_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if c_gpu.dtype == torch.float32:
+        y_o = oracle.bias_add(oracle.round_to_f32(c_ref), bias_bits).astype(np.float64)
+        g = c_gpu.cpu().numpy().astype(np.float64)
+        mag = np.maximum(np.abs(g), np.abs(y_o)).astype(np.float32)
+        bound = FP32_REL * cabs + np.spacing(mag).astype(np.float64)
+        bad = np.abs(g - y_o) > bound
+        if bad.any():
+            i = tuple(np.argwhere(bad)[0])
+            raise AssertionError(f"{what}: {bad.sum()} fp32 outputs out of bound; first {i}: "
+                                 f"gpu {g[i]!r} oracle {y_o[i]!r} bound {bound[i]!r}")
+        return {"n": int(g.size)}
+    gbits = c_gpu.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    key = bf16_key(oracle.round_to_bf16(c_ref))
+    cands = [oracle.bias_add(_bf16_from_key(key + d), bias_bits) for d in (0, -1, 1)]
+    exact = gbits == cands[0]
+    ok = exact | (gbits == cands[1]) | (gbits == cands[2])
+    g = (gbits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = c_ref + bias_vals[None, :]
+    near = np.abs(g - ref) <= FP32_REL * cabs + 2 * bf16_ulp(np.maximum(np.abs(c_ref), np.abs(ref)))
+    bad = ~ok & ~near
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what}: {bad.sum()} bf16 outputs not admissible; first {i}: gpu {g[i]!r} "
+                             f"gemm {c_ref[i]!r} bias {bias_vals[i[1]]!r}")
+    return {"exact": int(exact.sum()), "n": int(exact.size)}

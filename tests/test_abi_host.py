@@ -85,6 +85,12 @@ def test_argument_checks_precede_any_device_use(lib):
     assert lib.mxfp4_gemm_batch(2, gbad, None) == abi.MXFP4_ERR_MISALIGNED
     gbad = (G * 1)(G(16, 32, 48, 64, 4, 4, 4, 80, 4, 7))           # out dtype
     assert lib.mxfp4_gemm_batch(1, gbad, None) == abi.MXFP4_ERR_INVALID_ARG
+    gbad = (G * 2)(g_ok, G(16, 32, 48, 64, 4, 4, 4, 80, 4, 0, 104))  # bias not 16-byte aligned
+    assert lib.mxfp4_gemm_batch(2, gbad, None) == abi.MXFP4_ERR_MISALIGNED
+    # the bias entry point: bias required and 16-byte aligned, then the GEMM's own checks
+    assert lib.mxfp4_gemm_bias(16, 32, 48, 64, 4, 4, 4, None, 80, 4, 0, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_gemm_bias(16, 32, 48, 64, 4, 4, 4, 104, 80, 4, 0, None) == abi.MXFP4_ERR_MISALIGNED
+    assert lib.mxfp4_gemm_bias(16, 32, 48, 64, 4, 4, 4, 96, 80, 2, 0, None) == abi.MXFP4_ERR_INVALID_ARG
 
 
 def test_status_strings(lib):

@@ -11,7 +11,7 @@ import torch
 import oracle
 from mxfp4_block_scaled_quantize_gb300 import abi, workloads
 from mxfp4_block_scaled_quantize_gb300.linear import MXFP4Linear
-from parity import check_gemm
+from parity import check_gemm, check_gemm_bias
 
 pytestmark = pytest.mark.gpu
 
@@ -105,6 +105,79 @@ def test_ragged_shapes(M, N, K, out_dtype):
     c_gpu = gpu_gemm_from_bf16(a, b, out_dtype)
     c, cabs = oracle_gemm_from_bf16(a, b)
     check_gemm(c_gpu, c, cabs, f"gemm {M}x{N}x{K}")
+
+
+def bias_bf16(N, seed):
+    """A bf16 bias vector with magnitudes spread over 2^-8 .. 2^8 (as uint16 bits and a
+    CUDA tensor)."""
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal(N) * np.ldexp(1.0, rng.integers(-8, 9, N))
+    bits = oracle.round_to_bf16(v)
+    t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+    return bits, t
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 32), (200, 300, 40), (129, 257, 384), (64, 1000, 4600),
+                                   (384, 768, 640), (513, 255, 2048)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_gemm_bias(M, N, K, out_dtype):
+    # The fused `output + bias` against the oracle's GEMM followed by its bias add; N not a
+    # multiple of 8 exercises the bias reads at the ragged right edge.
+    a = workloads.student_t3((M, K), 1.0, 31 + M + 3 * N + 7 * K)
+    b = workloads.normal((N, K), 0.5, 37 + M + 5 * N + 11 * K)
+    bits, bias = bias_bf16(N, M + N + K)
+    aq, a_s = abi.quantize(pitched(a), dual=False)
+    bq, b_s = abi.quantize(pitched(b), dual=False)
+    out = abi.gemm(aq, a_s, bq, b_s, M, N, K, out_dtype=out_dtype, bias=bias)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    c, cabs = oracle_gemm_from_bf16(a, b)
+    check_gemm_bias(out, c, cabs, bits, f"gemm+bias {M}x{N}x{K}")
+
+
+def test_flux_mlp_forward_bias_sampled():
+    # Full Flux-12B MLP up-projection forward (M 4608, N 12288, K 3072) with the layer's
+    # bias, in the launch configuration of the forward step; sampled output rows.
+    wl = workloads.FLUX_MLP_STEP
+    lin = wl.linears[0]
+    t = wl.tensors(0)
+    bits, bias = bias_bf16(lin.N, 7)
+    layer = MXFP4Linear(lin.M, lin.N, lin.K, train=False)
+    layer.quantize_xw(t["X"].cuda(), t["W"].cuda())
+    y = layer.fwd_gemm(bias=bias)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    rows = np.array([0, 1, 127, 128, 255, 256, 2047, 3333, 4480, 4607])
+    c, cabs = oracle_gemm_from_bf16(t["X"], t["W"], rows=rows)
+    check_gemm_bias(y[torch.as_tensor(rows, device="cuda")], c, cabs, bits, "flux mlp fwd + bias")
+
+
+def test_batch_with_bias_equals_single_calls():
+    # Batched problems with and without a bias give each problem its own call's bytes.
+    probs = [(384, 768, 640, torch.bfloat16, True), (129, 257, 384, torch.float32, True),
+             (513, 255, 2048, torch.float32, False), (256, 520, 1000, torch.bfloat16, True)]
+    tasks, outs, refs = [], [], []
+    for i, (M, N, K, od, with_bias) in enumerate(probs):
+        a = workloads.student_t3((M, K), 1.0, 301 + i)
+        b = workloads.normal((N, K), 0.5, 401 + i)
+        aq, a_s = abi.quantize(pitched(a), dual=False)
+        bq, b_s = abi.quantize(pitched(b), dual=False)
+        code = abi.MXFP4_OUT_F32 if od == torch.float32 else abi.MXFP4_OUT_BF16
+        bias = bias_bf16(N, 501 + i)[1] if with_bias else None
+        ref = torch.full((M, N), float("nan"), dtype=od, device="cuda")
+        if with_bias:
+            abi.mxfp4_gemm_bias(aq, a_s, bq, b_s, M, N, K, bias, ref, N, code)
+        else:
+            abi.mxfp4_gemm(aq, a_s, bq, b_s, M, N, K, ref, N, code)
+        out = torch.full((M, N), float("nan"), dtype=od, device="cuda")
+        tasks.append((aq, a_s, bq, b_s, M, N, K, out, N, code, bias))
+        outs.append(out)
+        refs.append(ref)
+    abi.mxfp4_gemm_batch(tasks)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    for out, ref in zip(outs, refs):
+        assert torch.equal(out.view(torch.uint8).cpu(), ref.view(torch.uint8).cpu())
 
 
 def test_batch_equals_single_calls():

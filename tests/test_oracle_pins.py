@@ -318,3 +318,82 @@ def test_round_to_bf16_midpoints():
         assert got[3] == (even | 0x8000)
         assert got[4] == b[i]
     assert oracle.round_to_bf16(np.array([0.0, -0.0]))[1] == 0x8000
+
+
+# --- the layer's bias add after the GEMM (`output + bias` in `_forward_impl`) ---------------
+
+def _finite_bf16_patterns(shape, rng):
+    """Random finite bf16 bit patterns covering every exponent, zeros and subnormals."""
+    b = rng.integers(0, 0x10000, size=shape, dtype=np.uint32).astype(np.uint16)
+    nonfinite = (b & 0x7F80) == 0x7F80
+    b[nonfinite] &= 0xBFFF          # exponent 0xFF -> 0xBF: finite
+    flat = b.reshape(-1)
+    flat[:8] = [0x0000, 0x8000, 0x0001, 0x8001, 0x3F80, 0xBF80, 0x7F7F, 0xFF7F]
+    return b
+
+
+def _torch_bf16(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def test_bias_add_bf16_equals_torch_cpu_add():
+    # Pinned to the operation the layer runs: torch's own elementwise add of a bf16 output
+    # and a bf16 bias broadcast over rows, on the CPU.
+    import torch
+    rng = np.random.default_rng(17)
+    y = _finite_bf16_patterns((64, 96), rng)
+    bias = _finite_bf16_patterns((96,), rng)
+    got = oracle.bias_add(y, bias)
+    with np.errstate(over="ignore"):
+        want = (_torch_bf16(y) + _torch_bf16(bias)).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_bias_add_f32_equals_torch_cpu_add():
+    # fp32 output plus a bf16 bias: torch promotes the bias to fp32 and adds in fp32.
+    import torch
+    rng = np.random.default_rng(18)
+    y = rng.standard_normal((32, 80)).astype(np.float32) * np.float32(2.0) ** rng.integers(
+        -30, 30, (32, 80)).astype(np.float32)
+    bias = _finite_bf16_patterns((80,), rng)
+    got = oracle.bias_add(y, bias)
+    want = (torch.from_numpy(y) + _torch_bf16(bias)).numpy()
+    assert want.dtype == np.float32
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_bias_add_bf16_is_one_rounding_of_the_exact_sum():
+    # Two bf16 operands (8-bit significands) added in binary32 (24 bits) and rounded again
+    # to bf16: since 24 >= 2*8 + 2, the double rounding is innocuous and the result is the
+    # exact sum rounded once to bf16.  Checked where the fp64 sum is exact (exponents within
+    # 40 of each other), against the oracle's own single rounding of that fp64 sum.
+    rng = np.random.default_rng(19)
+    e1 = rng.integers(-120, 120, 4000)
+    d = rng.integers(-40, 41, 4000)
+    m1 = rng.integers(128, 256, 4000)
+    m2 = rng.integers(128, 256, 4000)
+    s1 = rng.choice([-1.0, 1.0], 4000)
+    s2 = rng.choice([-1.0, 1.0], 4000)
+    a = s1 * np.ldexp(m1.astype(np.float64), e1 - 7)
+    b = s2 * np.ldexp(m2.astype(np.float64), np.clip(e1 + d, -126, 127) - 7)
+    ab = oracle.round_to_bf16(a)
+    bb = oracle.round_to_bf16(b)
+    assert np.array_equal(f32_bits_to_bf16_values(ab), a) and np.array_equal(f32_bits_to_bf16_values(bb), b)
+    got = np.array([oracle.bias_add(ab[i:i + 1].reshape(1, 1), bb[i:i + 1])[0, 0] for i in range(4000)])
+    want = oracle.round_to_bf16(a + b)      # fp64 sum is exact here
+    plus_zero = (a + b) == 0                 # x + (-x) is +0 in round-to-nearest
+    assert np.array_equal(got[~plus_zero], want[~plus_zero])
+    assert np.all(got[plus_zero] == 0x0000)
+
+
+def test_bias_add_zero_bias_is_identity_except_negative_zero():
+    rng = np.random.default_rng(20)
+    y = _finite_bf16_patterns((16, 64), rng)
+    got = oracle.bias_add(y, np.zeros(64, np.uint16))
+    neg_zero = y == 0x8000
+    assert np.array_equal(got[~neg_zero], y[~neg_zero])
+    assert np.all(got[neg_zero] == 0x0000)   # -0 + +0 = +0
+    yf = np.array([[1.5, -0.0, 3e-39, -7.25]], np.float32)
+    gotf = oracle.bias_add(yf, np.zeros(4, np.uint16))
+    assert np.array_equal(gotf.view(np.uint32), np.array([[1.5, 0.0, 3e-39, -7.25]], np.float32).view(np.uint32))
