@@ -198,14 +198,17 @@ def run_ours(args, rank, world, local_rank):
     names = (["quant_dual_XW", "gemm_fwd", "quant_dual_dY", "gemm_dgrad_wgrad"]
              if lin.train else ["quant_row_XW", "gemm_fwd"])
 
-    def step_with_events(evs):
+    def sr_seed(k):
+        return (0x5EED0000 + k) if args.sr else None
+
+    def step_with_events(evs, k):
         evs[0].record(stream)
         layer.quantize_xw(x, w)
         evs[1].record(stream)
         layer.fwd_gemm(bias=bias)
         evs[2].record(stream)
         if lin.train:
-            layer.quantize_dy(dy)
+            layer.quantize_dy(dy, sr_seed=sr_seed(k))
             evs[3].record(stream)
             layer.bwd_gemms()
             evs[4].record(stream)
@@ -214,9 +217,9 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
 
-    for _ in range(args.warmup):
+    for i in range(args.warmup):
         flush_l2()
-        layer.step(x, w, dy, bias=bias)
+        layer.step(x, w, dy, bias=bias, sr_seed=sr_seed(i))
     torch.cuda.synchronize()
     if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
         raise RuntimeError("device error word set during warm-up")
@@ -241,7 +244,7 @@ def run_ours(args, rank, world, local_rank):
     for k in range(args.steps):
         flush_l2()
         step_events[k][0].record(stream)
-        layer.step(x, w, dy, bias=bias)
+        layer.step(x, w, dy, bias=bias, sr_seed=sr_seed(k))
         step_events[k][1].record(stream)
     torch.cuda.synchronize()
     t_end = time.time()
@@ -252,7 +255,7 @@ def run_ours(args, rank, world, local_rank):
     head_start()
     for k in range(args.steps):
         flush_l2()
-        step_with_events(events[k])
+        step_with_events(events[k], k)
     torch.cuda.synchronize()
     t_end2 = time.time()
     barrier()
@@ -276,13 +279,13 @@ def run_ours(args, rank, world, local_rank):
     d2h = sum(o.numel() * o.element_size() for o in houts if o is not None)
     e2e_steps = max(3, min(args.steps, 20))
     for _ in range(2):
-        layer.step_host(hx, hw, hdy, *houts, bias=bias)
+        layer.step_host(hx, hw, hdy, *houts, bias=bias, sr_seed=sr_seed(0))
     torch.cuda.synchronize()
     e_ms = []
     for _ in range(e2e_steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        layer.step_host(hx, hw, hdy, *houts, bias=bias)
+        layer.step_host(hx, hw, hdy, *houts, bias=bias, sr_seed=sr_seed(0))
         e1.record(stream)
         e1.synchronize()
         e_ms.append(e0.elapsed_time(e1))
@@ -341,7 +344,8 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(0,1e-3) grads)",
         "config": {"workload": args.workload, "M": M, "N": N, "K": K,
                    "step": ("dual-quant X,W; fwd" + (" + bias" if args.bias else "") +
-                            "; dual-quant dY; dgrad; wgrad") if lin.train
+                            "; dual-quant dY" + (" (stochastic rounding)" if args.sr else "") +
+                            "; dgrad; wgrad") if lin.train
                    else "row-quant X,W; fwd",
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then "
                          f"{L2_FLUSH_BYTES >> 20} MiB read)",
@@ -469,6 +473,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--sr", action="store_true",
+                    help="dY is quantized with stochastic rounding (the gradient quantizer's "
+                         "`use_sr`), a new Philox seed every step")
     ap.add_argument("--bias", action="store_true",
                     help="the forward adds the layer's bf16 bias inside the GEMM (the "
                          "`output + bias` that follows the GEMM in the layer's forward)")

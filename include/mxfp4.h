@@ -96,6 +96,25 @@ mxfp4_status mxfp4_quantize_dual(const void* x, int64_t M, int64_t K, int64_t ld
                                  void* q_row, void* s_row, void* q_col, void* s_col,
                                  mxfp4_scale_layout layout, mxfp4_stream_t stream);
 
+/* Dual quantizer with stochastically rounded elements: the gradient quantization of
+ * `_quantize_grad_dual` in primus_turbo_mxfp4_local.py with `use_sr` set (the
+ * `rowwise_use_sr` / `colwise_use_sr` flags; the layer's
+ * `mxfp4_gradient_stochastic_rounding` option), every other recipe flag off.  The pages
+ * name the flag only; what it computes here:
+ *   - scale bytes exactly as mxfp4_quantize_dual;
+ *   - each scaled element y: |y| >= 6 gives 6; otherwise, with lo <= |y| < hi its
+ *     neighbours on {0, .5, 1, 1.5, 2, 3, 4, 6}, hi if r < floor((|y| - lo)/(hi - lo) * 2^16)
+ *     and lo otherwise, with the sign kept; r = 16 random bits of the element;
+ *   - r: Philox4x32-10 keyed by `seed` (low word first), counter (b/8, a, packing, 0) for
+ *     row a, column b of the blob (packing 0: row blob of X, a = row of X; 1: col blob,
+ *     a = column of X), bits in word (b/2) % 4, low half for even b.
+ * The same seed gives the same bytes; the caller picks a new seed per step.  Arguments
+ * otherwise as mxfp4_quantize_dual. */
+mxfp4_status mxfp4_quantize_dual_sr(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                    void* q_row, void* s_row, void* q_col, void* s_col,
+                                    mxfp4_scale_layout layout, uint64_t seed,
+                                    mxfp4_stream_t stream);
+
 /* One tensor of a batched quantization: bf16 x[rows, k] with row pitch ldx elements and
  * its output buffers, as for mxfp4_quantize / mxfp4_quantize_dual (q_col and s_col are
  * read only for the dual quantizer). */

@@ -46,6 +46,7 @@ EXPORTED = (
     "mxfp4_quantize_sizes",
     "mxfp4_quantize",
     "mxfp4_quantize_dual",
+    "mxfp4_quantize_dual_sr",
     "mxfp4_quantize_batch",
     "mxfp4_gemm",
     "mxfp4_gemm_bias",
@@ -80,6 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                          ctypes.POINTER(ctypes.c_size_t)]
     lib.mxfp4_quantize.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp]
     lib.mxfp4_quantize_dual.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, vp]
+    lib.mxfp4_quantize_dual_sr.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, ctypes.c_uint64, vp]
     lib.mxfp4_quantize_batch.argtypes = [i32, ctypes.POINTER(QuantizeTask), i32, i32, vp]
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_gemm_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i32, vp]
@@ -141,6 +143,13 @@ def mxfp4_quantize_dual(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=MXFP4_S
     _check(load().mxfp4_quantize_dual(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
                                       _ptr(s_col), layout, _stream(stream)),
            "mxfp4_quantize_dual")
+
+
+def mxfp4_quantize_dual_sr(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=MXFP4_SCALE_TC,
+                           seed=0, stream=None) -> None:
+    _check(load().mxfp4_quantize_dual_sr(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
+                                         _ptr(s_col), layout, int(seed) & (2**64 - 1), _stream(stream)),
+           "mxfp4_quantize_dual_sr")
 
 
 def mxfp4_quantize_batch(tasks, dual: bool, layout=MXFP4_SCALE_TC, stream=None) -> None:
@@ -207,17 +216,22 @@ def alloc_blob(rows: int, k: int, layout: int = MXFP4_SCALE_TC, device="cuda"):
     return q, s
 
 
-def quantize(x, dual: bool = True, layout: int = MXFP4_SCALE_TC, stream=None):
-    """bf16 X[M,K] (CUDA, row pitch a multiple of 8) -> (row_q, row_s[, col_q, col_s])."""
+def quantize(x, dual: bool = True, layout: int = MXFP4_SCALE_TC, stream=None, sr_seed=None):
+    """bf16 X[M,K] (CUDA, row pitch a multiple of 8) -> (row_q, row_s[, col_q, col_s]);
+    with sr_seed (dual only) the elements are stochastically rounded."""
     import torch
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     rq, rs = alloc_blob(M, K, layout, x.device)
     if not dual:
+        assert sr_seed is None, "stochastic rounding is a mode of the dual quantizer"
         mxfp4_quantize(x, M, K, x.stride(0), rq, rs, layout, stream)
         return rq, rs
     cq, cs = alloc_blob(K, M, layout, x.device)
-    mxfp4_quantize_dual(x, M, K, x.stride(0), rq, rs, cq, cs, layout, stream)
+    if sr_seed is None:
+        mxfp4_quantize_dual(x, M, K, x.stride(0), rq, rs, cq, cs, layout, stream)
+    else:
+        mxfp4_quantize_dual_sr(x, M, K, x.stride(0), rq, rs, cq, cs, layout, sr_seed, stream)
     return rq, rs, cq, cs
 
 

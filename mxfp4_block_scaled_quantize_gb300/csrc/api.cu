@@ -115,6 +115,7 @@ mxfp4_status quantize_task(const void* x, int64_t M, int64_t K, int64_t ldx, voi
     a.kb_row = pad128(K) / 32;
     a.kb_col = pad128(M) / 32;
     a.tc_layout = layout == MXFP4_SCALE_TC ? 1 : 0;
+    a.seed = 0;
     a.err = dev->err;
     const int64_t before = j > 0 ? b->tile_end[j - 1] : 0;
     const int64_t end = before + static_cast<int64_t>(a.tiles_m) * a.tiles_k;
@@ -124,16 +125,17 @@ mxfp4_status quantize_task(const void* x, int64_t M, int64_t K, int64_t ldx, voi
     return MXFP4_OK;
 }
 
-mxfp4_status launch_batch(const mxfp4::QuantBatch& b, bool dual, DeviceState* dev, cudaStream_t stream) {
+mxfp4_status launch_batch(const mxfp4::QuantBatch& b, bool dual, DeviceState* dev, cudaStream_t stream,
+                          bool sr = false) {
     const int64_t tiles = b.tile_end[b.count - 1];
     const int64_t cap = static_cast<int64_t>(dev->sms) * mxfp4::quantize_ctas_per_sm();
     const int grid = static_cast<int>(tiles < cap ? tiles : cap);
-    return mxfp4::launch_quantize(b, dual, grid, stream) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+    return mxfp4::launch_quantize(b, dual, sr, grid, stream) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
 
 mxfp4_status quantize_common(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* s_row,
                              void* q_col, void* s_col, mxfp4_scale_layout layout, bool dual,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool sr = false, uint64_t seed = 0) {
     mxfp4_status st = quantize_check(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, dual);
     if (st != MXFP4_OK) return st;
     DeviceState* dev = nullptr;
@@ -143,7 +145,8 @@ mxfp4_status quantize_common(const void* x, int64_t M, int64_t K, int64_t ldx, v
     std::memset(&b, 0, sizeof(b));
     st = quantize_task(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, dev, &b, 0);
     if (st != MXFP4_OK) return st;
-    return launch_batch(b, dual, dev, stream);
+    b.args[0].seed = seed;
+    return launch_batch(b, dual, dev, stream, sr);
 }
 
 __global__ void selftest_wait_kernel(uint32_t* err, uint64_t limit_ns) {
@@ -272,6 +275,13 @@ mxfp4_status mxfp4_quantize_dual(const void* x, int64_t M, int64_t K, int64_t ld
                                  void* q_col, void* s_col, mxfp4_scale_layout layout, mxfp4_stream_t stream) {
     return quantize_common(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, true,
                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+mxfp4_status mxfp4_quantize_dual_sr(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* s_row,
+                                    void* q_col, void* s_col, mxfp4_scale_layout layout, uint64_t seed,
+                                    mxfp4_stream_t stream) {
+    return quantize_common(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, true,
+                           reinterpret_cast<cudaStream_t>(stream), true, seed);
 }
 
 mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* tasks, int32_t dual,

@@ -100,6 +100,7 @@ __device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t j) {
     return r * kOutRowBytes + ((j ^ ((r >> 1) & 3u)) << 4);
 }
 
+template <bool kBias>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxf4_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
                      const __grid_constant__ CUtensorMap cmap, const GemmArgs g) {
@@ -279,10 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) bulk_wait_read_all();   // the buffer's previous store has read it
                     __syncwarp();
                     uint32_t w[16];
+                    const uint16_t* const bias = kBias ? g.bias : nullptr;
                     if (g.out_f32)
-                        convert_piece<true>(&v[(c >> 1) & 3][(c & 1) * 16], g.bias, col0 + c * per, g.N, w);
+                        convert_piece<true>(&v[(c >> 1) & 3][(c & 1) * 16], bias, col0 + c * per, g.N, w);
                     else
-                        convert_piece<false>(v[c & 3], g.bias, col0 + c * per, g.N, w);
+                        convert_piece<false>(v[c & 3], bias, col0 + c * per, g.N, w);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         sts128(obuf + swz64(lane, j), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
@@ -304,14 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = out_bf16(v[c4][j], g.bias, col0 + c4 * 32 + j);
+                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = out_bf16(v[c4][j], kBias ? g.bias : nullptr, col0 + c4 * 32 + j);
             } else {
                 float* dst = reinterpret_cast<float*>(g.c) + row * g.ldc + col0;
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = out_f32(v[c4][j], g.bias, col0 + c4 * 32 + j);
+                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = out_f32(v[c4][j], kBias ? g.bias : nullptr, col0 + c4 * 32 + j);
             }
         }
         // Every TMA store of this warp is complete before the CTA may leave.
@@ -334,7 +336,8 @@ size_t gemm_smem_bytes() { return sizeof(GemmSmem) + 1024; }
 cudaError_t launch_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& cmap,
                         const GemmArgs& g, int grid, cudaStream_t stream) {
     const size_t smem = gemm_smem_bytes();
-    cudaError_t e = cudaFuncSetAttribute(gemm_mxf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = g.bias != nullptr ? gemm_mxf4_kernel<true> : gemm_mxf4_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -346,7 +349,7 @@ cudaError_t launch_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_mxf4_kernel, amap, bmap, cmap, g);
+    return cudaLaunchKernelEx(&cfg, kernel, amap, bmap, cmap, g);
 }
 
 }  // namespace mxfp4

@@ -93,7 +93,9 @@ __device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t j) {
 // kBatched = false: one problem (P.count == 1); its arguments stay constant-bank operands,
 // which the batched form's run-time problem index turns into registers (measured: the
 // forward GEMM spilled and lost 4 us in the batched form).
-template <bool kBatched>
+// kBias: some problem of the launch carries a bias (the instance without one compiles the
+// plain conversion only).
+template <bool kBatched, bool kBias>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ GemmPairBatch P) {
     extern __shared__ uint8_t smem_raw[];
@@ -300,10 +302,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (lane == 0) bulk_wait_read_all();
                     __syncwarp();
                     uint32_t w[16];
+                    const uint16_t* const bias = kBias ? g.bias : nullptr;
                     if (g.out_f32)
-                        convert_piece<true>(&v[(c >> 1) & 3][(c & 1) * 16], g.bias, col0 + c * per, g.N, w);
+                        convert_piece<true>(&v[(c >> 1) & 3][(c & 1) * 16], bias, col0 + c * per, g.N, w);
                     else
-                        convert_piece<false>(v[c & 3], g.bias, col0 + c * per, g.N, w);
+                        convert_piece<false>(v[c & 3], bias, col0 + c * per, g.N, w);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         sts128(obuf + swz64(lane, j), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
@@ -325,14 +328,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = out_bf16(v[c4][j], g.bias, col0 + c4 * 32 + j);
+                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = out_bf16(v[c4][j], kBias ? g.bias : nullptr, col0 + c4 * 32 + j);
             } else {
                 float* dst = reinterpret_cast<float*>(g.c) + row * g.ldc + col0;
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = out_f32(v[c4][j], g.bias, col0 + c4 * 32 + j);
+                        if (col0 + c4 * 32 + j < g.N) dst[c4 * 32 + j] = out_f32(v[c4][j], kBias ? g.bias : nullptr, col0 + c4 * 32 + j);
             }
         }
         if (lane == 0) bulk_wait_all();
@@ -358,7 +361,7 @@ int gemm_pair_max_clusters() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev] > 0) return cached[dev];
     const size_t smem = gemm_pair_smem_bytes();
-    if (cudaFuncSetAttribute(gemm_mxf4_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(gemm_mxf4_pair_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -366,14 +369,17 @@ int gemm_pair_max_clusters() {
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel<true>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel<true, true>, &cfg) != cudaSuccess) return 0;
     cached[dev] = n;
     return n;
 }
 
 cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream) {
     const size_t smem = gemm_pair_smem_bytes();
-    auto kernel = b.count > 1 ? gemm_mxf4_pair_kernel<true> : gemm_mxf4_pair_kernel<false>;
+    bool bias = false;
+    for (int j = 0; j < b.count; ++j) bias = bias || b.args[j].bias != nullptr;
+    auto kernel = b.count > 1 ? (bias ? gemm_mxf4_pair_kernel<true, true> : gemm_mxf4_pair_kernel<true, false>)
+                              : (bias ? gemm_mxf4_pair_kernel<false, true> : gemm_mxf4_pair_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];

@@ -22,6 +22,7 @@ struct QuantArgs {
     int64_t kb_row;      // Kp / 32
     int64_t kb_col;      // Mp / 32
     int32_t tc_layout;   // 1: tensor-core scale layout, 0: plain
+    uint64_t seed;       // Philox key of the stochastic-rounding instance (unused otherwise)
     uint32_t* err;       // device error word
 };
 
@@ -41,7 +42,8 @@ struct QuantBatch {
 size_t quantize_smem_bytes();
 int quantize_ctas_per_sm();
 
-cudaError_t launch_quantize(const QuantBatch& b, bool dual, int grid, cudaStream_t stream);
+// sr: elements stochastically rounded (dual only), with each task's seed.
+cudaError_t launch_quantize(const QuantBatch& b, bool dual, bool sr, int grid, cudaStream_t stream);
 
 // ---- GEMM ------------------------------------------------------------------------------
 struct GemmArgs {

@@ -150,6 +150,108 @@ __device__ __forceinline__ void encode_cols8(const uint32_t* w, uint64_t s2, uin
           "l"(s2));
 }
 
+// ---- stochastic rounding of the elements (the gradient quantizer's `use_sr` flag) -------
+// Random bits: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC 2011), key = the 64-bit seed,
+// counter = (b / 8, a, packing, 0) for blob row a, blob column b (packing 0: row blob of
+// X; 1: col blob, whose row a is column a of X); word (b / 2) % 4 of the result carries
+// the element's 16 bits, in its low half for even b.  One call serves 8 consecutive
+// elements of a blob row.
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint64_t seed) {
+    uint32_t x0 = c0, x1 = c1, x2 = c2, x3 = 0u;
+    uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, x0), lo0 = 0xD2511F53u * x0;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, x2), lo1 = 0xCD9E8D57u * x2;
+        const uint32_t n0 = hi1 ^ x1 ^ k0, n2 = hi0 ^ x3 ^ k1;
+        x0 = n0;
+        x1 = lo1;
+        x2 = n2;
+        x3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return make_uint4(x0, x1, x2, x3);
+}
+
+// A scaled element y onto the E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}: |y| >= 6 gives
+// 6; otherwise, between neighbours lo <= |y| < hi, hi when the 16 random bits r are below
+// floor((|y| - lo) / (hi - lo) * 2^16), else lo; the sign is kept.  Every step is exact in
+// fp32 (the gap is a power of two and |y| - lo loses no bits), so the result is exactly a
+// grid value and the round-to-nearest conversion below only encodes it.
+__device__ __forceinline__ float sr_round(float y, uint32_t r) {
+    const float a = fabsf(y);
+    float q = 6.0f;
+    if (a < 6.0f) {
+        const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
+        const float inv_gap = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
+        const float lo = floorf(a * inv_gap) * gap;
+        const uint32_t t = __float2uint_rz((a - lo) * inv_gap * 65536.0f);
+        q = r < t ? lo + gap : lo;
+    }
+    return copysignf(q, y);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t rnd16(uint32_t w, int hi) { return hi ? (w >> 16) : (w & 0xFFFFu); }
+
+// Eight grid values -> four bytes of codes, element 2k in the low nibble of byte k.
+__device__ __forceinline__ uint32_t pack_e2m1x8(const float* f) {
+    uint32_t q;
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+        : "=r"(q)
+        : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]), "f"(f[7]));
+    return q;
+}
+
+// encode8 with stochastic rounding: 8 consecutive elements of a blob row (v: word k holds
+// elements 2k, 2k+1), their scale 2^(127 - byte) as fp32, and their Philox words.
+__device__ __forceinline__ uint32_t encode8_sr(uint4 v, float inv, uint4 rw) {
+    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t r4[4] = {rw.x, rw.y, rw.z, rw.w};
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float x = (e & 1) ? bf16_hi(vw[e >> 1]) : bf16_lo(vw[e >> 1]);
+        f[e] = sr_round(__fmul_rn(x, inv), rnd16(r4[e >> 1], e & 1));
+    }
+    return pack_e2m1x8(f);
+}
+
+// encode_cols8 with stochastic rounding.  w[k] holds rows (k ^ 2rb) of the 8-row group
+// (column c0 in the low halves, c1 in the high halves); r0 / r1: the Philox words of the
+// group's 8 rows for c0 / c1, in true row order.  Output bytes in w's (permuted) order, as
+// encode_cols8 gives them.
+__device__ __forceinline__ void encode_cols8_sr(const uint32_t* w, float inv0, float inv1, uint4 r0, uint4 r1,
+                                                uint32_t rb, uint32_t* q0, uint32_t* q1) {
+    // word (k / 2) ^ rb of the true order is the one for w[k]: permute once by rb
+    uint32_t a0 = r0.x, a1 = r0.y, a2 = r0.z, a3 = r0.w;
+    uint32_t b0 = r1.x, b1 = r1.y, b2 = r1.z, b3 = r1.w;
+    if (rb & 1u) {
+        uint32_t t = a0; a0 = a1; a1 = t; t = a2; a2 = a3; a3 = t;
+        t = b0; b0 = b1; b1 = t; t = b2; b2 = b3; b3 = t;
+    }
+    if (rb & 2u) {
+        uint32_t t = a0; a0 = a2; a2 = t; t = a1; a1 = a3; a3 = t;
+        t = b0; b0 = b2; b2 = t; t = b1; b1 = b3; b3 = t;
+    }
+    const uint32_t ra[4] = {a0, a1, a2, a3}, rbw[4] = {b0, b1, b2, b3};
+    float f0[8], f1[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        f0[k] = sr_round(__fmul_rn(bf16_lo(w[k]), inv0), rnd16(ra[k >> 1], k & 1));
+        f1[k] = sr_round(__fmul_rn(bf16_hi(w[k]), inv1), rnd16(rbw[k >> 1], k & 1));
+    }
+    *q0 = pack_e2m1x8(f0);
+    *q1 = pack_e2m1x8(f1);
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
@@ -164,7 +266,7 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     return v;
 }
 
-template <bool kDual>
+template <bool kDual, bool kSR>
 __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     quantize_kernel(const __grid_constant__ QuantBatch P) {
     extern __shared__ uint8_t smem_raw[];
@@ -267,10 +369,20 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
             m = absmax2(m, m >> 16);
             const uint32_t byte = scale_byte(m);
             const uint32_t inv = inv_scale_bits(byte);
-            const uint64_t s2 = pack2(inv, inv);
-            const uint4 q = make_uint4(encode8(v0.x, v0.y, v0.z, v0.w, s2), encode8(v1.x, v1.y, v1.z, v1.w, s2),
-                                       encode8(v2.x, v2.y, v2.z, v2.w, s2), encode8(v3.x, v3.y, v3.z, v3.w, s2));
             const int64_t row = m0 + r;
+            uint4 q;
+            if (kSR) {
+                const float invf = __uint_as_float(inv);
+                const uint32_t c0 = static_cast<uint32_t>((k0 + 32 * b) >> 3), a = static_cast<uint32_t>(row);
+                q = make_uint4(encode8_sr(v0, invf, philox4x32_10(c0 + 0, a, 0u, p.seed)),
+                               encode8_sr(v1, invf, philox4x32_10(c0 + 1, a, 0u, p.seed)),
+                               encode8_sr(v2, invf, philox4x32_10(c0 + 2, a, 0u, p.seed)),
+                               encode8_sr(v3, invf, philox4x32_10(c0 + 3, a, 0u, p.seed)));
+            } else {
+                const uint64_t s2 = pack2(inv, inv);
+                q = make_uint4(encode8(v0.x, v0.y, v0.z, v0.w, s2), encode8(v1.x, v1.y, v1.z, v1.w, s2),
+                               encode8(v2.x, v2.y, v2.z, v2.w, s2), encode8(v3.x, v3.y, v3.z, v3.w, s2));
+            }
             if (row < p.M) {
                 *reinterpret_cast<uint4*>(p.q_row + row * p.ldq_row + ((k0 + 32 * b) >> 1)) = q;
                 if (!p.tc_layout) p.s_row[row * p.kb_row + (k0 >> 5) + b] = static_cast<uint8_t>(byte);
@@ -307,14 +419,23 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
             const uint32_t byte0 = scale_byte(m), byte1 = scale_byte(m >> 16);
             const uint64_t s2 = pack2(inv_scale_bits(byte0), inv_scale_bits(byte1));
             const uint32_t sel = 0x3210u ^ (0x1111u * static_cast<uint32_t>(rb));
+            const int64_t kc = k0 + 2 * pc;
             uint32_t q0[4], q1[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                encode_cols8(&w[8 * j], s2, &q0[j], &q1[j]);
+                if (kSR) {
+                    const uint32_t c0 = static_cast<uint32_t>(((m0 + rb * 32) >> 3) + j);
+                    encode_cols8_sr(&w[8 * j], __uint_as_float(inv_scale_bits(byte0)),
+                                    __uint_as_float(inv_scale_bits(byte1)),
+                                    philox4x32_10(c0, static_cast<uint32_t>(kc), 1u, p.seed),
+                                    philox4x32_10(c0, static_cast<uint32_t>(kc + 1), 1u, p.seed),
+                                    static_cast<uint32_t>(rb), &q0[j], &q1[j]);
+                } else {
+                    encode_cols8(&w[8 * j], s2, &q0[j], &q1[j]);
+                }
                 q0[j] = __byte_perm(q0[j], 0, sel);
                 q1[j] = __byte_perm(q1[j], 0, sel);
             }
-            const int64_t kc = k0 + 2 * pc;
             const int64_t off = (m0 + rb * 32) >> 1;
             if (kc < p.K) {
                 *reinterpret_cast<uint4*>(p.q_col + kc * p.ldq_col + off) = make_uint4(q0[0], q0[1], q0[2], q0[3]);
@@ -343,9 +464,10 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
 size_t quantize_smem_bytes() { return sizeof(QuantSmem) + 1024; }
 int quantize_ctas_per_sm() { return kQCtasPerSm; }
 
-cudaError_t launch_quantize(const QuantBatch& b, bool dual, int grid, cudaStream_t stream) {
+cudaError_t launch_quantize(const QuantBatch& b, bool dual, bool sr, int grid, cudaStream_t stream) {
     const size_t smem = quantize_smem_bytes();
-    auto k = dual ? quantize_kernel<true> : quantize_kernel<false>;
+    if (sr && !dual) return cudaErrorInvalidValue;
+    auto k = sr ? quantize_kernel<true, true> : dual ? quantize_kernel<true, false> : quantize_kernel<false, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];

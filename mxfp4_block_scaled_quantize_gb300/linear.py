@@ -48,9 +48,15 @@ class MXFP4Linear:
         else:
             abi.mxfp4_quantize(w, N, K, w.stride(0), *self.w_row, abi.MXFP4_SCALE_TC, stream)
 
-    def quantize_dy(self, dy, stream=None):
-        abi.mxfp4_quantize_dual(dy, self.M, self.N, dy.stride(0), *self.dy_row, *self.dy_col,
-                                abi.MXFP4_SCALE_TC, stream)
+    def quantize_dy(self, dy, stream=None, sr_seed=None):
+        """dY's two blobs; with sr_seed, stochastically rounded (the gradient quantizer's
+        `use_sr`, the layer's `mxfp4_gradient_stochastic_rounding` option)."""
+        if sr_seed is None:
+            abi.mxfp4_quantize_dual(dy, self.M, self.N, dy.stride(0), *self.dy_row, *self.dy_col,
+                                    abi.MXFP4_SCALE_TC, stream)
+        else:
+            abi.mxfp4_quantize_dual_sr(dy, self.M, self.N, dy.stride(0), *self.dy_row, *self.dy_col,
+                                       abi.MXFP4_SCALE_TC, sr_seed, stream)
 
     # -- steps a5..a7 ---------------------------------------------------------------------
     def fwd_gemm(self, stream=None, bias=None):
@@ -92,20 +98,20 @@ class MXFP4Linear:
         self.quantize_xw(x, w, stream)
         return self.fwd_gemm(stream, bias)
 
-    def backward(self, dy, stream=None):
+    def backward(self, dy, stream=None, sr_seed=None):
         assert self.train, "backward needs the column blobs of the dual quantizer"
-        self.quantize_dy(dy, stream)
+        self.quantize_dy(dy, stream, sr_seed)
         return self.bwd_gemms(stream)
 
-    def step(self, x, w, dy=None, stream=None, bias=None):
+    def step(self, x, w, dy=None, stream=None, bias=None, sr_seed=None):
         y = self.forward(x, w, stream, bias)
         if not self.train:
             return (y,)
-        dx, dw = self.backward(dy, stream)
+        dx, dw = self.backward(dy, stream, sr_seed)
         return y, dx, dw
 
     # -- the step from pinned host buffers to pinned host buffers --------------------------
-    def step_host(self, hx, hw, hdy=None, hy=None, hdx=None, hdw=None, bias=None):
+    def step_host(self, hx, hw, hdy=None, hy=None, hdx=None, hdw=None, bias=None, sr_seed=None):
         """One step with bf16 inputs in pinned host memory and results copied back to pinned
         host memory.  Host-to-device copies run on one copy stream, device-to-host copies on
         another, and the kernels on the current stream; each kernel waits only for the copy
@@ -150,7 +156,7 @@ class MXFP4Linear:
         send_back(self.fwd_gemm(bias=bias), hy)
         if self.train:
             compute.wait_event(ready[2])
-            self.quantize_dy(self._dy)
+            self.quantize_dy(self._dy, sr_seed=sr_seed)
             self.bwd_gemms()
             send_back(self.dw, hdw)
             send_back(self.dx, hdx)

@@ -52,6 +52,15 @@ def _load():
         for fn in (lib.oracle_bias_add_bf16, lib.oracle_bias_add_f32):
             fn.argtypes = [vp, vp, i64, i64, vp]
             fn.restype = None
+        lib.oracle_philox4x32_10.argtypes = [vp, vp, vp]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_sr_bits.argtypes = [ctypes.c_uint64, i64, i64, ctypes.c_int]
+        lib.oracle_sr_bits.restype = ctypes.c_uint32
+        lib.oracle_e2m1_encode_sr.argtypes = [f64, ctypes.c_uint32]
+        lib.oracle_e2m1_encode_sr.restype = u8
+        for fn in (lib.oracle_quantize_row_sr, lib.oracle_quantize_col_sr):
+            fn.argtypes = [vp, i64, i64, i64, vp, vp, ctypes.c_uint64, vp]
+            fn.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -199,3 +208,67 @@ def bias_add(y, bias_bits):
     out = np.empty((M, N), np.float32)
     _load().oracle_bias_add_f32(_ptr(y), _ptr(bias_bits), M, N, _ptr(out))
     return out
+
+
+# --- stochastic rounding (the gradient quantizer's `use_sr` flag) -------------------------
+
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 of a 4-word counter and a 2-word key -> 4 words (uint32)."""
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.empty(4, np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def sr_bits(seed, a, b, packing):
+    """16 random bits of element (row a, column b) of the row (0) or col (1) blob."""
+    return int(_load().oracle_sr_bits(int(seed) & (2**64 - 1), int(a), int(b), int(packing)))
+
+
+def e2m1_encode_sr(y, r):
+    """E2M1 code of the scaled element y with stochastic rounding driven by 16 bits r."""
+    return int(_load().oracle_e2m1_encode_sr(float(y), int(r)))
+
+
+def _ids(ids, n):
+    if ids is None:
+        return None
+    ids = np.ascontiguousarray(ids, dtype=np.int64)
+    assert ids.shape == (n,)
+    return ids
+
+
+def quantize_row_sr(x_bits, seed, row_ids=None):
+    """Row blob of X[M,K] with stochastically rounded elements (plain scale layout);
+    row_ids: each row's index in the full tensor when x_bits holds sampled rows."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    Kp = padded(K)
+    q = np.empty((M, Kp // 2), np.uint8)
+    s = np.empty((M, Kp // BLOCK), np.uint8)
+    ids = _ids(row_ids, M)
+    if _load().oracle_quantize_row_sr(_ptr(x_bits), M, K, K, _ptr(q), _ptr(s), int(seed) & (2**64 - 1),
+                                      None if ids is None else _ptr(ids)):
+        raise ValueError("non-finite input")
+    return q, s
+
+
+def quantize_col_sr(x_bits, seed, col_ids=None):
+    """Col blob of X[M,K] (row blob of X^T) with stochastically rounded elements;
+    col_ids: each column's index in the full tensor when x_bits holds sampled columns."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    Mp = padded(M)
+    q = np.empty((K, Mp // 2), np.uint8)
+    s = np.empty((K, Mp // BLOCK), np.uint8)
+    ids = _ids(col_ids, K)
+    if _load().oracle_quantize_col_sr(_ptr(x_bits), M, K, K, _ptr(q), _ptr(s), int(seed) & (2**64 - 1),
+                                      None if ids is None else _ptr(ids)):
+        raise ValueError("non-finite input")
+    return q, s
+
+
+def quantize_dual_sr(x_bits, seed):
+    """(row_q, row_s, col_q, col_s) of the dual quantizer with stochastic rounding."""
+    return quantize_row_sr(x_bits, seed) + quantize_col_sr(x_bits, seed)

@@ -253,3 +253,132 @@ void oracle_bias_add_f32(const float* y, const uint16_t* bias, int64_t M, int64_
             out[m * N + n] = s;
         }
 }
+
+/* ---------------------------------------------------------------------------------------
+ * Stochastic rounding of the elements (the `rowwise_use_sr` / `colwise_use_sr` flags that
+ * `_quantize_grad_dual` in primus_turbo_mxfp4_local.py sets from `use_sr`, i.e. from the
+ * layer's `mxfp4_gradient_stochastic_rounding` option; the pages name the flag and apply
+ * it to gradients only, and define nothing more).  Reading taken:
+ *   - the scale byte is the one of the round-to-nearest quantizer (the flag names the
+ *     element rounding only);
+ *   - a scaled element y with |y| >= 6 becomes 6 (saturation, as without the flag);
+ *     otherwise, with lo <= |y| < hi its two neighbours on {0, .5, 1, 1.5, 2, 3, 4, 6} and
+ *     P = (|y| - lo) / (hi - lo), the magnitude is hi when r < floor(P * 2^16) and lo
+ *     otherwise, r being 16 random bits of the element; the sign is kept;
+ *   - the random bits come from Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel
+ *     random numbers: as easy as 1, 2, 3", SC 2011), key = (seed low word, seed high
+ *     word), counter = (b / 8, a, packing, 0) for the element in row a, column b of the
+ *     blob being packed (packing 0: row blob of X; 1: col blob, i.e. row a = column of X,
+ *     b = row of X); of the four output words, word (b / 2) % 4 holds the element's bits
+ *     in its low half when b is even, its high half when b is odd.
+ * -------------------------------------------------------------------------------------- */
+
+/* One Philox4x32 round: two 32x32 -> 64-bit products, then the published permutation
+ * and key mixing. */
+static void philox_round(uint32_t c[4], const uint32_t k[2]) {
+    uint64_t p0 = (uint64_t)0xD2511F53u * c[0];
+    uint64_t p1 = (uint64_t)0xCD9E8D57u * c[2];
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ c[1] ^ k[0];
+    uint32_t n2 = hi0 ^ c[3] ^ k[1];
+    c[0] = n0;
+    c[1] = lo1;
+    c[2] = n2;
+    c[3] = lo0;
+}
+
+/* Philox4x32 with 10 rounds; the key is bumped by the Weyl constants between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c[4] = {ctr[0], ctr[1], ctr[2], ctr[3]};
+    uint32_t k[2] = {key[0], key[1]};
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k[0] += 0x9E3779B9u;
+            k[1] += 0xBB67AE85u;
+        }
+        philox_round(c, k);
+    }
+    for (int i = 0; i < 4; ++i) out[i] = c[i];
+}
+
+/* The 16 random bits of blob element (row a, column b) in the given packing. */
+uint32_t oracle_sr_bits(uint64_t seed, int64_t a, int64_t b, int packing) {
+    uint32_t ctr[4] = {(uint32_t)(b / 8), (uint32_t)a, (uint32_t)packing, 0u};
+    uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
+    uint32_t w[4];
+    oracle_philox4x32_10(ctr, key, w);
+    uint32_t word = w[(b / 2) % 4];
+    return (b % 2) ? (word >> 16) : (word & 0xFFFFu);
+}
+
+/* E2M1 code of the scaled element y under stochastic rounding with 16 random bits r. */
+uint8_t oracle_e2m1_encode_sr(double y, uint32_t r) {
+    static const double grid[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    uint8_t sign = signbit(y) ? 0x8 : 0x0;
+    double a = fabs(y);
+    if (a >= 6.0) return sign | 7;
+    int lo = 0;
+    while (grid[lo + 1] <= a) ++lo; /* grid[lo] <= a < grid[lo + 1] */
+    double p = (a - grid[lo]) / (grid[lo + 1] - grid[lo]); /* exact: the gap is 2^-1, 2^0 or 2^1 */
+    double t = floor(p * 65536.0);
+    return sign | (uint8_t)(((double)r < t) ? lo + 1 : lo);
+}
+
+static int quantize_block_sr(const double v[BLOCK], uint8_t q[BLOCK / 2], uint8_t* s, uint64_t seed,
+                             int64_t a, int64_t b0, int packing) {
+    double amax = 0.0;
+    for (int i = 0; i < BLOCK; ++i) {
+        if (!isfinite(v[i])) return -1;
+        if (fabs(v[i]) > amax) amax = fabs(v[i]);
+    }
+    uint8_t byte = oracle_e8m0_scale(amax);
+    int e = (int)byte - 127;
+    for (int j = 0; j < BLOCK / 2; ++j) {
+        uint8_t lo = oracle_e2m1_encode_sr(ldexp(v[2 * j], -e), oracle_sr_bits(seed, a, b0 + 2 * j, packing));
+        uint8_t hi = oracle_e2m1_encode_sr(ldexp(v[2 * j + 1], -e), oracle_sr_bits(seed, a, b0 + 2 * j + 1, packing));
+        q[j] = (uint8_t)(lo | (hi << 4));
+    }
+    *s = byte;
+    return 0;
+}
+
+/* Row blob of X[M,K] with stochastic rounding (packing 0); layout as oracle_quantize_row.
+ * row_ids (may be NULL): the row index a of each of the M rows in the full tensor, for
+ * quantizing sampled rows with the random bits of their true position. */
+int oracle_quantize_row_sr(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, uint8_t* s,
+                           uint64_t seed, const int64_t* row_ids) {
+    int64_t Kp = cdiv64(K, PAD) * PAD, KB = Kp / BLOCK;
+    double v[BLOCK];
+    for (int64_t r = 0; r < M; ++r)
+        for (int64_t b = 0; b < KB; ++b) {
+            for (int i = 0; i < BLOCK; ++i) {
+                int64_t k = b * BLOCK + i;
+                v[i] = (k < K) ? oracle_bf16_to_f64(x[r * ldx + k]) : 0.0;
+            }
+            if (quantize_block_sr(v, q + r * (Kp / 2) + b * (BLOCK / 2), s + r * KB + b, seed,
+                                  row_ids ? row_ids[r] : r, b * BLOCK, 0))
+                return -1;
+        }
+    return 0;
+}
+
+/* Col blob of X[M,K] with stochastic rounding (packing 1): the row blob of X^T, its row a
+ * being column a of X; layout as oracle_quantize_col.  col_ids (may be NULL): the column
+ * index of each of the K columns in the full tensor. */
+int oracle_quantize_col_sr(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, uint8_t* s,
+                           uint64_t seed, const int64_t* col_ids) {
+    int64_t Mp = cdiv64(M, PAD) * PAD, MB = Mp / BLOCK;
+    double v[BLOCK];
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t b = 0; b < MB; ++b) {
+            for (int i = 0; i < BLOCK; ++i) {
+                int64_t m = b * BLOCK + i;
+                v[i] = (m < M) ? oracle_bf16_to_f64(x[m * ldx + k]) : 0.0;
+            }
+            if (quantize_block_sr(v, q + k * (Mp / 2) + b * (BLOCK / 2), s + k * MB + b, seed,
+                                  col_ids ? col_ids[k] : k, b * BLOCK, 1))
+                return -1;
+        }
+    return 0;
+}

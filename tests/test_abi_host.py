@@ -58,6 +58,8 @@ def test_argument_checks_precede_any_device_use(lib):
     assert lib.mxfp4_quantize(18, 4, 8, 8, 32, 48, 0, None) == abi.MXFP4_ERR_MISALIGNED
     assert lib.mxfp4_quantize(16, 4, 6, 6, 32, 48, 0, None) == abi.MXFP4_ERR_MISALIGNED
     assert lib.mxfp4_quantize_dual(16, 4, 8, 8, 32, 48, None, 64, 1, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_quantize_dual_sr(16, 4, 8, 8, 32, 48, None, 64, 1, 7, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_quantize_dual_sr(18, 4, 8, 8, 32, 48, 64, 80, 1, 7, None) == abi.MXFP4_ERR_MISALIGNED
     assert lib.mxfp4_gemm(16, 32, 48, 64, 4, 4, 4, 80, 2, 0, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_gemm(16, 32, 48, 64, 4, 4, 4, 88, 4, 0, None) == abi.MXFP4_ERR_MISALIGNED
     assert lib.mxfp4_selftest_bounded_wait(0, None) == abi.MXFP4_ERR_INVALID_ARG

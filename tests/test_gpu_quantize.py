@@ -223,3 +223,88 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     t = workloads.TINY.tensors(0)["X"]
     check_quantized_full(t, quant(t, True, abi.MXFP4_SCALE_TC), abi.MXFP4_SCALE_TC, True,
                          "after timeout")
+
+
+# --- stochastic rounding (the gradient quantizer's `use_sr`) ----------------------------
+
+def quant_sr(x_cpu, layout, seed, ldx=None):
+    M, K = x_cpu.shape
+    if ldx is not None and ldx != K:
+        wide = torch.zeros((M, ldx), dtype=torch.bfloat16)
+        wide[:, :K] = x_cpu
+        xg = wide.cuda()[:, :K]
+    else:
+        xg = x_cpu.cuda()
+    outs = abi.quantize(xg, dual=True, layout=layout, sr_seed=seed)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    return outs
+
+
+def check_sr_full(x_cpu, outs, layout, seed, what):
+    xb = workloads.bf16_bits(x_cpu)
+    rq, rs, cq, cs = oracle.quantize_dual_sr(xb, seed)
+    tc = layout == abi.MXFP4_SCALE_TC
+    assert_bytes_equal(outs[0].cpu().numpy(), rq, f"{what} row q")
+    assert_bytes_equal(outs[1].cpu().numpy().reshape(-1), (oracle.scale_to_tc(rs) if tc else rs).reshape(-1),
+                       f"{what} row s")
+    assert_bytes_equal(outs[2].cpu().numpy(), cq, f"{what} col q")
+    assert_bytes_equal(outs[3].cpu().numpy().reshape(-1), (oracle.scale_to_tc(cs) if tc else cs).reshape(-1),
+                       f"{what} col s")
+
+
+@pytest.mark.parametrize("M,K,ldx", [(1, 8, 8), (32, 8, 16), (100, 40, 40), (130, 200, 200),
+                                     (257, 33, 40), (256, 512, 520), (129, 129, 136), (640, 384, 384)])
+@pytest.mark.parametrize("seed", [0, 0x9E3779B97F4A7C15])
+def test_sr_ragged_shapes(M, K, ldx, seed):
+    # Every byte of both blobs equals the oracle's stochastic rounding with the same seed
+    # (Philox bits, threshold rule and counter layout), edge blocks included.
+    x = _edge_input(M, K, 3 * M + K)
+    for layout in LAYOUTS:
+        check_sr_full(x, quant_sr(x, layout, seed, ldx), layout, seed, f"sr {M}x{K} seed {seed:#x}")
+
+
+def test_sr_every_finite_bf16_pattern():
+    b = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    fin = (b & 0x7F80) != 0x7F80
+    b = b[fin]
+    n = (b.size + 255) // 256 * 256
+    pad = np.zeros(n, np.uint16)
+    pad[:b.size] = b
+    x = _bits_to_bf16(pad.reshape(-1, 256))   # rows of 256: a 16-byte row pitch
+    check_sr_full(x, quant_sr(x, abi.MXFP4_SCALE_TC, 12345), abi.MXFP4_SCALE_TC, 12345, "sr all bf16")
+
+
+def test_sr_seed_behaviour():
+    # Same seed: identical bytes; another seed: different elements, the same scales.
+    x = workloads.normal((384, 640), 1.0, 77).cuda()
+    a = abi.quantize(x, dual=True, sr_seed=5)
+    b = abi.quantize(x, dual=True, sr_seed=5)
+    c = abi.quantize(x, dual=True, sr_seed=6)
+    n = abi.quantize(x, dual=True)
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    assert not torch.equal(a[0], c[0]) and not torch.equal(a[2], c[2])
+    assert torch.equal(a[1], n[1]) and torch.equal(a[3], n[3])
+
+
+def test_sr_flux_dy_sampled():
+    # The Flux-12B MLP gradient dY [4608, 12288] in the launch configuration of the
+    # backward step, against the oracle on sampled rows and columns at their true positions.
+    wl = workloads.FLUX_MLP_STEP
+    dy = wl.tensors(0)["dY"]
+    seed = 2026
+    outs = quant_sr(dy, abi.MXFP4_SCALE_TC, seed)
+    xb = workloads.bf16_bits(dy)
+    M, K = xb.shape
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([rng.choice(M, 24, replace=False), [0, 127, 128, M - 1]]))
+    cols = np.unique(np.concatenate([rng.choice(K, 24, replace=False), [0, 1, K - 2, K - 1]]))
+    rq, rs = oracle.quantize_row_sr(np.ascontiguousarray(xb[rows]), seed, row_ids=rows)
+    assert_bytes_equal(outs[0][torch.as_tensor(rows, device="cuda")].cpu().numpy(), rq, "sr dY row q")
+    from parity import gather_tc_rows
+    assert_bytes_equal(gather_tc_rows(outs[1].cpu().numpy(), rows, rs.shape[1]), rs, "sr dY row s")
+    cq, cs = oracle.quantize_col_sr(np.ascontiguousarray(xb[:, cols]), seed, col_ids=cols)
+    assert_bytes_equal(outs[2][torch.as_tensor(cols, device="cuda")].cpu().numpy(), cq, "sr dY col q")
+    assert_bytes_equal(gather_tc_rows(outs[3].cpu().numpy(), cols, cs.shape[1]), cs, "sr dY col s")

@@ -397,3 +397,117 @@ def test_bias_add_zero_bias_is_identity_except_negative_zero():
     yf = np.array([[1.5, -0.0, 3e-39, -7.25]], np.float32)
     gotf = oracle.bias_add(yf, np.zeros(4, np.uint16))
     assert np.array_equal(gotf.view(np.uint32), np.array([[1.5, 0.0, 3e-39, -7.25]], np.float32).view(np.uint32))
+
+
+# --- stochastic rounding (the gradient quantizer's `use_sr` flag) -----------------------
+
+def test_philox_known_answers():
+    # Philox4x32-10 against the known-answer vectors published with its definition.
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.json")) as f:
+        kat = json.load(f)
+    for v in kat["vectors"]:
+        ctr = [int(h, 16) for h in v["ctr"]]
+        key = [int(h, 16) for h in v["key"]]
+        out = [int(h, 16) for h in v["out"]]
+        assert [int(w) for w in oracle.philox4x32_10(ctr, key)] == out
+
+
+def _grid_neighbours(a):
+    """Exact neighbours lo <= a < hi on the E2M1 magnitudes (a < 6), as Fractions."""
+    grid = [Fraction(g) for g in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+    lo = max(g for g in grid if g <= a)
+    hi = min(g for g in grid if g > a)
+    return lo, hi
+
+
+@pytest.mark.parametrize("y", [0.0, 1e-30, 0.0009765625, 0.125, 0.25, 0.2509765625, 0.5, 0.75,
+                               0.9990234375, 1.25, 1.4990234375, 1.75, 2.5, 2.99609375, 3.5,
+                               4.0, 4.03125, 5.0, 5.9921875, -0.3125, -2.25, -5.5])
+def test_sr_rounds_up_for_exactly_floor_p_of_the_random_values(y):
+    # Over all 2^16 values of the random bits, the element rounds up for exactly
+    # floor(P * 2^16) of them, P = (|y| - lo) / (hi - lo) computed in exact rationals, and
+    # otherwise down: unbiased to within 2^-16 of the gap.
+    a = Fraction(abs(y))
+    lo, hi = _grid_neighbours(a)
+    p = (a - lo) / (hi - lo)
+    want_up = math.floor(p * 65536)
+    codes = np.array([oracle.e2m1_encode_sr(y, r) for r in range(65536)])
+    mags = np.array([E2M1_TABLE[c & 7] for c in codes])
+    assert set(np.unique(mags)) <= {float(lo), float(hi)}
+    assert int(np.sum(mags == float(hi))) == want_up
+    # the round-up values are the smallest random values
+    assert np.all(mags[:want_up] == float(hi)) and np.all(mags[want_up:] == float(lo))
+    assert np.all((codes & 8) == (8 if math.copysign(1.0, y) < 0 else 0))
+
+
+def test_sr_keeps_representable_values_and_saturates():
+    for g in E2M1_TABLE:
+        for sgn in (1.0, -1.0):
+            want = E2M1_TABLE.index(g) | (8 if sgn < 0 else 0)
+            for r in (0, 1, 12345, 65535):
+                assert oracle.e2m1_encode_sr(sgn * g, r) == want
+    for y in (6.0, 6.5, 7.9990234375):
+        for r in (0, 65535):
+            assert oracle.e2m1_encode_sr(y, r) == 7
+            assert oracle.e2m1_encode_sr(-y, r) == 15
+
+
+def _sr_block(seed_base=0):
+    rng = np.random.default_rng(23)
+    v = rng.standard_normal((4, 64)) * np.ldexp(1.0, rng.integers(-6, 6, (4, 1)))
+    return oracle.round_to_bf16(v)
+
+
+def test_sr_scales_are_the_round_to_nearest_scales():
+    xb = _sr_block()
+    q, s = oracle.quantize_row(xb)
+    for seed in (0, 1, 2**40 + 7):
+        qs, ss = oracle.quantize_row_sr(xb, seed)
+        assert np.array_equal(ss, s)
+        cq, cs = oracle.quantize_col(xb)
+        cqs, css = oracle.quantize_col_sr(xb, seed)
+        assert np.array_equal(css, cs)
+
+
+def test_sr_is_unbiased_over_seeds():
+    # The mean of the dequantized elements over many seeds approaches the input (elements
+    # below the saturation point; the scale is fixed by the block).
+    xb = _sr_block()
+    x = f32_bits_to_bf16_values(xb)
+    _, s = oracle.quantize_row(xb)
+    n = 1500
+    acc = np.zeros(x.shape)
+    acc2 = np.zeros(x.shape)
+    for seed in range(n):
+        q, ss = oracle.quantize_row_sr(xb, 1000 + seed)
+        d = oracle.dequantize(q, ss)[:, :x.shape[1]]
+        acc += d
+        acc2 += d * d
+    mean = acc / n
+    scale = np.ldexp(1.0, s.astype(np.int64) - 127).repeat(32, axis=1)[:, :x.shape[1]]
+    unsat = np.abs(x) / scale < 6
+    sd = np.sqrt(np.maximum(acc2 / n - mean * mean, 0.0))
+    gap = 2 * scale   # the widest gap between neighbours
+    tol = 5 * sd / np.sqrt(n) + gap * 2.0 ** -16 + 1e-300
+    assert np.all(np.abs(mean - x)[unsat] <= tol[unsat])
+    # and it is not round-to-nearest: some element takes both neighbours across seeds
+    assert np.any(sd[unsat] > 0)
+
+
+def test_sr_elements_are_a_grid_neighbour_and_seed_dependent():
+    xb = _sr_block()
+    x = f32_bits_to_bf16_values(xb)
+    q0, s = oracle.quantize_row_sr(xb, 5)
+    q1, _ = oracle.quantize_row_sr(xb, 6)
+    assert not np.array_equal(q0, q1)
+    d = oracle.dequantize(q0, s)[:, :x.shape[1]]
+    scale = np.ldexp(1.0, s.astype(np.int64) - 127).repeat(32, axis=1)[:, :x.shape[1]]
+    y = np.abs(x) / scale
+    gap = np.where(y < 2, 0.5, np.where(y < 4, 1.0, 2.0)) * scale
+    assert np.all(np.abs(d - x)[y < 6] < gap[y < 6])
+    # transposition: the col blob of X with a seed is the row blob of X^T packed as packing 1,
+    # which differs from packing 0 of X^T with the same seed (independent random bits)
+    cq, cs = oracle.quantize_col_sr(xb, 5)
+    rq, rs = oracle.quantize_row_sr(np.ascontiguousarray(xb.T), 5)
+    assert np.array_equal(cs, rs)
+    assert not np.array_equal(cq, rq)
