@@ -29,6 +29,7 @@ DEFAULT_WORKLOAD = "flux12b_mlp_up_train_step_4608x12288x3072"
 L2_FLUSH_BYTES = 256 << 20       # > 2x the 129 MB L2
 HEAD_START_CYCLES = 20_000_000   # ~10 ms of GPU sleep before the first timed step
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # dense FP4 / dense bf16 tensor rate (nominal)
+NOMINAL_FP8_OVER_BF16 = 4.5 / 2.25    # dense FP8 / dense bf16 tensor rate (nominal)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -72,6 +73,7 @@ KERNEL_SOURCES = {
     "gemm_mxf4_kernel": ("gemm.cu", "epilogue.cuh", "ptx.cuh", "launch.h"),
     "gemm_mxf4_pair_kernel": ("gemm_pair.cu", "epilogue.cuh", "ptx.cuh", "launch.h"),
     "quantize_kernel": ("quantize.cu", "ptx.cuh", "launch.h"),
+    "gemm_fp8_pair_kernel": ("gemm_fp8.cu", "epilogue.cuh", "ptx.cuh", "launch_fp8.h"),
 }
 
 
@@ -183,7 +185,10 @@ def run_ours(args, rank, world, local_rank):
     t = wl.tensors(0)
     x, w = t["X"].to(dev), t["W"].to(dev)
     dy = t["dY"].to(dev) if lin.train else None
-    layer = MXFP4Linear(M, N, K, train=lin.train, device=dev)
+    fp8_bwd = bool(args.fp8_backward) and lin.train
+    if args.fp8_backward and args.sr:
+        raise SystemExit("--sr is a mode of the MXFP4 backward, not of --fp8-backward")
+    layer = MXFP4Linear(M, N, K, train=lin.train, device=dev, backward="fp8" if fp8_bwd else "mxfp4")
     bias = (workloads.normal((N,), 0.02, 977).to(dev) if args.bias else None)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_src = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -195,7 +200,8 @@ def run_ours(args, rank, world, local_rank):
         flush_src.sum()
     stream = torch.cuda.current_stream(dev)
     n_k = layer.launches_per_step
-    names = (["quant_dual_XW", "gemm_fwd", "quant_dual_dY", "gemm_dgrad_wgrad"]
+    names = (["quant_row_XW", "gemm_fwd", "quant_fp8_dY_X_W", "gemm_fp8_dgrad_wgrad"] if fp8_bwd else
+             ["quant_dual_XW", "gemm_fwd", "quant_dual_dY", "gemm_dgrad_wgrad"]
              if lin.train else ["quant_row_XW", "gemm_fwd"])
 
     def sr_seed(k):
@@ -208,9 +214,15 @@ def run_ours(args, rank, world, local_rank):
         layer.fwd_gemm(bias=bias)
         evs[2].record(stream)
         if lin.train:
-            layer.quantize_dy(dy, sr_seed=sr_seed(k))
+            if fp8_bwd:
+                layer.quantize_fp8_bwd(dy)
+            else:
+                layer.quantize_dy(dy, sr_seed=sr_seed(k))
             evs[3].record(stream)
-            layer.bwd_gemms()
+            if fp8_bwd:
+                layer.fp8_bwd_gemms()
+            else:
+                layer.bwd_gemms()
             evs[4].record(stream)
 
     def barrier():
@@ -251,7 +263,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     # Per-kernel pass (same steps, an event between every two kernels, which serializes
     # their launches): the kernel durations behind the roofline and bandwidth figures.
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_k + 1)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     head_start()
     for k in range(args.steps):
         flush_l2()
@@ -264,7 +276,7 @@ def run_ours(args, rank, world, local_rank):
     if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
         raise RuntimeError("device error word set during the timed steps")
 
-    per_kernel = [[ev[i].elapsed_time(ev[i + 1]) for ev in events] for i in range(n_k)]
+    per_kernel = [[ev[i].elapsed_time(ev[i + 1]) for ev in events] for i in range(len(names))]
     step_ms = [ev[0].elapsed_time(ev[1]) for ev in step_events]
     total_ms = reduce_max_over_ranks(sum(step_ms), world, dev)
 
@@ -299,14 +311,21 @@ def run_ours(args, rank, world, local_rank):
     gemm_idx = [i for i, n in enumerate(names) if n.startswith("gemm")]
     quant_idx = [i for i, n in enumerate(names) if n.startswith("quant")]
     # algorithmic flops of each GEMM launch: the forward GEMM, and dgrad + wgrad together
-    launch_flops = {"gemm_fwd": 2 * M * N * K, "gemm_dgrad_wgrad": 4 * M * N * K}
+    launch_flops = {"gemm_fwd": 2 * M * N * K, "gemm_dgrad_wgrad": 4 * M * N * K,
+                    "gemm_fp8_dgrad_wgrad": 4 * M * N * K}
+    if fp8_bwd:
+        # the FP8 backward GEMM launch dominates; its peak is the FP8 one
+        gemm_idx = [names.index("gemm_fp8_dgrad_wgrad")]
+        fp4_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
     gemm_flops = sum(launch_flops[names[i]] for i in gemm_idx) / len(gemm_idx)   # per launch
     gemm_ms = statistics.mean([v for i in gemm_idx for v in per_kernel[i]])      # per launch
     gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
 
-    # algorithmic bytes of each quantizer launch (padding excluded)
-    elems = {"XW": M * K + N * K, "dY": M * N}   # elements each quantizer launch reads
-    bpe = 3.0625 if lin.train else 2.53125
+    # algorithmic bytes of each quantizer launch (padding excluded): bf16 read once, codes
+    # and scales written once
+    qbytes = {"quant_dual_XW": (M * K + N * K) * 3.0625, "quant_row_XW": (M * K + N * K) * 2.53125,
+              "quant_dual_dY": M * N * 3.0625,
+              "quant_fp8_dY_X_W": M * N * (2 + 2) + (M * K + N * K) * (2 + 1)}
     kern = {}
     for i, n in enumerate(names):
         ms = statistics.mean(per_kernel[i])
@@ -315,18 +334,19 @@ def run_ours(args, rank, world, local_rank):
             ent["tflops"] = round(launch_flops[n] / (ms * 1e-3) / 1e12, 1)
             ent["frac_of_fp4_peak"] = round(ent["tflops"] / fp4_peak, 4)
         else:
-            nbytes = elems[n.split("_")[-1]] * bpe
+            nbytes = qbytes[n]
             ent["gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
             ent["frac_of_hbm"] = round(ent["gbs"] / peaks["hbm_gbs"], 4)
         kern[n] = ent
-    q_bytes = sum(elems[names[i].split("_")[-1]] * bpe for i in quant_idx)
+    q_bytes = sum(qbytes[names[i]] for i in quant_idx)
     q_ms = sum(statistics.mean(per_kernel[i]) for i in quant_idx)
     quant_gbs = q_bytes / (q_ms * 1e-3) / 1e9
 
     step_flops = lin.flops_step
     value = whole_job_tflops(step_flops, args.steps, total_ms, world)
     e2e_value = whole_job_tflops(step_flops, 1, e2e_ms, world)
-    gemm_kernel = "gemm_mxf4_pair_kernel" if M > 128 else "gemm_mxf4_kernel"
+    gemm_kernel = ("gemm_fp8_pair_kernel" if fp8_bwd else
+                   "gemm_mxf4_pair_kernel" if M > 128 else "gemm_mxf4_kernel")
     traffic = profiled_traffic(gemm_kernel)
 
     line = {
@@ -340,10 +360,13 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp4_e2m1 (e8m0 block scales, fp32 accumulate, bf16 out)",
+        "dtype": "fp4_e2m1 (e8m0 block scales, fp32 accumulate, bf16 out)" + (
+            "; backward fp8_e5m2 (tensorwise scales, fp32 accumulate)" if fp8_bwd else ""),
         "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(0,1e-3) grads)",
         "config": {"workload": args.workload, "M": M, "N": N, "K": K,
-                   "step": ("dual-quant X,W; fwd" + (" + bias" if args.bias else "") +
+                   "step": ("row-quant X,W; fwd" + (" + bias" if args.bias else "") +
+                            "; fp8 tensorwise quant dY, X, W; fp8 dgrad; fp8 wgrad") if fp8_bwd else
+                           ("dual-quant X,W; fwd" + (" + bias" if args.bias else "") +
                             "; dual-quant dY" + (" (stochastic rounding)" if args.sr else "") +
                             "; dgrad; wgrad") if lin.train
                    else "row-quant X,W; fwd",
@@ -354,13 +377,14 @@ def run_ours(args, rank, world, local_rank):
                      "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1),
                      "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak, 4),
                      "traffic": traffic,
-                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x "
-                                    f"{NOMINAL_FP4_OVER_BF16:g} (nominal dense FP4/bf16 ratio)",
+                     "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x " + (
+                         f"{NOMINAL_FP8_OVER_BF16:g} (nominal dense FP8/bf16 ratio)" if fp8_bwd else
+                         f"{NOMINAL_FP4_OVER_BF16:g} (nominal dense FP4/bf16 ratio)"),
                      "algorithmic_flops_per_launch": int(gemm_flops)},
         "quant_roofline": {"bound": "hbm", "achieved": round(quant_gbs, 1),
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
-                           "bytes_per_element": bpe, "peak_source": peaks["source"]},
+                           "algorithmic_bytes_per_step": int(q_bytes), "peak_source": peaks["source"]},
         "kernels": kern,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
@@ -375,7 +399,7 @@ def run_ours(args, rank, world, local_rank):
 # ---------------------------------------------------------------------------------------
 # the CPU oracle on a bounded sample (cpu_baseline, and the reference arm)
 # ---------------------------------------------------------------------------------------
-def oracle_sample(workload_name, seconds):
+def oracle_sample(workload_name, seconds, fp8_backward=False):
     """Times the oracle on slices of the workload and extrapolates one full step.
 
     Sample: the oracle's dual (or row-only) quantizer on leading row slabs of X, W and dY,
@@ -393,7 +417,8 @@ def oracle_sample(workload_name, seconds):
     M, N, K = lin.M, lin.N, lin.K
     t = wl.tensors(0)
     bits = {k: workloads.bf16_bits(v) for k, v in t.items()}
-    quant = oracle.quantize_dual if lin.train else oracle.quantize_row
+    fp8 = fp8_backward and lin.train
+    quant = oracle.quantize_dual if (lin.train and not fp8) else oracle.quantize_row
 
     q_elems = q_time = 0.0
     t0 = time.perf_counter()
@@ -401,7 +426,12 @@ def oracle_sample(workload_name, seconds):
         for k in bits:
             slab = np.ascontiguousarray(bits[k][:128])
             s = time.perf_counter()
-            quant(slab)
+            if fp8:   # row-only MX for X and W, tensorwise E5M2 for all three
+                if k != "dY":
+                    quant(slab)
+                oracle.fp8_quantize_tw(slab, row=(k == "dY"), col=True)
+            else:
+                quant(slab)
             q_time += time.perf_counter() - s
             q_elems += slab.size
     xq, xs = oracle.quantize_row(np.ascontiguousarray(bits["X"][:8]))
@@ -421,7 +451,8 @@ def oracle_sample(workload_name, seconds):
     return {
         "step_seconds": step_s,
         "value": lin.flops_step / step_s / 1e12,
-        "sample": (f"oracle {'dual' if lin.train else 'row-only'} quantizer on 128-row slabs of "
+        "sample": (f"oracle {'row-only MX + tensorwise E5M2' if fp8 else 'dual' if lin.train else 'row-only'} "
+                   f"quantizer on 128-row slabs of "
                    f"X, W{', dY' if lin.train else ''} ({int(q_elems)} elements) and fp64 GEMM "
                    f"on 8x512 output blocks at K={oracle.padded(K)} ({int(g_macs)} MACs); "
                    f"one full step extrapolated per element / per MAC"),
@@ -476,6 +507,9 @@ def main():
     ap.add_argument("--sr", action="store_true",
                     help="dY is quantized with stochastic rounding (the gradient quantizer's "
                          "`use_sr`), a new Philox seed every step")
+    ap.add_argument("--fp8-backward", action="store_true",
+                    help="the hybrid backward: dY, X, W quantized tensorwise to FP8 E5M2 and "
+                         "dgrad / wgrad as FP8 GEMMs (the layer's mxfp4_backward_precision 'fp8')")
     ap.add_argument("--bias", action="store_true",
                     help="the forward adds the layer's bf16 bias inside the GEMM (the "
                          "`output + bias` that follows the GEMM in the layer's forward)")
@@ -497,7 +531,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:
-        base = oracle_sample(args.workload, args.cpu_baseline_seconds)
+        base = oracle_sample(args.workload, args.cpu_baseline_seconds, args.fp8_backward)
         line["cpu_baseline"] = {"value": base["value"], "unit": "TFLOP/s", "cores": base["cores"],
                                 "kind": "oracle", "sample": base["sample"]}
         print(json.dumps(line), flush=True)

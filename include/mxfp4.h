@@ -193,6 +193,64 @@ typedef struct {
  * failing task's status is returned and nothing is launched. */
 mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4_stream_t stream);
 
+/* ---- hybrid FP8 backward --------------------------------------------------------------
+ * `MXFP4LinearFunction.backward` in primus_turbo_mxfp4_local.py, when the layer's
+ * `mxfp4_backward_precision` is "fp8" (`backward_is_fp8`): dY, X and W are quantized
+ * tensorwise to FP8 E5M2 (`_quantize_fp8_tw(…, float8_e5m2)`) and dgrad / wgrad run as
+ * FP8 GEMMs with TENSORWISE scales (`gemm_fp8_impl`).  The forward stays MXFP4. */
+
+/* Tensorwise E5M2 quantization of bf16 X[M,K].  The pages call `_quantize_fp8_tw` without
+ * defining it; what it computes here:
+ *   amax = max |x| over the tensor;  scale = 57344 / amax in fp32 (57344 = the largest
+ *   finite E5M2 value; the largest finite fp32 if the quotient overflows; 1 if amax = 0);
+ *   element = E5M2 round-to-nearest-even of the fp32 product x * scale, saturating at
+ *   +-57344, sign of zero kept;  scale_inv = 1 / scale in fp32.
+ *   x          bf16 X[M,K], row pitch ldx elements (ldx >= K, ldx % 8 == 0), 16-byte aligned
+ *   q_row      out or NULL: X's codes, M rows of round16(K) bytes (padding bytes 0x00)
+ *   q_col      out or NULL: X^T's codes, K rows of round16(M) bytes (padding 0x00); at
+ *              least one of q_row / q_col; both 16-byte aligned
+ *   amax, scale_inv   out, one fp32 each in device memory (4-byte aligned); the GEMMs
+ *              read scale_inv from there, so no host synchronization is needed.
+ * Two launches on `stream` (an amax pass, then the conversion) after a 4-byte memset of
+ * *amax.  M, K >= 1. */
+mxfp4_status mxfp4_fp8_quantize_tw(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                   void* q_row, void* q_col, float* amax, float* scale_inv,
+                                   mxfp4_stream_t stream);
+
+/* FP8 GEMM C[M,N] = (A . B^T) * (*a_scale_inv) * (*b_scale_inv) over E5M2 codes, the form
+ * both backward `gemm_fp8_impl` calls take with the quantizer's column copies (dgrad:
+ * A = dY row copy, B = W column copy; wgrad: A = dY column copy, B = X column copy):
+ *   a   [M, round16(K)] codes;  b   [N, round16(K)] codes (16-byte aligned; bytes past K
+ *       are not read)
+ *   a_scale_inv, b_scale_inv   device fp32 (as mxfp4_fp8_quantize_tw leaves them)
+ *   c   out, C[M,N] row-major with pitch ldc elements (ldc >= N), bf16 or fp32
+ * Products accumulate in fp32 on the tensor cores; the accumulator is multiplied by the
+ * fp32 product of the two inverse scales and rounded once to the output dtype.
+ * M, N, K >= 1. */
+mxfp4_status mxfp4_fp8_gemm(const void* a, const float* a_scale_inv, const void* b,
+                            const float* b_scale_inv, int64_t M, int64_t N, int64_t K, void* c,
+                            int64_t ldc, mxfp4_out_dtype out_dtype, mxfp4_stream_t stream);
+
+/* One FP8 GEMM of a batch: the arguments of mxfp4_fp8_gemm. */
+typedef struct {
+    const void* a;
+    const float* a_scale_inv;
+    const void* b;
+    const float* b_scale_inv;
+    int64_t M;
+    int64_t N;
+    int64_t K;
+    void* c;
+    int64_t ldc;
+    mxfp4_out_dtype out_dtype;
+} mxfp4_fp8_gemm_task;
+
+/* 1..MXFP4_MAX_BATCH FP8 GEMMs in one launch of CTA pairs (dgrad and wgrad of the hybrid
+ * backward together), each with exactly its own call's result.  Outputs must not overlap
+ * each other or any input.  Every task is checked before anything runs. */
+mxfp4_status mxfp4_fp8_gemm_batch(int32_t count, const mxfp4_fp8_gemm_task* tasks,
+                                  mxfp4_stream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the device error word of the current
  * device: MXFP4_ERR_TIMEOUT if a bounded wait in any kernel of this library ran out
  * since the last call, MXFP4_ERR_CUDA if the synchronization itself failed, else OK. */

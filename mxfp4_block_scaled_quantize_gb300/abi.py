@@ -42,6 +42,14 @@ class QuantizeTask(ctypes.Structure):
                 ("ldx", ctypes.c_int64), ("q_row", ctypes.c_void_p), ("s_row", ctypes.c_void_p),
                 ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p)]
 
+class Fp8GemmTask(ctypes.Structure):
+    """mxfp4_fp8_gemm_task of include/mxfp4.h."""
+    _fields_ = [("a", ctypes.c_void_p), ("a_scale_inv", ctypes.c_void_p), ("b", ctypes.c_void_p),
+                ("b_scale_inv", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("c", ctypes.c_void_p), ("ldc", ctypes.c_int64),
+                ("out_dtype", ctypes.c_int)]
+
+
 EXPORTED = (
     "mxfp4_quantize_sizes",
     "mxfp4_quantize",
@@ -51,6 +59,9 @@ EXPORTED = (
     "mxfp4_gemm",
     "mxfp4_gemm_bias",
     "mxfp4_gemm_batch",
+    "mxfp4_fp8_quantize_tw",
+    "mxfp4_fp8_gemm",
+    "mxfp4_fp8_gemm_batch",
     "mxfp4_last_device_error",
     "mxfp4_selftest_bounded_wait",
     "mxfp4_status_string",
@@ -86,6 +97,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_gemm_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i32, vp]
     lib.mxfp4_gemm_batch.argtypes = [i32, ctypes.POINTER(GemmTask), vp]
+    lib.mxfp4_fp8_quantize_tw.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp]
+    lib.mxfp4_fp8_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
+    lib.mxfp4_fp8_gemm_batch.argtypes = [i32, ctypes.POINTER(Fp8GemmTask), vp]
     lib.mxfp4_last_device_error.argtypes = [vp]
     lib.mxfp4_selftest_bounded_wait.argtypes = [i64, vp]
     lib.mxfp4_status_string.argtypes = [i32]
@@ -184,6 +198,25 @@ def mxfp4_gemm_batch(tasks, stream=None) -> None:
     _check(load().mxfp4_gemm_batch(len(tasks), arr, _stream(stream)), "mxfp4_gemm_batch")
 
 
+def mxfp4_fp8_quantize_tw(x, M, K, ldx, q_row, q_col, amax, scale_inv, stream=None) -> None:
+    _check(load().mxfp4_fp8_quantize_tw(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(q_col), _ptr(amax),
+                                        _ptr(scale_inv), _stream(stream)), "mxfp4_fp8_quantize_tw")
+
+
+def mxfp4_fp8_gemm(a, a_scale_inv, b, b_scale_inv, M, N, K, c, ldc, out_dtype=MXFP4_OUT_BF16,
+                   stream=None) -> None:
+    _check(load().mxfp4_fp8_gemm(_ptr(a), _ptr(a_scale_inv), _ptr(b), _ptr(b_scale_inv), M, N, K, _ptr(c),
+                                 ldc, out_dtype, _stream(stream)), "mxfp4_fp8_gemm")
+
+
+def mxfp4_fp8_gemm_batch(tasks, stream=None) -> None:
+    """tasks: sequence of (a, a_scale_inv, b, b_scale_inv, M, N, K, c, ldc, out_dtype)."""
+    arr = (Fp8GemmTask * max(1, len(tasks)))()
+    for i, (a, sa, b, sb, M, N, K, c, ldc, od) in enumerate(tasks):
+        arr[i] = Fp8GemmTask(_ptr(a), _ptr(sa), _ptr(b), _ptr(sb), M, N, K, _ptr(c), ldc, od)
+    _check(load().mxfp4_fp8_gemm_batch(len(tasks), arr, _stream(stream)), "mxfp4_fp8_gemm_batch")
+
+
 def mxfp4_last_device_error(stream=None) -> int:
     """Returns the status (does not raise): MXFP4_ERR_TIMEOUT if a bounded wait ran out."""
     return int(load().mxfp4_last_device_error(_stream(stream)))
@@ -248,4 +281,37 @@ def gemm(a_q, a_s, b_q, b_s, M, N, K, out_dtype=None, out=None, stream=None, bia
     else:
         assert bias.dtype == torch.bfloat16 and bias.is_contiguous() and bias.numel() == N
         mxfp4_gemm_bias(a_q, a_s, b_q, b_s, M, N, K, bias, out, out.stride(0), code, stream)
+    return out
+
+
+def fp8_pitch(n: int) -> int:
+    """Row pitch in bytes of an E5M2 copy whose rows hold n elements (16-byte rounded)."""
+    return (n + 15) // 16 * 16
+
+
+def fp8_quantize(x, row: bool = True, col: bool = True, scalars=None, stream=None):
+    """Tensorwise E5M2 quantization of bf16 X[M,K] (CUDA): (q_row [M, pitch(K)] or None,
+    q_col [K, pitch(M)] or None, amax, scale_inv), the last two one-element fp32 CUDA
+    tensors (views into `scalars`, a 2-element fp32 tensor, when given)."""
+    import torch
+    assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    qr = torch.empty((M, fp8_pitch(K)), dtype=torch.uint8, device=x.device) if row else None
+    qc = torch.empty((K, fp8_pitch(M)), dtype=torch.uint8, device=x.device) if col else None
+    if scalars is None:
+        scalars = torch.empty(2, dtype=torch.float32, device=x.device)
+    amax, inv = scalars[0:1], scalars[1:2]
+    mxfp4_fp8_quantize_tw(x, M, K, x.stride(0), qr, qc, amax, inv, stream)
+    return qr, qc, amax, inv
+
+
+def fp8_gemm(a, a_scale_inv, b, b_scale_inv, M, N, K, out_dtype=None, out=None, stream=None):
+    """C[M,N] = (A . B^T) * a_scale_inv * b_scale_inv over E5M2 codes A [M, pitch(K)],
+    B [N, pitch(K)]."""
+    import torch
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a.device)
+    code = MXFP4_OUT_F32 if out.dtype == torch.float32 else MXFP4_OUT_BF16
+    assert out.dtype in (torch.float32, torch.bfloat16) and out.stride(1) == 1
+    mxfp4_fp8_gemm(a, a_scale_inv, b, b_scale_inv, M, N, K, out, out.stride(0), code, stream)
     return out

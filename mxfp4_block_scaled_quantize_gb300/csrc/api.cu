@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "launch.h"
+#include "launch_fp8.h"
 #include "mxfp4.h"
 #include "ptx.cuh"
 
@@ -241,6 +242,62 @@ mxfp4_status gemm_fill_pair(const mxfp4_gemm_task& t, DeviceState* dev, mxfp4::G
     return MXFP4_OK;
 }
 
+// ---- hybrid FP8 backward ------------------------------------------------------------
+
+inline int64_t pad16(int64_t n) { return cdiv(n, 16) * 16; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+mxfp4_status fp8_gemm_check(const mxfp4_fp8_gemm_task& t) {
+    if (!t.a || !t.a_scale_inv || !t.b || !t.b_scale_inv || !t.c) return MXFP4_ERR_INVALID_ARG;
+    if (t.M < 1 || t.N < 1 || t.K < 1 || t.M > kMaxDim || t.N > kMaxDim || t.K > kMaxDim)
+        return MXFP4_ERR_INVALID_ARG;
+    if (t.ldc < t.N || t.ldc > kMaxDim) return MXFP4_ERR_INVALID_ARG;
+    if (t.out_dtype != MXFP4_OUT_BF16 && t.out_dtype != MXFP4_OUT_F32) return MXFP4_ERR_INVALID_ARG;
+    if (!aligned16(t.a) || !aligned16(t.b) || !aligned16(t.c) || !aligned4(t.a_scale_inv) ||
+        !aligned4(t.b_scale_inv))
+        return MXFP4_ERR_MISALIGNED;
+    return MXFP4_OK;
+}
+
+// Appends a checked FP8 GEMM to the batch: A / B maps over the codes (pitch round16(K)
+// bytes, box 128 x 128, 128-byte swizzle) and C as for the MXFP4 GEMMs.
+mxfp4_status fp8_gemm_fill(const mxfp4_fp8_gemm_task& t, DeviceState* dev, mxfp4::Fp8GemmBatch* b) {
+    const int j = b->count;
+    mxfp4::Fp8GemmArgs& g = b->args[j];
+    const uint64_t ld = static_cast<uint64_t>(pad16(t.K));
+    if (!encode_2d(&b->amap[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, t.a, static_cast<uint64_t>(t.K),
+                   static_cast<uint64_t>(t.M), ld, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&b->bmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, t.b, static_cast<uint64_t>(t.K),
+                   static_cast<uint64_t>(t.N), ld, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MXFP4_ERR_CUDA;
+    const int64_t esize = t.out_dtype == MXFP4_OUT_F32 ? 4 : 2;
+    std::memset(&b->cmap[j], 0, sizeof(b->cmap[j]));
+    const bool c_tma = (t.ldc * esize) % 16 == 0 &&
+                       encode_2d(&b->cmap[j], t.out_dtype == MXFP4_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                 t.c, static_cast<uint64_t>(t.N), static_cast<uint64_t>(t.M),
+                                 static_cast<uint64_t>(t.ldc * esize), static_cast<uint32_t>(64 / esize), 32,
+                                 CU_TENSOR_MAP_SWIZZLE_64B);
+    g.M = t.M;
+    g.N = t.N;
+    g.tiles_m2 = static_cast<int32_t>(cdiv(t.M, 256));
+    g.tiles_n = static_cast<int32_t>(cdiv(t.N, 256));
+    g.k_stages = static_cast<int32_t>(cdiv(t.K, 128));
+    g.c = t.c;
+    g.ldc = t.ldc;
+    g.out_f32 = t.out_dtype == MXFP4_OUT_F32 ? 1 : 0;
+    g.c_tma = c_tma ? 1 : 0;
+    g.a_scale_inv = t.a_scale_inv;
+    g.b_scale_inv = t.b_scale_inv;
+    g.err = dev->err;
+    const int64_t before = j > 0 ? b->tile_end[j - 1] : 0;
+    const int64_t end = before + static_cast<int64_t>(g.tiles_m2) * g.tiles_n;
+    if (end > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;
+    b->tile_end[j] = static_cast<int32_t>(end);
+    b->count = j + 1;
+    return MXFP4_OK;
+}
+
 }  // namespace
 
 namespace mxfp4 {
@@ -357,6 +414,54 @@ mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4
     const int64_t pair_tiles = b.tile_end[b.count - 1];
     const int clusters = static_cast<int>(pair_tiles < max_clusters ? pair_tiles : max_clusters);
     return mxfp4::launch_gemm_pair(b, clusters, s) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
+mxfp4_status mxfp4_fp8_quantize_tw(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* q_col,
+                                   float* amax, float* scale_inv, mxfp4_stream_t stream) {
+    if (x == nullptr || (q_row == nullptr && q_col == nullptr) || amax == nullptr || scale_inv == nullptr)
+        return MXFP4_ERR_INVALID_ARG;
+    if (M < 1 || K < 1 || M > kMaxDim || K > kMaxDim || ldx < K || ldx > kMaxDim) return MXFP4_ERR_INVALID_ARG;
+    if (!aligned16(x) || (ldx % 8) != 0 || (q_row && !aligned16(q_row)) || (q_col && !aligned16(q_col)) ||
+        !aligned4(amax) || !aligned4(scale_inv))
+        return MXFP4_ERR_MISALIGNED;
+    DeviceState* dev = nullptr;
+    const mxfp4_status st = device_ready(&dev);
+    if (st != MXFP4_OK) return st;
+    mxfp4::Fp8QuantArgs a{x, M, K, ldx, q_row, pad16(K), q_col, pad16(M), amax, scale_inv};
+    return mxfp4::launch_fp8_quantize(a, dev->sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MXFP4_OK
+               : MXFP4_ERR_CUDA;
+}
+
+mxfp4_status mxfp4_fp8_gemm_batch(int32_t count, const mxfp4_fp8_gemm_task* tasks, mxfp4_stream_t stream) {
+    if (count < 1 || count > MXFP4_MAX_BATCH || tasks == nullptr) return MXFP4_ERR_INVALID_ARG;
+    for (int j = 0; j < count; ++j) {
+        const mxfp4_status st = fp8_gemm_check(tasks[j]);
+        if (st != MXFP4_OK) return st;
+    }
+    DeviceState* dev = nullptr;
+    mxfp4_status st = device_ready(&dev);
+    if (st != MXFP4_OK) return st;
+    const int max_clusters = mxfp4::gemm_fp8_max_clusters();
+    if (max_clusters < 1) return MXFP4_ERR_CUDA;
+    mxfp4::Fp8GemmBatch b;
+    std::memset(&b, 0, sizeof(b));
+    for (int j = 0; j < count; ++j) {
+        st = fp8_gemm_fill(tasks[j], dev, &b);
+        if (st != MXFP4_OK) return st;
+    }
+    const int64_t tiles = b.tile_end[b.count - 1];
+    const int clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
+    return mxfp4::launch_gemm_fp8(b, clusters, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MXFP4_OK
+               : MXFP4_ERR_CUDA;
+}
+
+mxfp4_status mxfp4_fp8_gemm(const void* a, const float* a_scale_inv, const void* b, const float* b_scale_inv,
+                            int64_t M, int64_t N, int64_t K, void* c, int64_t ldc, mxfp4_out_dtype out_dtype,
+                            mxfp4_stream_t stream) {
+    const mxfp4_fp8_gemm_task t{a, a_scale_inv, b, b_scale_inv, M, N, K, c, ldc, out_dtype};
+    return mxfp4_fp8_gemm_batch(1, &t, stream);
 }
 
 mxfp4_status mxfp4_last_device_error(mxfp4_stream_t stream) {

@@ -16,14 +16,32 @@ from . import abi
 
 
 class MXFP4Linear:
+    """backward = "mxfp4" (the default) or "fp8": the hybrid mode of the pages
+    (`mxfp4_backward_precision == "fp8"`, `backward_is_fp8`), where the forward keeps the
+    bf16 X and W and the backward quantizes dY, X and W tensorwise to E5M2 and runs dgrad
+    and wgrad as FP8 GEMMs.  In that mode the forward quantizes X and W row-only: their
+    column blobs would only feed an MXFP4 backward."""
+
     def __init__(self, M: int, N: int, K: int, train: bool = True, device="cuda",
-                 out_dtype=torch.bfloat16):
+                 out_dtype=torch.bfloat16, backward: str = "mxfp4"):
+        assert backward in ("mxfp4", "fp8")
         self.M, self.N, self.K, self.train = M, N, K, train
+        self.fp8_backward = train and backward == "fp8"
         L = abi.MXFP4_SCALE_TC
         self.x_row = abi.alloc_blob(M, K, L, device)
         self.w_row = abi.alloc_blob(N, K, L, device)
         self.y = torch.empty((M, N), dtype=out_dtype, device=device)
-        if train:
+        if self.fp8_backward:
+            p = abi.fp8_pitch
+            self.dy_f8 = torch.empty((M, p(N)), dtype=torch.uint8, device=device)
+            self.dy_f8_col = torch.empty((N, p(M)), dtype=torch.uint8, device=device)
+            self.x_f8_col = torch.empty((K, p(M)), dtype=torch.uint8, device=device)
+            self.w_f8_col = torch.empty((K, p(N)), dtype=torch.uint8, device=device)
+            self.f8_scalars = torch.zeros(6, dtype=torch.float32, device=device)   # (amax, scale_inv) x dY, X, W
+            self.dx = torch.empty((M, K), dtype=out_dtype, device=device)
+            self.dw = torch.empty((N, K), dtype=out_dtype, device=device)
+            self._saved = None
+        elif train:
             self.x_col = abi.alloc_blob(K, M, L, device)
             self.w_col = abi.alloc_blob(K, N, L, device)
             self.dy_row = abi.alloc_blob(M, N, L, device)
@@ -86,13 +104,15 @@ class MXFP4Linear:
     def quantize_xw(self, x, w, stream=None):
         """X and W in one launch (steps a1-a4 for both)."""
         M, N, K = self.M, self.N, self.K
-        if self.train:
+        if self.fp8_backward:
+            self._saved = (x, w)   # the hybrid backward re-quantizes the bf16 tensors
+        if self.train and not self.fp8_backward:
             tasks = [(x, M, K, x.stride(0), *self.x_row, *self.x_col),
                      (w, N, K, w.stride(0), *self.w_row, *self.w_col)]
         else:
             tasks = [(x, M, K, x.stride(0), *self.x_row, None, None),
                      (w, N, K, w.stride(0), *self.w_row, None, None)]
-        abi.mxfp4_quantize_batch(tasks, self.train, abi.MXFP4_SCALE_TC, stream)
+        abi.mxfp4_quantize_batch(tasks, self.train and not self.fp8_backward, abi.MXFP4_SCALE_TC, stream)
 
     def forward(self, x, w, stream=None, bias=None):
         self.quantize_xw(x, w, stream)
@@ -100,8 +120,38 @@ class MXFP4Linear:
 
     def backward(self, dy, stream=None, sr_seed=None):
         assert self.train, "backward needs the column blobs of the dual quantizer"
+        if self.fp8_backward:
+            assert sr_seed is None, "stochastic rounding belongs to the MXFP4 backward"
+            self.quantize_fp8_bwd(dy, stream)
+            return self.fp8_bwd_gemms(stream)
         self.quantize_dy(dy, stream, sr_seed)
         return self.bwd_gemms(stream)
+
+    # -- hybrid FP8 backward ----------------------------------------------------------------
+    def quantize_fp8_bwd(self, dy, stream=None):
+        """`_quantize_fp8_tw` of dY (row and column copies), X and W (column copies: the
+        K-major operands of the two TN GEMMs)."""
+        x, w = self._saved
+        sc = self.f8_scalars
+        abi.mxfp4_fp8_quantize_tw(dy, self.M, self.N, dy.stride(0), self.dy_f8, self.dy_f8_col,
+                                  sc[0:1], sc[1:2], stream)
+        abi.mxfp4_fp8_quantize_tw(x, self.M, self.K, x.stride(0), None, self.x_f8_col,
+                                  sc[2:3], sc[3:4], stream)
+        abi.mxfp4_fp8_quantize_tw(w, self.N, self.K, w.stride(0), None, self.w_f8_col,
+                                  sc[4:5], sc[5:6], stream)
+
+    def fp8_bwd_gemms(self, stream=None):
+        """dX = dY . W (A = dY codes, B = W^T codes) and dW = dY^T . X (A = dY^T codes,
+        B = X^T codes) in one launch, each scaled by its operands' inverse scales."""
+        code = abi.MXFP4_OUT_F32 if self.dx.dtype == torch.float32 else abi.MXFP4_OUT_BF16
+        sc = self.f8_scalars
+        abi.mxfp4_fp8_gemm_batch([
+            (self.dy_f8, sc[1:2], self.w_f8_col, sc[5:6], self.M, self.K, self.N, self.dx,
+             self.dx.stride(0), code),
+            (self.dy_f8_col, sc[1:2], self.x_f8_col, sc[3:4], self.N, self.K, self.M, self.dw,
+             self.dw.stride(0), code),
+        ], stream)
+        return self.dx, self.dw
 
     def step(self, x, w, dy=None, stream=None, bias=None, sr_seed=None):
         y = self.forward(x, w, stream, bias)
@@ -156,8 +206,7 @@ class MXFP4Linear:
         send_back(self.fwd_gemm(bias=bias), hy)
         if self.train:
             compute.wait_event(ready[2])
-            self.quantize_dy(self._dy, sr_seed=sr_seed)
-            self.bwd_gemms()
+            self.backward(self._dy, sr_seed=sr_seed)
             send_back(self.dw, hdw)
             send_back(self.dx, hdx)
         compute.wait_stream(d2h)
@@ -166,4 +215,6 @@ class MXFP4Linear:
     # launches per step (for the benchmark's launch count)
     @property
     def launches_per_step(self) -> int:
+        if self.fp8_backward:
+            return 2 + 3 * 2 + 1   # X+W, fwd; three FP8 quantizations (amax, convert); the GEMMs
         return 4 if self.train else 2

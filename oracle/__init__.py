@@ -52,6 +52,16 @@ def _load():
         for fn in (lib.oracle_bias_add_bf16, lib.oracle_bias_add_f32):
             fn.argtypes = [vp, vp, i64, i64, vp]
             fn.restype = None
+        lib.oracle_e5m2_decode.argtypes = [u8]
+        lib.oracle_e5m2_decode.restype = f64
+        lib.oracle_e5m2_encode.argtypes = [f64]
+        lib.oracle_e5m2_encode.restype = u8
+        lib.oracle_fp8_quantize_tw.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, vp]
+        lib.oracle_fp8_quantize_tw.restype = ctypes.c_int
+        lib.oracle_fp8_dequantize.argtypes = [vp, i64, i64, i64, vp]
+        lib.oracle_fp8_dequantize.restype = None
+        lib.oracle_fp8_output_scale.argtypes = [ctypes.c_float, ctypes.c_float]
+        lib.oracle_fp8_output_scale.restype = ctypes.c_float
         lib.oracle_philox4x32_10.argtypes = [vp, vp, vp]
         lib.oracle_philox4x32_10.restype = None
         lib.oracle_sr_bits.argtypes = [ctypes.c_uint64, i64, i64, ctypes.c_int]
@@ -272,3 +282,59 @@ def quantize_col_sr(x_bits, seed, col_ids=None):
 def quantize_dual_sr(x_bits, seed):
     """(row_q, row_s, col_q, col_s) of the dual quantizer with stochastic rounding."""
     return quantize_row_sr(x_bits, seed) + quantize_col_sr(x_bits, seed)
+
+
+# --- hybrid FP8 backward: tensorwise E5M2 quantization and the FP8 GEMM ---------------
+
+FP8_PITCH = 16   # row pitch of the E5M2 copies: a multiple of 16 bytes
+
+
+def fp8_pitch(n):
+    """Row pitch in bytes of an E5M2 copy whose rows hold n elements."""
+    return cdiv(n, FP8_PITCH) * FP8_PITCH
+
+
+def e5m2_decode(code):
+    return float(_load().oracle_e5m2_decode(int(code)))
+
+
+def e5m2_encode(v):
+    return int(_load().oracle_e5m2_encode(float(v)))
+
+
+def fp8_quantize_tw(x_bits, row=True, col=True):
+    """Tensorwise E5M2 quantization of X[M,K] (bf16 bits): (q_row [M, pitch(K)] or None,
+    q_col [K, pitch(M)] or None, amax, scale_inv), padding bytes 0x00."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    qr = np.empty((M, fp8_pitch(K)), np.uint8) if row else None
+    qc = np.empty((K, fp8_pitch(M)), np.uint8) if col else None
+    amax = np.zeros(1, np.float32)
+    inv = np.zeros(1, np.float32)
+    if _load().oracle_fp8_quantize_tw(_ptr(x_bits), M, K, K, None if qr is None else _ptr(qr), fp8_pitch(K),
+                                      None if qc is None else _ptr(qc), fp8_pitch(M), _ptr(amax), _ptr(inv)):
+        raise ValueError("non-finite input")
+    return qr, qc, float(amax[0]), float(inv[0])
+
+
+def fp8_dequantize(q, cols):
+    """E5M2 codes [R, pitch] -> fp64 [R, cols]."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    R, ld = q.shape
+    out = np.empty((R, cols), np.float64)
+    _load().oracle_fp8_dequantize(_ptr(q), R, cols, ld, _ptr(out))
+    return out
+
+
+def fp8_output_scale(a_scale_inv, b_scale_inv):
+    return float(_load().oracle_fp8_output_scale(a_scale_inv, b_scale_inv))
+
+
+def fp8_gemm(a_q, a_scale_inv, b_q, b_scale_inv, K, rows=None):
+    """C = (A . B^T) * s over E5M2 codes A [M, pitch], B [N, pitch] (first K columns), s the
+    binary32 product of the inverse scales; returns (C, sum_k |a_k b_k| * s) in fp64."""
+    a = fp8_dequantize(a_q if rows is None else np.ascontiguousarray(a_q[rows]), K)
+    b = fp8_dequantize(b_q, K)
+    c, cabs = gemm_dequantized(a, b)
+    s = fp8_output_scale(a_scale_inv, b_scale_inv)
+    return c * s, cabs * s

@@ -35,6 +35,7 @@
  *
  * Everything is computed in fp64, where every step above is exact.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -381,4 +382,99 @@ int oracle_quantize_col_sr(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
                 return -1;
         }
     return 0;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Hybrid FP8 backward (`backward_is_fp8` in `MXFP4LinearFunction.backward`,
+ * primus_turbo_mxfp4_local.py): dY, X and W are quantized tensorwise to FP8 E5M2
+ * (`_quantize_fp8_tw(…, fp8_bwd_dtype)`, the dtype being `float8_e5m2` and the granularity
+ * TENSORWISE in the parallel-linear constructors) and dgrad / wgrad run as FP8 GEMMs
+ * (`gemm_fp8_impl`) whose result carries the two tensors' inverse scales.  The pages call
+ * `_quantize_fp8_tw` without defining it; reading taken (the usual tensorwise recipe):
+ *   amax = max |x| over the tensor; scale = 57344 / amax in binary32 (57344 = the largest
+ *   finite E5M2 value), the largest finite binary32 if that overflows, 1 if amax = 0;
+ *   element = E5M2 round-to-nearest-even of (binary32) x * scale, saturating at +-57344,
+ *   sign of zero kept; scale_inv = 1 / scale in binary32.
+ * GEMM: C = (sum_k a_k b_k) * s with s = a_scale_inv * b_scale_inv rounded to binary32.
+ * -------------------------------------------------------------------------------------- */
+
+/* E5M2 code (bit 7 sign, bits 6..2 exponent with bias 15, bits 1..0 mantissa) -> value. */
+double oracle_e5m2_decode(uint8_t code) {
+    int sign = (code >> 7) & 1;
+    int exp = (code >> 2) & 31;
+    int man = code & 3;
+    double mag;
+    if (exp == 0) mag = ldexp((double)man, -16);              /* subnormal: man * 2^-16 */
+    else if (exp == 31) mag = man ? NAN : INFINITY;
+    else mag = ldexp(1.0 + man / 4.0, exp - 15);
+    return sign ? -mag : mag;
+}
+
+/* Round-to-nearest-even of a finite value onto E5M2, saturating at +-57344. */
+uint8_t oracle_e5m2_encode(double v) {
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a >= 57344.0) return sign | 0x7B;                     /* 1.75 * 2^15 */
+    double quantum;
+    if (a < ldexp(1.0, -14)) {
+        quantum = ldexp(1.0, -16);                             /* subnormal spacing */
+    } else {
+        int E;
+        frexp(a, &E);                                          /* a in [2^(E-1), 2^E) */
+        quantum = ldexp(1.0, (E - 1) - 2);                     /* 2 mantissa bits */
+    }
+    double r = nearbyint(a / quantum) * quantum;
+    if (r >= 57344.0) return sign | 0x7B;
+    if (r == 0.0) return sign;
+    int E;
+    frexp(r, &E);
+    int e = E - 1;
+    if (e < -14) return sign | (uint8_t)(r / ldexp(1.0, -16)); /* subnormal */
+    int man = (int)((r / ldexp(1.0, e) - 1.0) * 4.0);
+    return sign | (uint8_t)(((e + 15) << 2) | man);
+}
+
+/* Tensorwise E5M2 quantization of X[M,K] (bf16 bits, pitch ldx): q_row [M, ldr] holds X's
+ * codes (may be NULL), q_col [K, ldc] the codes of X^T (may be NULL); pitches in bytes,
+ * bytes past K (row copy) or M (col copy) are 0x00.  Writes amax and scale_inv.  Returns
+ * -1 on a non-finite input. */
+int oracle_fp8_quantize_tw(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q_row, int64_t ldr,
+                           uint8_t* q_col, int64_t ldc, float* amax_out, float* scale_inv_out) {
+    float amax = 0.0f;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            float v = bf16_bits_to_f32(x[m * ldx + k]);
+            if (!isfinite(v)) return -1;
+            if (fabsf(v) > amax) amax = fabsf(v);
+        }
+    volatile float scale = 1.0f;
+    if (amax > 0.0f) {
+        scale = 57344.0f / amax;
+        if (isinf(scale)) scale = FLT_MAX;
+    }
+    volatile float inv = 1.0f / scale;
+    if (q_row) memset(q_row, 0, (size_t)(M * ldr));
+    if (q_col) memset(q_col, 0, (size_t)(K * ldc));
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k) {
+            volatile float y = bf16_bits_to_f32(x[m * ldx + k]) * scale;
+            uint8_t c = oracle_e5m2_encode((double)y);
+            if (q_row) q_row[m * ldr + k] = c;
+            if (q_col) q_col[k * ldc + m] = c;
+        }
+    *amax_out = amax;
+    *scale_inv_out = inv;
+    return 0;
+}
+
+/* Codes [R, ld] (first Kc columns used) -> fp64 values [R, Kc]. */
+void oracle_fp8_dequantize(const uint8_t* q, int64_t R, int64_t Kc, int64_t ld, double* out) {
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t k = 0; k < Kc; ++k) out[r * Kc + k] = oracle_e5m2_decode(q[r * ld + k]);
+}
+
+/* The GEMM's output scale: the two inverse scales multiplied in binary32. */
+float oracle_fp8_output_scale(float a_scale_inv, float b_scale_inv) {
+    volatile float s = a_scale_inv * b_scale_inv;
+    return s;
 }

@@ -95,6 +95,29 @@ def test_argument_checks_precede_any_device_use(lib):
     assert lib.mxfp4_gemm_bias(16, 32, 48, 64, 4, 4, 4, 96, 80, 2, 0, None) == abi.MXFP4_ERR_INVALID_ARG
 
 
+def test_fp8_argument_checks_precede_any_device_use(lib):
+    # quantize: input, at least one output copy, scalar outputs, alignment
+    assert lib.mxfp4_fp8_quantize_tw(16, 4, 8, 8, None, None, 64, 68, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_fp8_quantize_tw(16, 4, 8, 8, 32, None, None, 68, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_fp8_quantize_tw(16, 4, 8, 6, 32, None, 64, 68, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_fp8_quantize_tw(16, 4, 8, 12, 32, None, 64, 68, None) == abi.MXFP4_ERR_MISALIGNED
+    assert lib.mxfp4_fp8_quantize_tw(16, 4, 8, 8, 40, None, 64, 68, None) == abi.MXFP4_ERR_MISALIGNED
+    assert lib.mxfp4_fp8_quantize_tw(16, 4, 8, 8, 32, 48, 66, 68, None) == abi.MXFP4_ERR_MISALIGNED
+    # GEMM: operands, scales, output pitch, dtype, alignment
+    assert lib.mxfp4_fp8_gemm(16, None, 48, 64, 4, 4, 4, 80, 4, 0, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_fp8_gemm(16, 32, 48, 64, 4, 4, 4, 80, 2, 0, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_fp8_gemm(16, 32, 48, 64, 4, 4, 4, 80, 4, 3, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_fp8_gemm(16, 34, 48, 64, 4, 4, 4, 80, 4, 0, None) == abi.MXFP4_ERR_MISALIGNED
+    assert lib.mxfp4_fp8_gemm(24, 32, 48, 64, 4, 4, 4, 80, 4, 0, None) == abi.MXFP4_ERR_MISALIGNED
+    G = abi.Fp8GemmTask
+    g_ok = G(16, 32, 48, 64, 4, 4, 4, 80, 4, 0)
+    garr = (G * 5)(*([g_ok] * 5))
+    assert lib.mxfp4_fp8_gemm_batch(0, garr, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_fp8_gemm_batch(5, garr, None) == abi.MXFP4_ERR_INVALID_ARG
+    gbad = (G * 2)(g_ok, G(16, 32, 48, 64, 4, 4, 4, 88, 4, 0))
+    assert lib.mxfp4_fp8_gemm_batch(2, gbad, None) == abi.MXFP4_ERR_MISALIGNED
+
+
 def test_status_strings(lib):
     for code in range(6):
         assert abi.status_string(code).startswith("MXFP4_")

@@ -511,3 +511,77 @@ def test_sr_elements_are_a_grid_neighbour_and_seed_dependent():
     rq, rs = oracle.quantize_row_sr(np.ascontiguousarray(xb.T), 5)
     assert np.array_equal(cs, rs)
     assert not np.array_equal(cq, rq)
+
+
+# --- hybrid FP8 backward: E5M2 codec, tensorwise scale, FP8 GEMM ------------------------
+
+def test_e5m2_decode_matches_torch_for_every_code():
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e5m2).float().numpy().astype(np.float64)
+    got = np.array([oracle.e5m2_decode(c) for c in codes])
+    fin = np.isfinite(want)
+    assert np.array_equal(got[fin], want[fin])
+    assert np.array_equal(np.signbit(got[fin]), np.signbit(want[fin]))
+    assert np.array_equal(np.isnan(got), np.isnan(want)) and np.array_equal(np.isinf(got), np.isinf(want))
+
+
+def test_e5m2_encode_matches_torch_cast_below_saturation():
+    # Round-to-nearest-even onto E5M2 against torch's float8_e5m2 cast, on every finite
+    # bf16 value scaled into the E5M2 range at several powers of two, and random fp32.
+    import torch
+    b, v = all_finite_bf16()
+    rng = np.random.default_rng(31)
+    vals = [v * 2.0 ** s for s in (-140, -120, -16, 0, 14)]
+    vals.append(rng.standard_normal(20000) * 2.0 ** rng.integers(-20, 16, 20000))
+    x = np.concatenate(vals)
+    x = x[np.abs(x) < 57344.0].astype(np.float32)
+    want = torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    got = np.array([oracle.e5m2_encode(float(t)) for t in x], np.uint8)
+    assert np.array_equal(got, want)
+
+
+def test_e5m2_saturates_at_the_largest_finite_value():
+    for v in (57344.0, 57345.0, 61440.0, 1e30):
+        assert oracle.e5m2_encode(v) == 0x7B and oracle.e5m2_encode(-v) == 0xFB
+    assert oracle.e5m2_decode(0x7B) == 57344.0
+
+
+def test_fp8_tensorwise_scale_and_layout():
+    rng = np.random.default_rng(32)
+    x = oracle.round_to_bf16(rng.standard_normal((70, 45)) * 3e-3)
+    xv = f32_bits_to_bf16_values(x)
+    qr, qc, amax, inv = oracle.fp8_quantize_tw(x)
+    assert amax == np.max(np.abs(xv))
+    scale = np.float32(57344.0) / np.float32(amax)
+    assert inv == np.float32(1.0) / scale
+    # the element of largest magnitude lands on the largest code
+    i = np.unravel_index(np.argmax(np.abs(xv)), xv.shape)
+    assert qr[i] & 0x7F == 0x7B
+    # each element is the E5M2 rounding of the binary32 product x * scale
+    y = (xv.astype(np.float32) * scale).astype(np.float32)
+    assert np.array_equal(qr[:, :45], np.array([[oracle.e5m2_encode(float(t)) for t in row] for row in y], np.uint8))
+    # the col copy is the row copy transposed; padding bytes are zero
+    assert np.array_equal(qc[:, :70], qr[:, :45].T)
+    assert not qr[:, 45:].any() and not qc[:, 70:].any()
+    # all-zero tensor: scale 1
+    z = np.zeros((4, 16), np.uint16)
+    qr0, _, a0, inv0 = oracle.fp8_quantize_tw(z, col=False)
+    assert a0 == 0.0 and inv0 == 1.0 and not qr0.any()
+
+
+def test_fp8_gemm_exact_on_tiny_inputs():
+    # C = (sum_k a_k b_k) * s against exact rational arithmetic.
+    rng = np.random.default_rng(33)
+    K = 40
+    a = rng.integers(0, 256, (3, oracle.fp8_pitch(K)), dtype=np.uint8)
+    b = rng.integers(0, 256, (5, oracle.fp8_pitch(K)), dtype=np.uint8)
+    for q in (a, b):   # drop infinities and NaNs (exponent 31)
+        q[(q & 0x7C) == 0x7C] &= 0x7B
+    c, cabs = oracle.fp8_gemm(a, np.float32(0.375), b, np.float32(1.0e-3), K)
+    s = Fraction(float(np.float32(np.float32(0.375) * np.float32(1.0e-3))))
+    for m in range(3):
+        for n in range(5):
+            exact = sum(Fraction(oracle.e5m2_decode(a[m, k])) * Fraction(oracle.e5m2_decode(b[n, k]))
+                        for k in range(K)) * s
+            assert abs(Fraction(c[m, n]) - exact) <= abs(exact) * Fraction(1, 2**50)
