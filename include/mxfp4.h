@@ -211,11 +211,28 @@ mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4
  *              least one of q_row / q_col; both 16-byte aligned
  *   amax, scale_inv   out, one fp32 each in device memory (4-byte aligned); the GEMMs
  *              read scale_inv from there, so no host synchronization is needed.
- * Two launches on `stream` (an amax pass, then the conversion) after a 4-byte memset of
- * *amax.  M, K >= 1. */
+ * Three launches on `stream`: *amax zeroed, an amax pass, the conversion.  M, K >= 1. */
 mxfp4_status mxfp4_fp8_quantize_tw(const void* x, int64_t M, int64_t K, int64_t ldx,
                                    void* q_row, void* q_col, float* amax, float* scale_inv,
                                    mxfp4_stream_t stream);
+
+/* One tensor of a batch: the arguments of mxfp4_fp8_quantize_tw. */
+typedef struct {
+    const void* x;
+    int64_t M;
+    int64_t K;
+    int64_t ldx;
+    void* q_row;
+    void* q_col;
+    float* amax;
+    float* scale_inv;
+} mxfp4_fp8_quantize_task;
+
+/* 1..MXFP4_MAX_BATCH tensors quantized tensorwise with the same three launches (the hybrid
+ * backward quantizes dY, X and W together), each with exactly its own call's result.
+ * Tasks must not overlap in memory.  Every task is checked before anything runs. */
+mxfp4_status mxfp4_fp8_quantize_tw_batch(int32_t count, const mxfp4_fp8_quantize_task* tasks,
+                                         mxfp4_stream_t stream);
 
 /* FP8 GEMM C[M,N] = (A . B^T) * (*a_scale_inv) * (*b_scale_inv) over E5M2 codes, the form
  * both backward `gemm_fp8_impl` calls take with the quantizer's column copies (dgrad:

@@ -42,6 +42,13 @@ class QuantizeTask(ctypes.Structure):
                 ("ldx", ctypes.c_int64), ("q_row", ctypes.c_void_p), ("s_row", ctypes.c_void_p),
                 ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p)]
 
+class Fp8QuantizeTask(ctypes.Structure):
+    """mxfp4_fp8_quantize_task of include/mxfp4.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("M", ctypes.c_int64), ("K", ctypes.c_int64), ("ldx", ctypes.c_int64),
+                ("q_row", ctypes.c_void_p), ("q_col", ctypes.c_void_p), ("amax", ctypes.c_void_p),
+                ("scale_inv", ctypes.c_void_p)]
+
+
 class Fp8GemmTask(ctypes.Structure):
     """mxfp4_fp8_gemm_task of include/mxfp4.h."""
     _fields_ = [("a", ctypes.c_void_p), ("a_scale_inv", ctypes.c_void_p), ("b", ctypes.c_void_p),
@@ -60,6 +67,7 @@ EXPORTED = (
     "mxfp4_gemm_bias",
     "mxfp4_gemm_batch",
     "mxfp4_fp8_quantize_tw",
+    "mxfp4_fp8_quantize_tw_batch",
     "mxfp4_fp8_gemm",
     "mxfp4_fp8_gemm_batch",
     "mxfp4_last_device_error",
@@ -98,6 +106,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_gemm_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i32, vp]
     lib.mxfp4_gemm_batch.argtypes = [i32, ctypes.POINTER(GemmTask), vp]
     lib.mxfp4_fp8_quantize_tw.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp]
+    lib.mxfp4_fp8_quantize_tw_batch.argtypes = [i32, ctypes.POINTER(Fp8QuantizeTask), vp]
     lib.mxfp4_fp8_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_fp8_gemm_batch.argtypes = [i32, ctypes.POINTER(Fp8GemmTask), vp]
     lib.mxfp4_last_device_error.argtypes = [vp]
@@ -201,6 +210,15 @@ def mxfp4_gemm_batch(tasks, stream=None) -> None:
 def mxfp4_fp8_quantize_tw(x, M, K, ldx, q_row, q_col, amax, scale_inv, stream=None) -> None:
     _check(load().mxfp4_fp8_quantize_tw(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(q_col), _ptr(amax),
                                         _ptr(scale_inv), _stream(stream)), "mxfp4_fp8_quantize_tw")
+
+
+def mxfp4_fp8_quantize_tw_batch(tasks, stream=None) -> None:
+    """tasks: sequence of (x, M, K, ldx, q_row, q_col, amax, scale_inv); q_row or q_col may
+    be None."""
+    arr = (Fp8QuantizeTask * max(1, len(tasks)))()
+    for i, (x, M, K, ldx, qr, qc, amax, inv) in enumerate(tasks):
+        arr[i] = Fp8QuantizeTask(_ptr(x), M, K, ldx, _ptr(qr), _ptr(qc), _ptr(amax), _ptr(inv))
+    _check(load().mxfp4_fp8_quantize_tw_batch(len(tasks), arr, _stream(stream)), "mxfp4_fp8_quantize_tw_batch")
 
 
 def mxfp4_fp8_gemm(a, a_scale_inv, b, b_scale_inv, M, N, K, c, ldc, out_dtype=MXFP4_OUT_BF16,

@@ -416,21 +416,45 @@ mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4
     return mxfp4::launch_gemm_pair(b, clusters, s) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
 
-mxfp4_status mxfp4_fp8_quantize_tw(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* q_col,
-                                   float* amax, float* scale_inv, mxfp4_stream_t stream) {
-    if (x == nullptr || (q_row == nullptr && q_col == nullptr) || amax == nullptr || scale_inv == nullptr)
-        return MXFP4_ERR_INVALID_ARG;
-    if (M < 1 || K < 1 || M > kMaxDim || K > kMaxDim || ldx < K || ldx > kMaxDim) return MXFP4_ERR_INVALID_ARG;
-    if (!aligned16(x) || (ldx % 8) != 0 || (q_row && !aligned16(q_row)) || (q_col && !aligned16(q_col)) ||
-        !aligned4(amax) || !aligned4(scale_inv))
-        return MXFP4_ERR_MISALIGNED;
+mxfp4_status mxfp4_fp8_quantize_tw_batch(int32_t count, const mxfp4_fp8_quantize_task* tasks,
+                                         mxfp4_stream_t stream) {
+    if (count < 1 || count > MXFP4_MAX_BATCH || tasks == nullptr) return MXFP4_ERR_INVALID_ARG;
+    for (int j = 0; j < count; ++j) {
+        const mxfp4_fp8_quantize_task& t = tasks[j];
+        if (t.x == nullptr || (t.q_row == nullptr && t.q_col == nullptr) || t.amax == nullptr ||
+            t.scale_inv == nullptr)
+            return MXFP4_ERR_INVALID_ARG;
+        if (t.M < 1 || t.K < 1 || t.M > kMaxDim || t.K > kMaxDim || t.ldx < t.K || t.ldx > kMaxDim)
+            return MXFP4_ERR_INVALID_ARG;
+        if (!aligned16(t.x) || (t.ldx % 8) != 0 || (t.q_row && !aligned16(t.q_row)) ||
+            (t.q_col && !aligned16(t.q_col)) || !aligned4(t.amax) || !aligned4(t.scale_inv))
+            return MXFP4_ERR_MISALIGNED;
+    }
     DeviceState* dev = nullptr;
     const mxfp4_status st = device_ready(&dev);
     if (st != MXFP4_OK) return st;
-    mxfp4::Fp8QuantArgs a{x, M, K, ldx, q_row, pad16(K), q_col, pad16(M), amax, scale_inv};
-    return mxfp4::launch_fp8_quantize(a, dev->sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+    mxfp4::Fp8QuantBatch b;
+    std::memset(&b, 0, sizeof(b));
+    int64_t rows = 0, tiles = 0;
+    for (int j = 0; j < count; ++j) {
+        const mxfp4_fp8_quantize_task& t = tasks[j];
+        b.t[j] = mxfp4::Fp8QuantArgs{t.x, t.M, t.K, t.ldx, t.q_row, pad16(t.K), t.q_col, pad16(t.M), t.amax,
+                                     t.scale_inv};
+        rows += t.M;
+        tiles += cdiv(t.M, 64) * cdiv(t.K, 64);
+        b.row_end[j] = rows;
+        b.tile_end[j] = tiles;
+    }
+    b.count = count;
+    return mxfp4::launch_fp8_quantize(b, dev->sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MXFP4_OK
                : MXFP4_ERR_CUDA;
+}
+
+mxfp4_status mxfp4_fp8_quantize_tw(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* q_col,
+                                   float* amax, float* scale_inv, mxfp4_stream_t stream) {
+    const mxfp4_fp8_quantize_task t{x, M, K, ldx, q_row, q_col, amax, scale_inv};
+    return mxfp4_fp8_quantize_tw_batch(1, &t, stream);
 }
 
 mxfp4_status mxfp4_fp8_gemm_batch(int32_t count, const mxfp4_fp8_gemm_task* tasks, mxfp4_stream_t stream) {

@@ -23,7 +23,17 @@ struct Fp8QuantArgs {
     float* scale_inv;
 };
 
-cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int sms, cudaStream_t stream);
+// Up to kMaxFp8Tasks tensors in one pass of each kernel: row_end / tile_end are the
+// running totals of each task's rows and 64 x 64 tiles.
+constexpr int kMaxFp8Tasks = 4;
+struct Fp8QuantBatch {
+    Fp8QuantArgs t[kMaxFp8Tasks];
+    int64_t row_end[kMaxFp8Tasks];
+    int64_t tile_end[kMaxFp8Tasks];
+    int32_t count;
+};
+
+cudaError_t launch_fp8_quantize(const Fp8QuantBatch& b, int sms, cudaStream_t stream);
 
 // One FP8 GEMM C[M,N] = (A . B^T) * (*a_scale_inv) * (*b_scale_inv): A [M, K] and B [N, K]
 // E5M2 codes, K-major, row pitches lda / ldb bytes.
@@ -44,7 +54,6 @@ struct Fp8GemmArgs {
 // Up to kMaxFp8Tasks GEMMs in one launch of CTA pairs, tile t belonging to the first
 // problem j with t < tile_end[j].  amap / bmap: u8 {K, rows} maps, box {128, 128}, 128-byte
 // swizzle; cmap as for the MXFP4 GEMMs (box of 64 bytes x 32 rows, 64-byte swizzle).
-constexpr int kMaxFp8Tasks = 4;
 struct Fp8GemmBatch {
     CUtensorMap amap[kMaxFp8Tasks];
     CUtensorMap bmap[kMaxFp8Tasks];

@@ -7,9 +7,10 @@
 // largest finite fp32 if that overflows, 1 for amax = 0); element = E5M2 round-to-nearest-
 // even of x * scale (fp32 product), saturating at +-57344; scale_inv = 1 / scale.
 //
-// Two launches: an amax pass (each warp folds its maximum into the output amax with one
-// atomicMax on the fp32 bit pattern, which orders like the value for non-negative floats)
-// and a conversion pass over 64 x 64 tiles that writes the row copy (X's codes, row pitch
+// Up to four tensors go through three launches together: the amax words are zeroed, an
+// amax pass (each warp folds its maxima into the tasks' amax words with one atomicMax on
+// the fp32 bit pattern, which orders like the value for non-negative floats) and a
+// conversion pass over 64 x 64 tiles that writes the row copy (X's codes, row pitch
 // ldr bytes) and/or the column copy (X^T's codes, row pitch ldc bytes) through a shared
 // transpose, so both copies leave in 16-byte row pieces.  The column copies are what keep
 // the FP8 GEMMs in the same K-major ("TN") form as the MXFP4 ones: dgrad reads W^T, wgrad
@@ -26,26 +27,53 @@ namespace {
 constexpr int kFt = 64;            // tile edge
 constexpr int kFThreads = 256;     // 4 threads per tile row, 16 elements each
 
-__global__ void __launch_bounds__(256) fp8_amax_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
-                                                        int64_t ldx, uint32_t* amax_bits) {
-    uint32_t m = 0;   // largest |x| as fp32 bits (bf16 magnitude bits << 16)
-    const int64_t chunks = (K + 7) / 8;
-    const int64_t total = M * chunks;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / chunks, c = (i % chunks) * 8;
-        const uint16_t* p = x + r * ldx + c;
-        if (c + 8 <= K) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+__global__ void fp8_zero_kernel(const __grid_constant__ Fp8QuantBatch B) {
+    if (static_cast<int>(threadIdx.x) < B.count) *B.t[threadIdx.x].amax = 0.0f;
+}
+
+// One warp per row at a time (rows of all tasks in sequence, task of a row by row_end),
+// its lanes across the row's 8-element chunks, four independent 16-byte loads in flight
+// per lane; no division on the hot path.
+__global__ void __launch_bounds__(256) fp8_amax_kernel(const __grid_constant__ Fp8QuantBatch B) {
+    uint32_t m[kMaxFp8Tasks] = {0u, 0u, 0u, 0u};   // per task: largest |x| as bf16 magnitude bits
+    const int64_t rows = B.row_end[B.count - 1];
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    int j = 0;
+    for (int64_t g = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g < rows; g += warps) {
+        while (j + 1 < B.count && g >= B.row_end[j]) ++j;   // rows only grow along the loop
+        const Fp8QuantArgs& a = B.t[j];
+        const int64_t r = g - (j > 0 ? B.row_end[j - 1] : 0);
+        const uint16_t* const row = static_cast<const uint16_t*>(a.x) + r * a.ldx;
+        const int64_t K = a.K;
+        uint32_t v = 0;
+        for (int64_t c0 = static_cast<int64_t>(lane) * 8; c0 < K; c0 += 32 * 8 * 4) {
+            uint4 q[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) m = max(m, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
-        } else {
-            for (int64_t j = 0; c + j < K; ++j) m = max(m, static_cast<uint32_t>(__ldg(p + j)) & 0x7FFFu);
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + u * 32 * 8;
+                q[u] = c + 8 <= K ? __ldg(reinterpret_cast<const uint4*>(row + c)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v = max(v, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+                const int64_t c = c0 + u * 32 * 8;
+                if (c < K && c + 8 > K)   // the row's ragged last chunk
+                    for (int64_t k = 0; c + k < K; ++k) v = max(v, static_cast<uint32_t>(__ldg(row + c + k)) & 0x7FFFu);
+            }
         }
+#pragma unroll
+        for (int k = 0; k < kMaxFp8Tasks; ++k)
+            if (k == j) m[k] = max(m[k], v);
     }
-    m = __reduce_max_sync(0xFFFFFFFFu, m);
-    if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(amax_bits, m << 16);
+#pragma unroll
+    for (int k = 0; k < kMaxFp8Tasks; ++k) {
+        if (k >= B.count) break;
+        const uint32_t w = __reduce_max_sync(0xFFFFFFFFu, m[k]);
+        if (lane == 0 && w != 0) atomicMax(reinterpret_cast<uint32_t*>(B.t[k].amax), w << 16);
+    }
 }
 
 __device__ __forceinline__ uint32_t e5m2x2(float lo, float hi) {
@@ -54,50 +82,76 @@ __device__ __forceinline__ uint32_t e5m2x2(float lo, float hi) {
     return r;
 }
 
-__global__ void __launch_bounds__(kFThreads) fp8_quantize_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
-                                                                 int64_t ldx, uint8_t* q_row, int64_t ldr,
-                                                                 uint8_t* q_col, int64_t ldc, const float* amax_p,
-                                                                 float* scale_inv_p) {
-    __shared__ __align__(16) uint8_t tile[kFt][kFt + 16];
-    const float amax = *amax_p;
+__device__ __forceinline__ float tensor_scale(float amax) {
     float scale = 1.0f;
     if (amax > 0.0f) {
         scale = __fdiv_rn(57344.0f, amax);
         if (isinf(scale)) scale = FLT_MAX;
     }
-    if (blockIdx.x == 0 && threadIdx.x == 0) *scale_inv_p = __fdiv_rn(1.0f, scale);
+    return scale;
+}
 
+// The 16 elements of tile tg that thread (r, c) converts: row m0 + r, columns k0 + c ..
+// + 15 of its task (zero outside the tensor).
+__device__ __forceinline__ void load_piece(const Fp8QuantBatch& B, int64_t tg, int r, int c, uint32_t* w) {
+    int j = 0;
+    while (j + 1 < B.count && tg >= B.tile_end[j]) ++j;
+    const Fp8QuantArgs& a = B.t[j];
+    const int64_t tl = tg - (j > 0 ? B.tile_end[j - 1] : 0);
+    const int64_t tiles_k = (a.K + kFt - 1) / kFt;
+    const int64_t row = (tl / tiles_k) * kFt + r, col = (tl % tiles_k) * kFt + c;
+    const uint16_t* p = static_cast<const uint16_t*>(a.x) + row * a.ldx + col;
+    if (row < a.M && col + 16 <= a.K) {
+        const uint4 va = __ldg(reinterpret_cast<const uint4*>(p));
+        const uint4 vb = __ldg(reinterpret_cast<const uint4*>(p + 8));
+        w[0] = va.x; w[1] = va.y; w[2] = va.z; w[3] = va.w;
+        w[4] = vb.x; w[5] = vb.y; w[6] = vb.z; w[7] = vb.w;
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t lo = (row < a.M && col + 2 * e < a.K) ? __ldg(p + 2 * e) : 0u;
+            const uint32_t hi = (row < a.M && col + 2 * e + 1 < a.K) ? __ldg(p + 2 * e + 1) : 0u;
+            w[e] = lo | (hi << 16);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kFThreads) fp8_quantize_kernel(const __grid_constant__ Fp8QuantBatch B) {
+    __shared__ __align__(16) uint8_t tile[kFt][kFt + 16];
+    if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < B.count) {
+        const Fp8QuantArgs& a = B.t[threadIdx.x];
+        *a.scale_inv = __fdiv_rn(1.0f, tensor_scale(*a.amax));
+    }
     const int t = threadIdx.x;
     const int r = t >> 2, c = (t & 3) * 16;
-    const int64_t tiles_k = (K + kFt - 1) / kFt;
-    const int64_t tiles = ((M + kFt - 1) / kFt) * tiles_k;
-    for (int64_t tl = blockIdx.x; tl < tiles; tl += gridDim.x) {
-        const int64_t m0 = (tl / tiles_k) * kFt, k0 = (tl % tiles_k) * kFt;
-        // 16 elements of row m0 + r, columns k0 + c .. + 15 (zero outside X)
+    const int64_t tiles = B.tile_end[B.count - 1];
+    uint32_t next[8];
+    if (static_cast<int64_t>(blockIdx.x) < tiles) load_piece(B, blockIdx.x, r, c, next);
+    for (int64_t tg = blockIdx.x; tg < tiles; tg += gridDim.x) {
         uint32_t w[8];
-        const int64_t row = m0 + r, col = k0 + c;
-        const uint16_t* p = x + row * ldx + col;
-        if (row < M && col + 16 <= K) {
-            const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
-            const uint4 b = __ldg(reinterpret_cast<const uint4*>(p + 8));
-            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-            w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-        } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t lo = (row < M && col + 2 * j < K) ? __ldg(p + 2 * j) : 0u;
-                const uint32_t hi = (row < M && col + 2 * j + 1 < K) ? __ldg(p + 2 * j + 1) : 0u;
-                w[j] = lo | (hi << 16);
-            }
-        }
+        for (int e = 0; e < 8; ++e) w[e] = next[e];
+        // the next tile's loads go out before this tile's stores and barriers
+        if (tg + gridDim.x < tiles) load_piece(B, tg + gridDim.x, r, c, next);
+        int j = 0;
+        while (j + 1 < B.count && tg >= B.tile_end[j]) ++j;
+        const Fp8QuantArgs& a = B.t[j];
+        const int64_t tl = tg - (j > 0 ? B.tile_end[j - 1] : 0);
+        const int64_t M = a.M, K = a.K, ldr = a.ldr, ldc = a.ldc;
+        uint8_t* const q_row = static_cast<uint8_t*>(a.q_row);
+        uint8_t* const q_col = static_cast<uint8_t*>(a.q_col);
+        const float scale = tensor_scale(*a.amax);
+        const int64_t tiles_k = (K + kFt - 1) / kFt;
+        const int64_t m0 = (tl / tiles_k) * kFt, k0 = (tl % tiles_k) * kFt;
+        const int64_t row = m0 + r, col = k0 + c;
         uint32_t q[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t e01 = e5m2x2(__fmul_rn(__uint_as_float(w[2 * j] << 16), scale),
-                                        __fmul_rn(__uint_as_float(w[2 * j] & 0xFFFF0000u), scale));
-            const uint32_t e23 = e5m2x2(__fmul_rn(__uint_as_float(w[2 * j + 1] << 16), scale),
-                                        __fmul_rn(__uint_as_float(w[2 * j + 1] & 0xFFFF0000u), scale));
-            q[j] = e01 | (e23 << 16);
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t e01 = e5m2x2(__fmul_rn(__uint_as_float(w[2 * e] << 16), scale),
+                                        __fmul_rn(__uint_as_float(w[2 * e] & 0xFFFF0000u), scale));
+            const uint32_t e23 = e5m2x2(__fmul_rn(__uint_as_float(w[2 * e + 1] << 16), scale),
+                                        __fmul_rn(__uint_as_float(w[2 * e + 1] & 0xFFFF0000u), scale));
+            q[e] = e01 | (e23 << 16);
         }
         if (q_row != nullptr && row < M && col < ldr)
             *reinterpret_cast<uint4*>(q_row + row * ldr + col) = make_uint4(q[0], q[1], q[2], q[3]);
@@ -108,10 +162,10 @@ __global__ void __launch_bounds__(kFThreads) fp8_quantize_kernel(const uint16_t*
             const int kc = t >> 2;
             uint32_t o[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                o[j] = static_cast<uint32_t>(tile[c + 4 * j][kc]) | (static_cast<uint32_t>(tile[c + 4 * j + 1][kc]) << 8) |
-                       (static_cast<uint32_t>(tile[c + 4 * j + 2][kc]) << 16) |
-                       (static_cast<uint32_t>(tile[c + 4 * j + 3][kc]) << 24);
+            for (int e = 0; e < 4; ++e)
+                o[e] = static_cast<uint32_t>(tile[c + 4 * e][kc]) | (static_cast<uint32_t>(tile[c + 4 * e + 1][kc]) << 8) |
+                       (static_cast<uint32_t>(tile[c + 4 * e + 2][kc]) << 16) |
+                       (static_cast<uint32_t>(tile[c + 4 * e + 3][kc]) << 24);
             const int64_t krow = k0 + kc, mcol = m0 + c;
             if (krow < K && mcol < ldc)
                 *reinterpret_cast<uint4*>(q_col + krow * ldc + mcol) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -122,21 +176,19 @@ __global__ void __launch_bounds__(kFThreads) fp8_quantize_kernel(const uint16_t*
 
 }  // namespace
 
-cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int sms, cudaStream_t stream) {
-    cudaError_t e = cudaMemsetAsync(a.amax, 0, sizeof(float), stream);
+cudaError_t launch_fp8_quantize(const Fp8QuantBatch& b, int sms, cudaStream_t stream) {
+    fp8_zero_kernel<<<1, 32, 0, stream>>>(b);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int64_t chunks = a.M * ((a.K + 7) / 8);
-    const int64_t want = (chunks + 255) / 256;
+    const int64_t rows = b.row_end[b.count - 1];
+    const int64_t want = (rows + 7) / 8;   // 8 warps per CTA, one row each
     const int grid1 = static_cast<int>(want < int64_t{sms} * 8 ? want : int64_t{sms} * 8);
-    fp8_amax_kernel<<<grid1 > 0 ? grid1 : 1, 256, 0, stream>>>(static_cast<const uint16_t*>(a.x), a.M, a.K, a.ldx,
-                                                               reinterpret_cast<uint32_t*>(a.amax));
+    fp8_amax_kernel<<<grid1 > 0 ? grid1 : 1, 256, 0, stream>>>(b);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int64_t tiles = ((a.M + kFt - 1) / kFt) * ((a.K + kFt - 1) / kFt);
+    const int64_t tiles = b.tile_end[b.count - 1];
     const int grid2 = static_cast<int>(tiles < int64_t{sms} * 8 ? tiles : int64_t{sms} * 8);
-    fp8_quantize_kernel<<<grid2, kFThreads, 0, stream>>>(static_cast<const uint16_t*>(a.x), a.M, a.K, a.ldx,
-                                                         static_cast<uint8_t*>(a.q_row), a.ldr,
-                                                         static_cast<uint8_t*>(a.q_col), a.ldc, a.amax, a.scale_inv);
+    fp8_quantize_kernel<<<grid2, kFThreads, 0, stream>>>(b);
     return cudaGetLastError();
 }
 

@@ -133,12 +133,11 @@ class MXFP4Linear:
         K-major operands of the two TN GEMMs)."""
         x, w = self._saved
         sc = self.f8_scalars
-        abi.mxfp4_fp8_quantize_tw(dy, self.M, self.N, dy.stride(0), self.dy_f8, self.dy_f8_col,
-                                  sc[0:1], sc[1:2], stream)
-        abi.mxfp4_fp8_quantize_tw(x, self.M, self.K, x.stride(0), None, self.x_f8_col,
-                                  sc[2:3], sc[3:4], stream)
-        abi.mxfp4_fp8_quantize_tw(w, self.N, self.K, w.stride(0), None, self.w_f8_col,
-                                  sc[4:5], sc[5:6], stream)
+        abi.mxfp4_fp8_quantize_tw_batch([
+            (dy, self.M, self.N, dy.stride(0), self.dy_f8, self.dy_f8_col, sc[0:1], sc[1:2]),
+            (x, self.M, self.K, x.stride(0), None, self.x_f8_col, sc[2:3], sc[3:4]),
+            (w, self.N, self.K, w.stride(0), None, self.w_f8_col, sc[4:5], sc[5:6]),
+        ], stream)
 
     def fp8_bwd_gemms(self, stream=None):
         """dX = dY . W (A = dY codes, B = W^T codes) and dW = dY^T . X (A = dY^T codes,
@@ -216,5 +215,5 @@ class MXFP4Linear:
     @property
     def launches_per_step(self) -> int:
         if self.fp8_backward:
-            return 2 + 3 * 2 + 1   # X+W, fwd; three FP8 quantizations (amax, convert); the GEMMs
+            return 2 + 3 + 1   # X+W, fwd; FP8 quantization of dY, X, W (zero, amax, convert); the GEMMs
         return 4 if self.train else 2

@@ -103,6 +103,15 @@ def test_fp8_argument_checks_precede_any_device_use(lib):
     assert lib.mxfp4_fp8_quantize_tw(16, 4, 8, 12, 32, None, 64, 68, None) == abi.MXFP4_ERR_MISALIGNED
     assert lib.mxfp4_fp8_quantize_tw(16, 4, 8, 8, 40, None, 64, 68, None) == abi.MXFP4_ERR_MISALIGNED
     assert lib.mxfp4_fp8_quantize_tw(16, 4, 8, 8, 32, 48, 66, 68, None) == abi.MXFP4_ERR_MISALIGNED
+    Q = abi.Fp8QuantizeTask
+    q_ok = Q(16, 4, 8, 8, 32, None, 64, 68)
+    qarr = (Q * 5)(*([q_ok] * 5))
+    assert lib.mxfp4_fp8_quantize_tw_batch(0, qarr, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_fp8_quantize_tw_batch(5, qarr, None) == abi.MXFP4_ERR_INVALID_ARG
+    qbad = (Q * 2)(q_ok, Q(16, 4, 8, 8, None, None, 64, 68))      # no output copy
+    assert lib.mxfp4_fp8_quantize_tw_batch(2, qbad, None) == abi.MXFP4_ERR_INVALID_ARG
+    qbad = (Q * 2)(q_ok, Q(16, 4, 8, 8, 40, None, 64, 68))        # q_row not 16-byte aligned
+    assert lib.mxfp4_fp8_quantize_tw_batch(2, qbad, None) == abi.MXFP4_ERR_MISALIGNED
     # GEMM: operands, scales, output pitch, dtype, alignment
     assert lib.mxfp4_fp8_gemm(16, None, 48, 64, 4, 4, 4, 80, 4, 0, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_fp8_gemm(16, 32, 48, 64, 4, 4, 4, 80, 2, 0, None) == abi.MXFP4_ERR_INVALID_ARG

@@ -158,3 +158,32 @@ def test_hybrid_backward_flux_mlp_sampled():
     (cx, ax), (cw, aw) = oracle_hybrid_backward(t, rdx, rdw)
     check_gemm(dx[torch.as_tensor(rdx, device="cuda")], cx, ax, "flux hybrid dgrad")
     check_gemm(dw[torch.as_tensor(rdw, device="cuda")], cw, aw, "flux hybrid wgrad")
+
+
+def test_fp8_quantize_batch_equals_single_calls():
+    # One batched call over 1..3 tensors (row and/or column copies) gives each tensor its
+    # own call's bytes and scalars.
+    shapes = [((384, 1000), True, True), ((129, 200), False, True), ((640, 384), True, False)]
+    xs = [pitched(workloads.student_t3(s, 0.1 * (i + 1), 801 + i)) for i, (s, _, _) in enumerate(shapes)]
+    singles = []
+    for x, (_, row, col) in zip(xs, shapes):
+        qr, qc, amax, inv = abi.fp8_quantize(x, row=row, col=col)
+        singles.append((qr, qc, amax.clone(), inv.clone()))
+    torch.cuda.synchronize()
+    for n in (1, 2, 3):
+        tasks, outs = [], []
+        sc = torch.full((2 * n,), float("nan"), dtype=torch.float32, device="cuda")
+        for i, (x, (_, row, col)) in enumerate(zip(xs[:n], shapes[:n])):
+            M, K = x.shape
+            qr = torch.full((M, abi.fp8_pitch(K)), 0xAB, dtype=torch.uint8, device="cuda") if row else None
+            qc = torch.full((K, abi.fp8_pitch(M)), 0xAB, dtype=torch.uint8, device="cuda") if col else None
+            tasks.append((x, M, K, x.stride(0), qr, qc, sc[2 * i:2 * i + 1], sc[2 * i + 1:2 * i + 2]))
+            outs.append((qr, qc, sc[2 * i:2 * i + 1], sc[2 * i + 1:2 * i + 2]))
+        abi.mxfp4_fp8_quantize_tw_batch(tasks)
+        torch.cuda.synchronize()
+        assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+        for got, want in zip(outs, singles[:n]):
+            for g, w in zip(got, want):
+                assert (g is None) == (w is None)
+                if g is not None:
+                    assert torch.equal(g.view(torch.uint8).cpu(), w.view(torch.uint8).cpu())
