@@ -399,14 +399,18 @@ def run_ours(args, rank, world, local_rank):
 # ---------------------------------------------------------------------------------------
 # the CPU oracle on a bounded sample (cpu_baseline, and the reference arm)
 # ---------------------------------------------------------------------------------------
-def oracle_sample(workload_name, seconds, fp8_backward=False):
+def oracle_sample(workload_name, seconds, fp8_backward=False, threads=1):
     """Times the oracle on slices of the workload and extrapolates one full step.
 
-    Sample: the oracle's dual (or row-only) quantizer on leading row slabs of X, W and dY,
-    and its fp64 GEMM on a block of output rows of each GEMM shape; each part is repeated
-    until it has run for about seconds/2.  Step time = per-element quantizer time x all
-    quantized elements + per-MAC GEMM time x all MACs of the step's GEMMs.
+    Sample: the oracle's quantizers (dual, or row-only; with fp8_backward, row-only MX for
+    X and W plus tensorwise E5M2 of dY, X and W) on 128-row slabs of X, W and dY, and its
+    fp64 GEMM on 8-row blocks of output against 512 columns; each part runs for about
+    seconds/2 of wall time on `threads` host threads at once (the oracle's C functions
+    release the GIL, so the threads run in parallel; each thread takes its own slabs and
+    blocks).  Step time = wall time per quantized element x all quantized elements + wall
+    time per MAC x all MACs of the step's GEMMs.
     """
+    import concurrent.futures
     import numpy as np
 
     import oracle
@@ -419,46 +423,71 @@ def oracle_sample(workload_name, seconds, fp8_backward=False):
     bits = {k: workloads.bf16_bits(v) for k, v in t.items()}
     fp8 = fp8_backward and lin.train
     quant = oracle.quantize_dual if (lin.train and not fp8) else oracle.quantize_row
+    threads = max(1, int(threads))
 
-    q_elems = q_time = 0.0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds / 2:
-        for k in bits:
-            slab = np.ascontiguousarray(bits[k][:128])
-            s = time.perf_counter()
-            if fp8:   # row-only MX for X and W, tensorwise E5M2 for all three
-                if k != "dY":
-                    quant(slab)
-                oracle.fp8_quantize_tw(slab, row=(k == "dY"), col=True)
-            else:
-                quant(slab)
-            q_time += time.perf_counter() - s
-            q_elems += slab.size
-    xq, xs = oracle.quantize_row(np.ascontiguousarray(bits["X"][:8]))
+    def slab(k, w):
+        rows = bits[k].shape[0]
+        r0 = (128 * w) % max(1, rows - 127)
+        return np.ascontiguousarray(bits[k][r0:r0 + 128])
+
+    def quant_worker(w):
+        slabs = {k: slab(k, w) for k in bits}
+        elems = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds / 2:
+            for k, sl in slabs.items():
+                if fp8:   # row-only MX for X and W, tensorwise E5M2 for all three
+                    if k != "dY":
+                        quant(sl)
+                    oracle.fp8_quantize_tw(sl, row=(k == "dY"), col=True)
+                else:
+                    quant(sl)
+                elems += sl.size
+        return elems
+
     wq, ws = oracle.quantize_row(np.ascontiguousarray(bits["W"][:512]))
-    a = oracle.dequantize(xq, xs)
     b = oracle.dequantize(wq, ws)
-    g_macs = g_time = 0.0
-    t0 = time.perf_counter()
-    while time.perf_counter() - t0 < seconds / 2:
-        s = time.perf_counter()
-        oracle.gemm_dequantized(a, b, want_abs=False)
-        g_time += time.perf_counter() - s
-        g_macs += a.shape[0] * b.shape[0] * a.shape[1]
+
+    def gemm_worker(w):
+        xq, xs = oracle.quantize_row(slab("X", w)[:8])
+        a = oracle.dequantize(xq, xs)
+        macs = 0
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds / 2:
+            oracle.gemm_dequantized(a, b, want_abs=False)
+            macs += a.shape[0] * b.shape[0] * a.shape[1]
+        return macs
+
+    with concurrent.futures.ThreadPoolExecutor(threads) as ex:
+        t0 = time.perf_counter()
+        q_elems = sum(ex.map(quant_worker, range(threads)))
+        q_wall = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        g_macs = sum(ex.map(gemm_worker, range(threads)))
+        g_wall = time.perf_counter() - t0
     total_q = M * K + N * K + (M * N if lin.train else 0)
+    if fp8:
+        total_q = 2 * (M * K + N * K) + M * N
     total_macs = M * N * K * (3 if lin.train else 1)
-    step_s = q_time / q_elems * total_q + g_time / g_macs * total_macs
+    step_s = q_wall / q_elems * total_q + g_wall / g_macs * total_macs
+    kind = "row-only MX + tensorwise E5M2" if fp8 else "dual" if lin.train else "row-only"
     return {
         "step_seconds": step_s,
         "value": lin.flops_step / step_s / 1e12,
-        "sample": (f"oracle {'row-only MX + tensorwise E5M2' if fp8 else 'dual' if lin.train else 'row-only'} "
-                   f"quantizer on 128-row slabs of "
-                   f"X, W{', dY' if lin.train else ''} ({int(q_elems)} elements) and fp64 GEMM "
-                   f"on 8x512 output blocks at K={oracle.padded(K)} ({int(g_macs)} MACs); "
-                   f"one full step extrapolated per element / per MAC"),
-        "cores": 1,
+        "sample": (f"oracle {kind} quantizer on 128-row slabs of X, W{', dY' if lin.train else ''} "
+                   f"({int(q_elems)} elements) and fp64 GEMM on 8x512 output blocks at "
+                   f"K={oracle.padded(K)} ({int(g_macs)} MACs), on {threads} host thread(s); one "
+                   f"full step extrapolated per element / per MAC of wall time"),
+        "cores": threads,
         "kind": "oracle",
     }
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
 
 
 def run_reference(args, rank, world):
@@ -467,9 +496,10 @@ def run_reference(args, rank, world):
     import oracle.build
     oracle.build.build()
     per = max(2.0, args.cpu_baseline_seconds / max(1, args.steps))
+    cores = host_cores()
     for _ in range(args.warmup):
-        oracle_sample(args.workload, 0.2)
-    vals = [oracle_sample(args.workload, per) for _ in range(args.steps)]
+        oracle_sample(args.workload, 0.2, args.fp8_backward, cores)
+    vals = [oracle_sample(args.workload, per, args.fp8_backward, cores) for _ in range(args.steps)]
     step_s = statistics.mean(v["step_seconds"] for v in vals)
     value = vals[0]["value"] if len(vals) == 1 else statistics.mean(v["value"] for v in vals)
     from mxfp4_block_scaled_quantize_gb300 import workloads
@@ -490,7 +520,7 @@ def run_reference(args, rank, world):
         "data": "synthetic",
         "config": {"workload": args.workload, "M": lin.M, "N": lin.N, "K": lin.K,
                    "parallelism": "host cores of rank 0"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": vals[0]["sample"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -531,9 +561,13 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:
-        base = oracle_sample(args.workload, args.cpu_baseline_seconds, args.fp8_backward)
+        # the oracle on every host core, and on one (half of the time budget each)
+        cores = host_cores()
+        base = oracle_sample(args.workload, args.cpu_baseline_seconds / 2, args.fp8_backward, cores)
+        one = oracle_sample(args.workload, args.cpu_baseline_seconds / 2, args.fp8_backward, 1)
         line["cpu_baseline"] = {"value": base["value"], "unit": "TFLOP/s", "cores": base["cores"],
-                                "kind": "oracle", "sample": base["sample"]}
+                                "kind": "oracle", "sample": base["sample"],
+                                "single_core_value": one["value"]}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
