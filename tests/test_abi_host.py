@@ -127,6 +127,23 @@ def test_fp8_argument_checks_precede_any_device_use(lib):
     assert lib.mxfp4_fp8_gemm_batch(2, gbad, None) == abi.MXFP4_ERR_MISALIGNED
 
 
+def test_no_usable_device_fails_loudly(lib):
+    # Well-formed calls on a host without a CUDA device return an error status (no
+    # fallback path, nothing dereferenced: the device gate comes before any launch).
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    bad = (abi.MXFP4_ERR_CUDA, abi.MXFP4_ERR_UNSUPPORTED_DEVICE)
+    assert lib.mxfp4_quantize(0x10000, 4, 8, 8, 0x20000, 0x30000, 1, None) in bad
+    assert lib.mxfp4_quantize_dual(0x10000, 4, 8, 8, 0x20000, 0x30000, 0x40000, 0x50000, 1, None) in bad
+    assert lib.mxfp4_quantize_dual_sr(0x10000, 4, 8, 8, 0x20000, 0x30000, 0x40000, 0x50000, 1, 7, None) in bad
+    assert lib.mxfp4_gemm(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x50000, 4, 0, None) in bad
+    assert lib.mxfp4_gemm_bias(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x60000, 0x50000, 4, 0, None) in bad
+    assert lib.mxfp4_fp8_quantize_tw(0x10000, 4, 8, 8, 0x20000, None, 0x30000, 0x30004, None) in bad
+    assert lib.mxfp4_fp8_gemm(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x50000, 4, 0, None) in bad
+    assert lib.mxfp4_last_device_error(None) in bad
+
+
 def test_status_strings(lib):
     for code in range(6):
         assert abi.status_string(code).startswith("MXFP4_")

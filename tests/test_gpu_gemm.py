@@ -288,3 +288,22 @@ def test_gemm_argument_errors():
     assert lib.mxfp4_gemm(p(q), p(s), p(q), p(s), 128, 128, 0, p(c), 128, 0, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_gemm(p(q) + 8, p(s), p(q), p(s), 128, 128, 128, p(c), 128, 0, None) == abi.MXFP4_ERR_MISALIGNED
     assert lib.mxfp4_gemm(p(q), p(s), p(q), p(s), 128, 128, 128, p(c), 128, 5, None) == abi.MXFP4_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("backward", ["mxfp4", "fp8"])
+def test_repeated_steps_are_bit_identical(backward):
+    # The same kernels with the same arguments give bit-identical outputs: every output tile
+    # is computed by one CTA pair in a fixed K order, and the only atomic (the FP8 amax) is
+    # a maximum, which does not depend on the order of arrival.
+    wl = workloads.FLUX_MLP_STEP
+    lin = wl.linears[0]
+    t = wl.tensors(0)
+    x, w, dy = (t[k].cuda() for k in ("X", "W", "dY"))
+    layer = MXFP4Linear(lin.M, lin.N, lin.K, train=True, backward=backward)
+    first = [o.clone() for o in layer.step(x, w, dy)]
+    for _ in range(2):
+        outs = layer.step(x, w, dy)
+        torch.cuda.synchronize()
+        for a, b in zip(outs, first):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
