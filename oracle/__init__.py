@@ -52,6 +52,9 @@ def _load():
         for fn in (lib.oracle_bias_add_bf16, lib.oracle_bias_add_f32):
             fn.argtypes = [vp, vp, i64, i64, vp]
             fn.restype = None
+        for fn in (lib.oracle_quantize_row_2d, lib.oracle_quantize_col_2d):
+            fn.argtypes = [vp, i64, i64, i64, vp, vp]
+            fn.restype = ctypes.c_int
         lib.oracle_e5m2_decode.argtypes = [u8]
         lib.oracle_e5m2_decode.restype = f64
         lib.oracle_e5m2_encode.argtypes = [f64]
@@ -338,3 +341,29 @@ def fp8_gemm(a_q, a_scale_inv, b_q, b_scale_inv, K, rows=None):
     c, cabs = gemm_dequantized(a, b)
     s = fp8_output_scale(a_scale_inv, b_scale_inv)
     return c * s, cabs * s
+
+
+# --- 2-D (32 x 32) block scales for weights ---------------------------------------------
+
+def quantize_row_2d(x_bits):
+    """Row blob of X[M,K] with one scale per 32 x 32 block (plain scale layout)."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    Kp = padded(K)
+    q = np.empty((M, Kp // 2), np.uint8)
+    s = np.empty((M, Kp // BLOCK), np.uint8)
+    if _load().oracle_quantize_row_2d(_ptr(x_bits), M, K, K, _ptr(q), _ptr(s)):
+        raise ValueError("non-finite input")
+    return q, s
+
+
+def quantize_col_2d(x_bits):
+    """Col blob of X[M,K] with the same 32 x 32 block scales."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    Mp = padded(M)
+    q = np.empty((K, Mp // 2), np.uint8)
+    s = np.empty((K, Mp // BLOCK), np.uint8)
+    if _load().oracle_quantize_col_2d(_ptr(x_bits), M, K, K, _ptr(q), _ptr(s)):
+        raise ValueError("non-finite input")
+    return q, s

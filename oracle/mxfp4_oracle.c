@@ -38,6 +38,7 @@
 #include <float.h>
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define BLOCK 32
@@ -477,4 +478,84 @@ void oracle_fp8_dequantize(const uint8_t* q, int64_t R, int64_t Kc, int64_t ld, 
 float oracle_fp8_output_scale(float a_scale_inv, float b_scale_inv) {
     volatile float s = a_scale_inv * b_scale_inv;
     return s;
+}
+
+/* ---------------------------------------------------------------------------------------
+ * 2-D block scales for weights: `_quantize_weight_dual` in primus_turbo_mxfp4_local.py sets
+ * `rowwise_use_2d_block` and `colwise_use_2d_block` for the weight (activations and
+ * gradients keep 1 x 32 blocks).  The pages name the flags only; reading taken: W is cut
+ * into 32 x 32 blocks (padding +0), each block gets one E8M0 scale from the amax of its
+ * 1024 elements by the same rule as a 1 x 32 block, and every element of the block is
+ * encoded with that scale in both packings.  So the row blob's scale of (row r, block kb)
+ * and the col blob's scale of (column k, block mb) are the scale of the 2-D block that
+ * holds them, and the two blobs dequantize to exact transposes of each other.
+ * -------------------------------------------------------------------------------------- */
+
+/* Scale bytes of the 2-D blocks of X[M,K]: s2d[ceil(M/32), Kp/32]. */
+static int block2d_scales(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* s2d) {
+    int64_t Kp = cdiv64(K, PAD) * PAD, KB = Kp / BLOCK, MB = cdiv64(M, BLOCK);
+    for (int64_t mb = 0; mb < MB; ++mb)
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            double amax = 0.0;
+            for (int64_t i = 0; i < BLOCK; ++i)
+                for (int64_t j = 0; j < BLOCK; ++j) {
+                    int64_t m = mb * BLOCK + i, k = kb * BLOCK + j;
+                    if (m >= M || k >= K) continue;
+                    double v = oracle_bf16_to_f64(x[m * ldx + k]);
+                    if (!isfinite(v)) return -1;
+                    if (fabs(v) > amax) amax = fabs(v);
+                }
+            s2d[mb * KB + kb] = oracle_e8m0_scale(amax);
+        }
+    return 0;
+}
+
+/* Row blob of X[M,K] with 2-D block scales; layout as oracle_quantize_row. */
+int oracle_quantize_row_2d(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, uint8_t* s) {
+    int64_t Kp = cdiv64(K, PAD) * PAD, KB = Kp / BLOCK, MB = cdiv64(M, BLOCK);
+    uint8_t* s2d = (uint8_t*)malloc((size_t)(MB * KB));
+    if (!s2d) return -2;
+    if (block2d_scales(x, M, K, ldx, s2d)) { free(s2d); return -1; }
+    for (int64_t r = 0; r < M; ++r)
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            uint8_t byte = s2d[(r / BLOCK) * KB + kb];
+            int e = (int)byte - 127;
+            for (int j = 0; j < BLOCK / 2; ++j) {
+                int64_t k0 = kb * BLOCK + 2 * j, k1 = k0 + 1;
+                double v0 = (k0 < K) ? oracle_bf16_to_f64(x[r * ldx + k0]) : 0.0;
+                double v1 = (k1 < K) ? oracle_bf16_to_f64(x[r * ldx + k1]) : 0.0;
+                uint8_t lo = oracle_e2m1_encode(ldexp(v0, -e));
+                uint8_t hi = oracle_e2m1_encode(ldexp(v1, -e));
+                q[r * (Kp / 2) + kb * (BLOCK / 2) + j] = (uint8_t)(lo | (hi << 4));
+            }
+            s[r * KB + kb] = byte;
+        }
+    free(s2d);
+    return 0;
+}
+
+/* Col blob of X[M,K] with 2-D block scales: the row blob of X^T, the 2-D blocks being the
+ * same; layout as oracle_quantize_col. */
+int oracle_quantize_col_2d(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, uint8_t* s) {
+    int64_t Kp = cdiv64(K, PAD) * PAD, KB = Kp / BLOCK;
+    int64_t Mp = cdiv64(M, PAD) * PAD, MBp = Mp / BLOCK, MB = cdiv64(M, BLOCK);
+    uint8_t* s2d = (uint8_t*)malloc((size_t)(MB * KB));
+    if (!s2d) return -2;
+    if (block2d_scales(x, M, K, ldx, s2d)) { free(s2d); return -1; }
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t mb = 0; mb < MBp; ++mb) {
+            uint8_t byte = (mb < MB) ? s2d[mb * KB + k / BLOCK] : 0;
+            int e = (int)byte - 127;
+            for (int j = 0; j < BLOCK / 2; ++j) {
+                int64_t m0 = mb * BLOCK + 2 * j, m1 = m0 + 1;
+                double v0 = (m0 < M) ? oracle_bf16_to_f64(x[m0 * ldx + k]) : 0.0;
+                double v1 = (m1 < M) ? oracle_bf16_to_f64(x[m1 * ldx + k]) : 0.0;
+                uint8_t lo = oracle_e2m1_encode(ldexp(v0, -e));
+                uint8_t hi = oracle_e2m1_encode(ldexp(v1, -e));
+                q[k * (Mp / 2) + mb * (BLOCK / 2) + j] = (uint8_t)(lo | (hi << 4));
+            }
+            s[k * MBp + mb] = byte;
+        }
+    free(s2d);
+    return 0;
 }

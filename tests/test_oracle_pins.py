@@ -585,3 +585,58 @@ def test_fp8_gemm_exact_on_tiny_inputs():
             exact = sum(Fraction(oracle.e5m2_decode(a[m, k])) * Fraction(oracle.e5m2_decode(b[n, k]))
                         for k in range(K)) * s
             assert abs(Fraction(c[m, n]) - exact) <= abs(exact) * Fraction(1, 2**50)
+
+
+# --- 2-D (32 x 32) block scales for weights --------------------------------------------
+
+def _weight_like(M, K, seed):
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal((M, K)) * 0.02 * np.ldexp(1.0, rng.integers(-3, 4, (M, 1)))
+    return oracle.round_to_bf16(v)
+
+
+@pytest.mark.parametrize("M,K", [(64, 128), (100, 200), (33, 40)])
+def test_2d_blocks_give_transposed_blobs(M, K):
+    # One scale per 32 x 32 block, shared by both packings: the col blob dequantizes to the
+    # exact transpose of the row blob, and its scale bytes are the row blob's, transposed.
+    xb = _weight_like(M, K, M + K)
+    rq, rs = oracle.quantize_row_2d(xb)
+    cq, cs = oracle.quantize_col_2d(xb)
+    dr = oracle.dequantize(rq, rs)[:, :K]
+    dc = oracle.dequantize(cq, cs)[:, :M]
+    assert np.array_equal(dr.T, dc)
+    for r in range(M):
+        for kb in range(oracle.padded(K) // 32):
+            for k in range(kb * 32, min(K, kb * 32 + 32)):
+                assert cs[k, r // 32] == rs[r, kb]
+
+
+def test_2d_block_scale_is_the_rule_over_1024_elements():
+    # Against the 1 x 32 rule: a 2-D block's scale is the 1-D rule applied to its largest
+    # element, i.e. the largest 1-D scale among its 32 rows (amax over a superset), and
+    # equals the 1-D scales where every row of the block has the same amax.
+    xb = _weight_like(96, 128, 7)
+    _, rs2 = oracle.quantize_row_2d(xb)
+    _, rs1 = oracle.quantize_row(xb)
+    for mb in range(3):
+        for kb in range(4):
+            blk1 = rs1[mb * 32:(mb + 1) * 32, kb]
+            assert np.all(rs2[mb * 32:(mb + 1) * 32, kb] == blk1.max())
+    # constant-magnitude blocks: the 2-D and 1-D scales agree
+    c = np.full((32, 32), 0x3FC0, np.uint16)   # 1.5 everywhere
+    assert np.array_equal(oracle.quantize_row_2d(c)[1], oracle.quantize_row(c)[1])
+
+
+def test_2d_blocks_hand_worked():
+    # A 32 x 32 block whose largest magnitude is 12 (scale 2^(3-2) = 2): 3 -> 1.5 (code 3),
+    # 12 -> 6 (code 7), -0.5 -> -0.25 which ties to -0 (code 0x8); the row whose own
+    # largest magnitude is 3 keeps the block's scale byte 128.
+    x = np.zeros((32, 32), np.uint16)
+    x[0, 0] = 0x4040          # 3.0
+    x[5, 7] = 0x4140          # 12.0
+    x[9, 2] = 0xBF00          # -0.5
+    rq, rs = oracle.quantize_row_2d(x)
+    assert np.all(rs[:, 0] == 128) and np.all(rs[:, 1:] == 0)
+    assert rq[0, 0] & 0xF == 3
+    assert (rq[5, 3] >> 4) == 7
+    assert rq[9, 1] & 0xF == 0x8
