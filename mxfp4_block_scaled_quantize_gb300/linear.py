@@ -1,14 +1,18 @@
 """The MXFP4 linear layer's data path, Y = X . W^T, as a sequence of C-ABI calls.
 
-Follows the dataflow of `MXFP4LinearFunction` in primus_turbo_mxfp4_local.py with every
-quantization recipe flag off:
+Follows the dataflow of `MXFP4LinearFunction` in primus_turbo_mxfp4_local.py:
   forward   dual-quantize X and W (row-only when no backward follows, the "row-only
-            packing" of Primus PR #1107), Y = X_row . W_row^T
-  backward  dual-quantize dY, dX = dY_row . (W_col)^T, dW = dY_col . (X_col)^T
-Only the column blobs of X and W need to live from forward to backward; bf16 X and W are
-not kept.  All buffers are allocated once (torch as the allocator) and reused, so a step
-is four launches on one stream: X and W quantized together, the forward GEMM, dY, and
-dgrad with wgrad in one GEMM launch.
+            packing" of Primus PR #1107), Y = X_row . W_row^T, with the layer's bias add
+            (`output + bias` of `_forward_impl`) fused into the GEMM when a bias is given
+  backward  dual-quantize dY (optionally with stochastic rounding, the gradient
+            quantizer's `use_sr`), dX = dY_row . (W_col)^T, dW = dY_col . (X_col)^T;
+            or, with backward="fp8", the pages' hybrid backward (tensorwise E5M2 of dY,
+            X, W and FP8 GEMMs)
+The other recipe flags (2-D weight blocks, Hadamard transform, shuffles) are off.  In the
+MXFP4 backward only the column blobs of X and W live from forward to backward; bf16 X
+and W are not kept.  All buffers are allocated once (torch as the allocator) and reused,
+so an MXFP4 step is four launches on one stream: X and W quantized together, the forward
+GEMM, dY, and dgrad with wgrad in one GEMM launch.
 """
 import torch
 
