@@ -1,15 +1,24 @@
-"""Benchmark of the GB300 MXFP4 linear hot path: one Flux-12B MLP up-projection training
-step (dual-quantize X, W, dY; fwd, dgrad and wgrad block-scaled GEMMs) per step.
+"""Benchmark of the GB300 MXFP4 linear hot path at Flux-12B shapes.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--cpu-baseline-seconds S]
+                    [--workload NAME] [--cpu-baseline-seconds S] [--no-extras]
+                    [--sr | --fp8-backward] [--bias]
 
-Prints one JSON line (rank 0).  `value` is the step's GEMM work (3 x 2MNK flops) divided
-by the device time of the whole step, quantizers included, summed over all ranks' steps;
-per-kernel times, the GEMM roofline and the dual-quantizer bandwidth come with it.
-Under torchrun each rank runs its own replica of the step on its own GPU (the path has
-no exchange step), so scaling is weak.  `--impl reference` times the CPU oracle on a
-bounded sample of the same workload instead.
+One step is one training step of every MXFP4 linear of the workload, in the order of a
+block's training step: each linear's forward (X and W quantized in one launch, then
+Y = X . W^T), then each linear's backward in reverse order (dY quantized, then dgrad and
+wgrad in one GEMM launch).  The default workload is Flux-12B's single-stream block:
+linear1 X[4608,3072] . W1[21504,3072]^T and linear2 H[4608,15360] . W2[3072,15360]^T,
+3.131 TFLOP per step.
+
+Prints one JSON line (rank 0).  `value` is the step's GEMM work divided by the device time
+of the whole step, quantizers included, summed over all ranks' steps.  With it: per-kernel
+medians and means, the GEMM roofline, the quantizer bandwidth, the same step replayed as a
+CUDA graph, an end-to-end step from pinned host buffers through the library's host-step
+entry point, and (N = 1, `extras`) the Flux QKV forward with row-only quantization and the
+quantizer bandwidth sweep.  Under torchrun each rank runs its own replica of the step on
+its own GPU (the path has no exchange step), so scaling is weak.  `--impl reference`
+times the CPU oracle on a bounded sample of the same workload instead.
 """
 import argparse
 import hashlib
@@ -25,13 +34,18 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MXFP4 GEMM TFLOPS + dual-quant GB/s at Flux-12B shapes; % of roofline"
-DEFAULT_WORKLOAD = "flux12b_mlp_up_train_step_4608x12288x3072"
+DEFAULT_WORKLOAD = "flux12b_single_block_linears_train"
 L2_FLUSH_BYTES = 256 << 20       # > 2x the 129 MB L2
 HEAD_START_CYCLES = 20_000_000   # ~10 ms of GPU sleep before the first timed step
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # dense FP4 / dense bf16 tensor rate (nominal)
 NOMINAL_FP8_OVER_BF16 = 4.5 / 2.25    # dense FP8 / dense bf16 tensor rate (nominal)
+SPEC_FP4_TFLOPS = 15000.0        # dense FP4 per GB300 GPU (GB300 NVL72: 1.08 EF / 72)
+SPEC_HBM_GBS = 8000.0            # HBM3e, nominal (~8 TB/s)
+MMA_MXF4_ISSUE_TFLOPS = 9690.0   # back-to-back kind::mxf4 M256 N256 K64 on all SMs (measured)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+DUAL_BYTES = 2 + 2 * (0.5 + 1 / 32)      # per element: bf16 read, two blobs written
+ROW_BYTES = 2 + 0.5 + 1 / 32
 
 
 def dist_env():
@@ -88,9 +102,9 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
-    the current kernel sources (else None)."""
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -98,7 +112,7 @@ def profiled_traffic(kernel):
     except (OSError, ValueError):
         return None
     ent = t.get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash(kernel):
+    if not ent or ent.get("source_hash") != kernel_source_hash(kernel) or ent.get("workload") != workload:
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -161,6 +175,32 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------------------
+# algorithmic work of each stage of a step
+# ---------------------------------------------------------------------------------------
+def op_work(name, lin):
+    """(flops, bytes) of one stage `name` of linear `lin`: GEMM stages count 2MNK flops per
+    GEMM with the logical K; quantizer stages count the bf16 read plus the codes and scale
+    bytes written, padding excluded."""
+    M, N, K = lin.M, lin.N, lin.K
+    kind = name.split(".", 1)[1]
+    return {
+        "quant_dual_XW": (0, (M * K + N * K) * DUAL_BYTES),
+        "quant_row_XW": (0, (M * K + N * K) * ROW_BYTES),
+        "quant_dual_dY": (0, M * N * DUAL_BYTES),
+        "quant_fp8_dY_X_W": (0, M * N * (2 + 2) + (M * K + N * K) * (2 + 1)),
+        "gemm_fwd": (2 * M * N * K, 0),
+        "gemm_dgrad_wgrad": (4 * M * N * K, 0),
+        "gemm_fp8_dgrad_wgrad": (4 * M * N * K, 0),
+    }[kind]
+
+
+def summarize(ms_list):
+    return {"median_us": round(statistics.median(ms_list) * 1e3, 2),
+            "mean_us": round(statistics.mean(ms_list) * 1e3, 2),
+            "min_us": round(min(ms_list) * 1e3, 2)}
+
+
+# ---------------------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------------------
 def run_ours(args, rank, world, local_rank):
@@ -168,7 +208,7 @@ def run_ours(args, rank, world, local_rank):
     import torch.distributed as dist
 
     from mxfp4_block_scaled_quantize_gb300 import abi, workloads
-    from mxfp4_block_scaled_quantize_gb300.linear import MXFP4Linear
+    from mxfp4_block_scaled_quantize_gb300.linear import MXFP4Block
     import __graft_entry__
 
     torch.cuda.set_device(local_rank)
@@ -180,18 +220,20 @@ def run_ours(args, rank, world, local_rank):
     abi.load()
 
     wl = workloads.WORKLOADS[args.workload]
-    lin = wl.linears[0]
-    M, N, K = lin.M, lin.N, lin.K
-    t = wl.tensors(0)
-    x, w = t["X"].to(dev), t["W"].to(dev)
-    dy = t["dY"].to(dev) if lin.train else None
-    fp8_bwd = bool(args.fp8_backward) and lin.train
+    lins = wl.linears
+    train = lins[0].train
+    fp8_bwd = bool(args.fp8_backward) and train
     if args.fp8_backward and args.sr:
         raise SystemExit("--sr is a mode of the MXFP4 backward, not of --fp8-backward")
-    layer = MXFP4Linear(M, N, K, train=lin.train, device=dev, backward="fp8" if fp8_bwd else "mxfp4")
-    bias = (workloads.normal((N,), 0.02, 977).to(dev) if args.bias else None)
+    host_t = [wl.tensors(i) for i in range(len(lins))]
+    inputs = [{k: v.to(dev) for k, v in t.items()} for t in host_t]
+    block = MXFP4Block([(l.name, l.M, l.N, l.K) for l in lins], train=train, device=dev,
+                       backward="fp8" if fp8_bwd else "mxfp4")
+    bias = ([workloads.normal((l.N,), 0.02, 977 + i).to(dev) for i, l in enumerate(lins)]
+            if args.bias else None)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_src = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    lin_of = {l.name: l for l in lins}
 
     def flush_l2():
         # Write a buffer larger than L2, then read another one: no input of the step is left
@@ -199,48 +241,35 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()
         flush_src.sum()
     stream = torch.cuda.current_stream(dev)
-    n_k = layer.launches_per_step
-    names = (["quant_row_XW", "gemm_fwd", "quant_fp8_dY_X_W", "gemm_fp8_dgrad_wgrad"] if fp8_bwd else
-             ["quant_dual_XW", "gemm_fwd", "quant_dual_dY", "gemm_dgrad_wgrad"]
-             if lin.train else ["quant_row_XW", "gemm_fwd"])
 
     def sr_seed(k):
         return (0x5EED0000 + k) if args.sr else None
 
-    def step_with_events(evs, k):
-        evs[0].record(stream)
-        layer.quantize_xw(x, w)
-        evs[1].record(stream)
-        layer.fwd_gemm(bias=bias)
-        evs[2].record(stream)
-        if lin.train:
-            if fp8_bwd:
-                layer.quantize_fp8_bwd(dy)
-            else:
-                layer.quantize_dy(dy, sr_seed=sr_seed(k))
-            evs[3].record(stream)
-            if fp8_bwd:
-                layer.fp8_bwd_gemms()
-            else:
-                layer.bwd_gemms()
-            evs[4].record(stream)
+    def ops(k):
+        return block.ops(inputs, bias, sr_seed(k))
+    names = [n for n, _, _ in ops(0)]
+    launches_per_step = sum(n for _, _, n in ops(0))
+
+    def run_step(k):
+        for _, fn, _ in ops(k):
+            fn()
 
     def barrier():
         if world > 1:
             dist.barrier()
-
-    for i in range(args.warmup):
-        flush_l2()
-        layer.step(x, w, dy, bias=bias, sr_seed=sr_seed(i))
-    torch.cuda.synchronize()
-    if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
-        raise RuntimeError("device error word set during warm-up")
 
     def head_start():
         # Keep the GPU busy (outside every timed interval) while the host queues the first
         # steps, so no step waits on the host's launch calls.
         if hasattr(torch.cuda, "_sleep"):
             torch.cuda._sleep(HEAD_START_CYCLES)
+
+    for i in range(args.warmup):
+        flush_l2()
+        run_step(i)
+    torch.cuda.synchronize()
+    if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
+        raise RuntimeError("device error word set during warm-up")
 
     sampler = ClockSampler(local_rank)
     if rank == 0:
@@ -256,19 +285,54 @@ def run_ours(args, rank, world, local_rank):
     for k in range(args.steps):
         flush_l2()
         step_events[k][0].record(stream)
-        layer.step(x, w, dy, bias=bias, sr_seed=sr_seed(k))
+        run_step(k)
         step_events[k][1].record(stream)
     torch.cuda.synchronize()
-    t_end = time.time()
     barrier()
-    # Per-kernel pass (same steps, an event between every two kernels, which serializes
+    # Per-kernel pass (same steps, an event between every two stages, which serializes
     # their launches): the kernel durations behind the roofline and bandwidth figures.
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     head_start()
     for k in range(args.steps):
         flush_l2()
-        step_with_events(events[k], k)
+        evs = events[k]
+        evs[0].record(stream)
+        for i, (_, fn, _) in enumerate(ops(k)):
+            fn()
+            evs[i + 1].record(stream)
     torch.cuda.synchronize()
+    # CUDA-graph pass: one step captured once and replayed, which takes the host's launch
+    # calls out of the picture (the same kernels and arguments; with --sr every replay uses
+    # the first step's seed).
+    graph = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            run_step(0)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            run_step(0)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            flush_l2()
+            g.replay()
+        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+        head_start()
+        for k in range(args.steps):
+            flush_l2()
+            gev[k][0].record(stream)
+            g.replay()
+            gev[k][1].record(stream)
+        torch.cuda.synchronize()
+        gms = [a.elapsed_time(b) for a, b in gev]
+        graph = {"ms_per_step_median": round(statistics.median(gms), 4),
+                 "ms_per_step_mean": round(statistics.mean(gms), 4)}
+    except Exception as e:   # reported, not hidden: the eager numbers stand on their own
+        graph = {"error": f"{type(e).__name__}: {e}"[:200]}
+        torch.cuda.synchronize()
     t_end2 = time.time()
     barrier()
     sampler.mark(t_start, t_end2)
@@ -280,74 +344,84 @@ def run_ours(args, rank, world, local_rank):
     step_ms = [ev[0].elapsed_time(ev[1]) for ev in step_events]
     total_ms = reduce_max_over_ranks(sum(step_ms), world, dev)
 
-    # ---- end to end: inputs from pinned host memory, results back to pinned host memory,
-    #      through the layer's host-buffer step (copies overlapped with the kernels)
-    hx, hw = t["X"].pin_memory(), t["W"].pin_memory()
-    hdy = t["dY"].pin_memory() if lin.train else None
-    outs = [layer.y] + ([layer.dx, layer.dw] if lin.train else [])
-    houts = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    houts += [None] * (3 - len(houts))
-    h2d = sum(a.numel() * a.element_size() for a in (hx, hw, hdy) if a is not None)
-    d2h = sum(o.numel() * o.element_size() for o in houts if o is not None)
+    # ---- end to end: inputs from pinned host memory, results back to pinned host memory
+    plain = not (fp8_bwd or args.sr or args.bias)
+    hin = [{k: v.pin_memory() for k, v in t.items()} for t in host_t]
+    houts = []
+    for L in block.layers:
+        outs = [L.y] + ([L.dx, L.dw] if train else [])
+        houts.append([torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs])
+    h2d = sum(v.numel() * v.element_size() for t in hin for v in t.values())
+    d2h = sum(o.numel() * o.element_size() for os_ in houts for o in os_)
+
+    def e2e_step():
+        if plain:
+            # the library's own host-buffer step (mxfp4_linear_step_host, one C-ABI call)
+            block.step_host(hin, houts)
+        else:
+            # the options are not in the host-step entry point: per layer, torch copies on
+            # copy streams around the layer's C-ABI calls
+            for L, t, o, i in zip(block.layers, hin, houts, range(len(lins))):
+                o3 = list(o) + [None] * (3 - len(o))
+                L.step_host(t["X"], t["W"], t.get("dY"), *o3, bias=bias[i] if bias else None,
+                            sr_seed=sr_seed(0))
+
     e2e_steps = max(3, min(args.steps, 20))
     for _ in range(2):
-        layer.step_host(hx, hw, hdy, *houts, bias=bias, sr_seed=sr_seed(0))
+        e2e_step()
     torch.cuda.synchronize()
     e_ms = []
     for _ in range(e2e_steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        layer.step_host(hx, hw, hdy, *houts, bias=bias, sr_seed=sr_seed(0))
+        e2e_step()
         e1.record(stream)
         e1.synchronize()
         e_ms.append(e0.elapsed_time(e1))
-    e2e_ms = reduce_max_over_ranks(statistics.mean(e_ms), world, dev)
+    e2e_ms = reduce_max_over_ranks(statistics.median(e_ms), world, dev)
+    if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
+        raise RuntimeError("device error word set during the end-to-end steps")
+
+    extras = run_extras(args, dev, flush_l2, head_start) if (rank == 0 and world == 1 and args.extras) else None
 
     if rank != 0:
         return None
 
     peaks = load_peaks()
     fp4_peak = peaks["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
-    gemm_idx = [i for i, n in enumerate(names) if n.startswith("gemm")]
-    quant_idx = [i for i, n in enumerate(names) if n.startswith("quant")]
-    # algorithmic flops of each GEMM launch: the forward GEMM, and dgrad + wgrad together
-    launch_flops = {"gemm_fwd": 2 * M * N * K, "gemm_dgrad_wgrad": 4 * M * N * K,
-                    "gemm_fp8_dgrad_wgrad": 4 * M * N * K}
-    if fp8_bwd:
-        # the FP8 backward GEMM launch dominates; its peak is the FP8 one
-        gemm_idx = [names.index("gemm_fp8_dgrad_wgrad")]
-        fp4_peak = peaks["bf16_tflops"] * NOMINAL_FP8_OVER_BF16
-    gemm_flops = sum(launch_flops[names[i]] for i in gemm_idx) / len(gemm_idx)   # per launch
-    gemm_ms = statistics.mean([v for i in gemm_idx for v in per_kernel[i]])      # per launch
-    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
-
-    # algorithmic bytes of each quantizer launch (padding excluded): bf16 read once, codes
-    # and scales written once
-    qbytes = {"quant_dual_XW": (M * K + N * K) * 3.0625, "quant_row_XW": (M * K + N * K) * 2.53125,
-              "quant_dual_dY": M * N * 3.0625,
-              "quant_fp8_dY_X_W": M * N * (2 + 2) + (M * K + N * K) * (2 + 1)}
+    gemm_peak = peaks["bf16_tflops"] * (NOMINAL_FP8_OVER_BF16 if fp8_bwd else NOMINAL_FP4_OVER_BF16)
     kern = {}
+    gemm_flops = gemm_ms = q_bytes = q_ms = 0.0
+    n_gemm = 0
     for i, n in enumerate(names):
+        flops, nbytes = op_work(n, lin_of[n.split(".")[0]])
+        ent = summarize(per_kernel[i])
         ms = statistics.mean(per_kernel[i])
-        ent = {"avg_us": round(ms * 1e3, 2), "min_us": round(min(per_kernel[i]) * 1e3, 2)}
-        if n.startswith("gemm"):
-            ent["tflops"] = round(launch_flops[n] / (ms * 1e-3) / 1e12, 1)
-            ent["frac_of_fp4_peak"] = round(ent["tflops"] / fp4_peak, 4)
+        if flops:
+            ent["tflops"] = round(flops / (ms * 1e-3) / 1e12, 1)
+            peak = gemm_peak if "fp8" in n else fp4_peak
+            ent["frac_of_peak"] = round(ent["tflops"] / peak, 4)
+            if "fp8" in n or not fp8_bwd:
+                gemm_flops += flops
+                gemm_ms += ms
+                n_gemm += 1
         else:
-            nbytes = qbytes[n]
             ent["gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
             ent["frac_of_hbm"] = round(ent["gbs"] / peaks["hbm_gbs"], 4)
+            q_bytes += nbytes
+            q_ms += ms
         kern[n] = ent
-    q_bytes = sum(qbytes[names[i]] for i in quant_idx)
-    q_ms = sum(statistics.mean(per_kernel[i]) for i in quant_idx)
+    gemm_tflops = gemm_flops / (gemm_ms * 1e-3) / 1e12
     quant_gbs = q_bytes / (q_ms * 1e-3) / 1e9
 
-    step_flops = lin.flops_step
+    step_flops = sum(l.flops_step for l in lins)
     value = whole_job_tflops(step_flops, args.steps, total_ms, world)
     e2e_value = whole_job_tflops(step_flops, 1, e2e_ms, world)
     gemm_kernel = ("gemm_fp8_pair_kernel" if fp8_bwd else
-                   "gemm_mxf4_pair_kernel" if M > 128 else "gemm_mxf4_kernel")
-    traffic = profiled_traffic(gemm_kernel)
+                   "gemm_mxf4_pair_kernel" if min(l.M for l in lins) > 128 else "gemm_mxf4_kernel")
+    traffic = profiled_traffic(gemm_kernel, args.workload)
+    mode = ("; backward fp8 (tensorwise E5M2 of dY, X, W; fp8 dgrad + wgrad)" if fp8_bwd else
+            "; dY stochastically rounded" if args.sr else "") + ("; bias fused" if args.bias else "")
 
     line = {
         "metric": METRIC,
@@ -357,58 +431,156 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(total_ms / args.steps, 4),
+        "ms_per_step_median": round(statistics.median(step_ms), 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "fp4_e2m1 (e8m0 block scales, fp32 accumulate, bf16 out)" + (
             "; backward fp8_e5m2 (tensorwise scales, fp32 accumulate)" if fp8_bwd else ""),
-        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(0,1e-3) grads)",
-        "config": {"workload": args.workload, "M": M, "N": N, "K": K,
-                   "step": ("row-quant X,W; fwd" + (" + bias" if args.bias else "") +
-                            "; fp8 tensorwise quant dY, X, W; fp8 dgrad; fp8 wgrad") if fp8_bwd else
-                           ("dual-quant X,W; fwd" + (" + bias" if args.bias else "") +
-                            "; dual-quant dY" + (" (stochastic rounding)" if args.sr else "") +
-                            "; dgrad; wgrad") if lin.train
-                   else "row-quant X,W; fwd",
+        "data": "synthetic (seeded N(0,1) / GELU-like activations, N(0,0.02) weights, N(0,1e-3) grads)",
+        "config": {"workload": args.workload,
+                   "linears": [{"name": l.name, "M": l.M, "N": l.N, "K": l.K} for l in lins],
+                   "gemm_tflop_per_step": round(step_flops / 1e12, 4),
+                   "step": ("forwards in order (quant X+W, fwd GEMM), backwards in reverse order "
+                            "(quant dY, dgrad+wgrad GEMM)" if train else "quant X+W (row-only), fwd GEMM") + mode,
                    "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then "
                          f"{L2_FLUSH_BYTES >> 20} MiB read)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "kernel": gemm_kernel,
-                     "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp4_peak, 4),
+                     "achieved": round(gemm_tflops, 1), "peak": round(gemm_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(gemm_tflops / gemm_peak, 4),
                      "traffic": traffic,
                      "peak_source": f"{peaks['source']} bf16 {peaks['bf16_tflops']} TFLOP/s x " + (
                          f"{NOMINAL_FP8_OVER_BF16:g} (nominal dense FP8/bf16 ratio)" if fp8_bwd else
                          f"{NOMINAL_FP4_OVER_BF16:g} (nominal dense FP4/bf16 ratio)"),
-                     "algorithmic_flops_per_launch": int(gemm_flops)},
+                     "frac_of_spec_15pf": None if fp8_bwd else round(gemm_tflops / SPEC_FP4_TFLOPS, 4),
+                     "frac_of_mxf4_issue_ceiling": None if fp8_bwd else round(gemm_tflops / MMA_MXF4_ISSUE_TFLOPS, 4),
+                     "launches_per_step": n_gemm,
+                     "algorithmic_flops_per_launch": int(gemm_flops / max(1, n_gemm))},
         "quant_roofline": {"bound": "hbm", "achieved": round(quant_gbs, 1),
                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
                            "frac": round(quant_gbs / peaks["hbm_gbs"], 4),
+                           "frac_of_spec_8tbs": round(quant_gbs / SPEC_HBM_GBS, 4),
                            "algorithmic_bytes_per_step": int(q_bytes), "peak_source": peaks["source"]},
         "kernels": kern,
+        "graph": graph,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": n_k * args.steps,
-        "kernel_times": "second pass over the same steps with an event between kernels",
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "path": "mxfp4_linear_step_host (one C-ABI call per step, pinned host buffers)" if plain
+                        else "per layer: torch copies on copy streams + the layer's C-ABI calls"},
+        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches_note": "library kernels in the timed step pass (L2 flushes are torch's)",
+        "kernel_times": "second pass over the same steps with an event between stages",
+        "extras": extras,
         "clocks": clocks,
         "device": torch.cuda.get_device_name(dev),
     }
     return line
 
 
+def run_extras(args, dev, flush_l2, head_start):
+    """Lines for the other Flux configs, timed the same way: the QKV projection forward with
+    row-only quantization (X[4608,3072], W[9216,3072]) and the quantizer bandwidth sweep
+    (dual quantization of M x K bf16 tensors for every M in {4608, 18432, 4600} and K in
+    {3072, 12288, 15360}; the largest, 18432 x 15360, moves 867 MB)."""
+    import torch
+
+    from mxfp4_block_scaled_quantize_gb300 import abi, workloads
+    from mxfp4_block_scaled_quantize_gb300.linear import MXFP4Block
+
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    n = max(5, min(args.steps, 50))
+
+    # QKV forward (row-only X, W, then the forward GEMM)
+    wl = workloads.FLUX_QKV_FWD
+    lin = wl.linears[0]
+    t = {k: v.to(dev) for k, v in wl.tensors(0).items()}
+    blk = MXFP4Block([(lin.name, lin.M, lin.N, lin.K)], train=False, device=dev)
+    ops = blk.ops([t])
+    for _ in range(3):
+        for _, fn, _ in ops:
+            fn()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(ops) + 1)] for _ in range(n)]
+    head_start()
+    for k in range(n):
+        flush_l2()
+        evs[k][0].record(stream)
+        for i, (_, fn, _) in enumerate(ops):
+            fn()
+            evs[k][i + 1].record(stream)
+    torch.cuda.synchronize()
+    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    g_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    qb = (lin.M * lin.K + lin.N * lin.K) * ROW_BYTES
+    out[wl.name] = {
+        "quant_row_XW": dict(summarize(q_ms), gbs=round(qb / (statistics.mean(q_ms) * 1e-3) / 1e9, 1),
+                             frac_of_hbm=round(qb / (statistics.mean(q_ms) * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)),
+        "gemm_fwd": dict(summarize(g_ms), tflops=round(lin.flops_fwd / (statistics.mean(g_ms) * 1e-3) / 1e12, 1)),
+        "step_tflops": round(lin.flops_fwd / ((statistics.mean(q_ms) + statistics.mean(g_ms)) * 1e-3) / 1e12, 1),
+    }
+    del blk, t
+
+    # quantizer sweep: dual quantization, inputs drawn on the device from a seed (the values
+    # do not change the work; the bit-exact sweep lives in the parity tests)
+    sweep = {}
+    gen = torch.Generator(device=dev)
+    for M in workloads.SWEEP_M:
+        for K in workloads.SWEEP_K:
+            gen.manual_seed(M * 100003 + K)
+            x = torch.randn((M, K), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+            outs = abi.quantize(x, dual=True)
+            ms = []
+            for k in range(n + 3):
+                flush_l2()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                abi.mxfp4_quantize_dual(x, M, K, x.stride(0), *outs, abi.MXFP4_SCALE_TC)
+                e1.record(stream)
+                if k >= 3:
+                    ms.append((e0, e1))
+            torch.cuda.synchronize()
+            ms = [a.elapsed_time(b) for a, b in ms]
+            nbytes = M * K * DUAL_BYTES
+            gbs = nbytes / (statistics.median(ms) * 1e-3) / 1e9
+            sweep[f"{M}x{K}"] = {"median_us": round(statistics.median(ms) * 1e3, 2), "mb": round(nbytes / 1e6, 1),
+                                 "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                                 "frac_of_spec_8tbs": round(gbs / SPEC_HBM_GBS, 4)}
+            del x, outs
+    out["quant_dual_sweep"] = sweep
+    if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
+        raise RuntimeError("device error word set during the extra lines")
+    return out
+
+
 # ---------------------------------------------------------------------------------------
 # the CPU oracle on a bounded sample (cpu_baseline, and the reference arm)
 # ---------------------------------------------------------------------------------------
+_SAMPLE_BITS = {}
+
+
+def _sample_bits(workload_name):
+    """The first 512 rows of every tensor of the workload as bf16 bits (drawn once)."""
+    if workload_name not in _SAMPLE_BITS:
+        from mxfp4_block_scaled_quantize_gb300 import workloads
+        wl = workloads.WORKLOADS[workload_name]
+        _SAMPLE_BITS[workload_name] = [
+            {k: workloads.bf16_bits(v[:512]) for k, v in wl.tensors(i).items()}
+            for i in range(len(wl.linears))]
+    return _SAMPLE_BITS[workload_name]
+
+
 def oracle_sample(workload_name, seconds, fp8_backward=False, threads=1):
     """Times the oracle on slices of the workload and extrapolates one full step.
 
     Sample: the oracle's quantizers (dual, or row-only; with fp8_backward, row-only MX for
-    X and W plus tensorwise E5M2 of dY, X and W) on 128-row slabs of X, W and dY, and its
-    fp64 GEMM on 8-row blocks of output against 512 columns; each part runs for about
-    seconds/2 of wall time on `threads` host threads at once (the oracle's C functions
+    X and W plus tensorwise E5M2 of dY, X and W) on 128-row slabs of each linear's X, W and
+    dY, and its fp64 GEMM on 8-row blocks of output against 512 columns; each part runs for
+    about seconds/2 of wall time on `threads` host threads at once (the oracle's C functions
     release the GIL, so the threads run in parallel; each thread takes its own slabs and
     blocks).  Step time = wall time per quantized element x all quantized elements + wall
-    time per MAC x all MACs of the step's GEMMs.
+    time per MAC x all MACs of the step's GEMMs, summed over the linears.
     """
     import concurrent.futures
     import numpy as np
@@ -417,25 +589,27 @@ def oracle_sample(workload_name, seconds, fp8_backward=False, threads=1):
     from mxfp4_block_scaled_quantize_gb300 import workloads
 
     wl = workloads.WORKLOADS[workload_name]
-    lin = wl.linears[0]
-    M, N, K = lin.M, lin.N, lin.K
-    t = wl.tensors(0)
-    bits = {k: workloads.bf16_bits(v) for k, v in t.items()}
-    fp8 = fp8_backward and lin.train
-    quant = oracle.quantize_dual if (lin.train and not fp8) else oracle.quantize_row
+    lins = wl.linears
+    train = lins[0].train
+    fp8 = fp8_backward and train
+    quant = oracle.quantize_dual if (train and not fp8) else oracle.quantize_row
     threads = max(1, int(threads))
+    bits = _sample_bits(workload_name)
 
-    def slab(k, w):
-        rows = bits[k].shape[0]
+    def slab(li, k, w):
+        b = bits[li][k]
+        rows = b.shape[0]
         r0 = (128 * w) % max(1, rows - 127)
-        return np.ascontiguousarray(bits[k][r0:r0 + 128])
+        return np.ascontiguousarray(b[r0:r0 + 128])
+
+    per_elem_bytes = ROW_BYTES if quant is oracle.quantize_row else DUAL_BYTES
 
     def quant_worker(w):
-        slabs = {k: slab(k, w) for k in bits}
+        slabs = [(k, slab(li, k, w)) for li in range(len(lins)) for k in bits[li]]
         elems = 0
         t0 = time.perf_counter()
         while time.perf_counter() - t0 < seconds / 2:
-            for k, sl in slabs.items():
+            for k, sl in slabs:
                 if fp8:   # row-only MX for X and W, tensorwise E5M2 for all three
                     if k != "dY":
                         quant(sl)
@@ -445,11 +619,12 @@ def oracle_sample(workload_name, seconds, fp8_backward=False, threads=1):
                 elems += sl.size
         return elems
 
-    wq, ws = oracle.quantize_row(np.ascontiguousarray(bits["W"][:512]))
+    wq, ws = oracle.quantize_row(bits[0]["W"])
     b = oracle.dequantize(wq, ws)
+    kp = b.shape[1]
 
     def gemm_worker(w):
-        xq, xs = oracle.quantize_row(slab("X", w)[:8])
+        xq, xs = oracle.quantize_row(slab(0, "X", w)[:8])
         a = oracle.dequantize(xq, xs)
         macs = 0
         t0 = time.perf_counter()
@@ -465,19 +640,24 @@ def oracle_sample(workload_name, seconds, fp8_backward=False, threads=1):
         t0 = time.perf_counter()
         g_macs = sum(ex.map(gemm_worker, range(threads)))
         g_wall = time.perf_counter() - t0
-    total_q = M * K + N * K + (M * N if lin.train else 0)
-    if fp8:
-        total_q = 2 * (M * K + N * K) + M * N
-    total_macs = M * N * K * (3 if lin.train else 1)
+    total_q = total_macs = 0
+    for l in lins:
+        if fp8:
+            total_q += 2 * (l.M * l.K + l.N * l.K) + l.M * l.N
+        else:
+            total_q += l.M * l.K + l.N * l.K + (l.M * l.N if train else 0)
+        total_macs += l.M * l.N * l.K * (3 if train else 1)
     step_s = q_wall / q_elems * total_q + g_wall / g_macs * total_macs
-    kind = "row-only MX + tensorwise E5M2" if fp8 else "dual" if lin.train else "row-only"
+    kind = "row-only MX + tensorwise E5M2" if fp8 else "dual" if train else "row-only"
     return {
         "step_seconds": step_s,
-        "value": lin.flops_step / step_s / 1e12,
-        "sample": (f"oracle {kind} quantizer on 128-row slabs of X, W{', dY' if lin.train else ''} "
-                   f"({int(q_elems)} elements) and fp64 GEMM on 8x512 output blocks at "
-                   f"K={oracle.padded(K)} ({int(g_macs)} MACs), on {threads} host thread(s); one "
-                   f"full step extrapolated per element / per MAC of wall time"),
+        "value": sum(l.flops_step for l in lins) / step_s / 1e12,
+        "quant_gbs": None if fp8 else q_elems * per_elem_bytes / q_wall / 1e9,
+        "gemm_gflops": 2 * g_macs / g_wall / 1e9,
+        "sample": (f"oracle {kind} quantizer on 128-row slabs of every linear's X, W"
+                   f"{', dY' if train else ''} ({int(q_elems)} elements) and fp64 GEMM on 8x512 "
+                   f"output blocks at K={kp} ({int(g_macs)} MACs), on {threads} host thread(s); "
+                   f"one full step extrapolated per element / per MAC of wall time"),
         "cores": threads,
         "kind": "oracle",
     }
@@ -503,7 +683,7 @@ def run_reference(args, rank, world):
     step_s = statistics.mean(v["step_seconds"] for v in vals)
     value = vals[0]["value"] if len(vals) == 1 else statistics.mean(v["value"] for v in vals)
     from mxfp4_block_scaled_quantize_gb300 import workloads
-    lin = workloads.WORKLOADS[args.workload].linears[0]
+    lins = workloads.WORKLOADS[args.workload].linears
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -518,10 +698,12 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "M": lin.M, "N": lin.N, "K": lin.K,
+        "config": {"workload": args.workload,
+                   "linears": [{"name": l.name, "M": l.M, "N": l.N, "K": l.K} for l in lins],
                    "parallelism": "host cores of rank 0"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": vals[0]["sample"]},
+                         "sample": vals[0]["sample"],
+                         "quant_gbs": vals[0]["quant_gbs"], "gemm_gflops": vals[0]["gemm_gflops"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -529,11 +711,13 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="skip the QKV-forward and quantizer-sweep lines")
     ap.add_argument("--sr", action="store_true",
                     help="dY is quantized with stochastic rounding (the gradient quantizer's "
                          "`use_sr`), a new Philox seed every step")
@@ -567,7 +751,10 @@ def main():
         one = oracle_sample(args.workload, args.cpu_baseline_seconds / 2, args.fp8_backward, 1)
         line["cpu_baseline"] = {"value": base["value"], "unit": "TFLOP/s", "cores": base["cores"],
                                 "kind": "oracle", "sample": base["sample"],
-                                "single_core_value": one["value"]}
+                                "quant_gbs": base["quant_gbs"], "gemm_gflops": base["gemm_gflops"],
+                                "single_core_value": one["value"],
+                                "single_core_quant_gbs": one["quant_gbs"],
+                                "single_core_gemm_gflops": one["gemm_gflops"]}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

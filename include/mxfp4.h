@@ -63,7 +63,8 @@ typedef enum {
     MXFP4_ERR_MISALIGNED = 2,         /* a pointer or pitch breaks the 16-byte rule       */
     MXFP4_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3    */
     MXFP4_ERR_CUDA = 4,               /* a CUDA runtime/driver call or a launch failed    */
-    MXFP4_ERR_TIMEOUT = 5             /* a kernel's bounded wait ran out (device word)    */
+    MXFP4_ERR_TIMEOUT = 5,            /* a kernel's bounded wait ran out (device word)    */
+    MXFP4_ERR_NONFINITE = 6           /* a tensorwise FP8 amax was NaN or inf (device word) */
 } mxfp4_status;
 
 typedef enum { MXFP4_SCALE_PLAIN = 0, MXFP4_SCALE_TC = 1 } mxfp4_scale_layout;
@@ -211,7 +212,10 @@ mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4
  *              least one of q_row / q_col; both 16-byte aligned
  *   amax, scale_inv   out, one fp32 each in device memory (4-byte aligned); the GEMMs
  *              read scale_inv from there, so no host synchronization is needed.
- * Three launches on `stream`: *amax zeroed, an amax pass, the conversion.  M, K >= 1. */
+ * Three launches on `stream`: *amax zeroed, an amax pass, the conversion.  M, K >= 1.
+ * Inputs must be finite: a NaN or infinity makes amax non-finite, the codes and scale_inv
+ * of that tensor are then meaningless, and the conversion records it in the device error
+ * word (mxfp4_last_device_error returns MXFP4_ERR_NONFINITE). */
 mxfp4_status mxfp4_fp8_quantize_tw(const void* x, int64_t M, int64_t K, int64_t ldx,
                                    void* q_row, void* q_col, float* amax, float* scale_inv,
                                    mxfp4_stream_t stream);
@@ -268,9 +272,53 @@ typedef struct {
 mxfp4_status mxfp4_fp8_gemm_batch(int32_t count, const mxfp4_fp8_gemm_task* tasks,
                                   mxfp4_stream_t stream);
 
+/* ---- a step from host memory to host memory -------------------------------------------
+ * The data path of `MXFP4LinearFunction` (primus_turbo_mxfp4_local.py) for linears whose
+ * bf16 inputs and results live in host memory: per linear, forward = dual (train) or
+ * row-only quantization of X and W and Y = X . W^T; backward = dual quantization of dY,
+ * dX = dY . W and dW = dY^T . X.  The forwards run in task order and the backwards in
+ * reverse task order, the order of a block's backward pass (Flux-12B's single-stream block:
+ * linear1 then linear2 forward, linear2 then linear1 backward). */
+typedef struct {
+    const void* x;     /* host bf16 X[M,K], dense rows of K elements                     */
+    const void* w;     /* host bf16 W[N,K], dense                                        */
+    const void* dy;    /* host bf16 dY[M,N], dense (train); ignored otherwise            */
+    void* y;           /* host out: Y[M,N] in out_dtype, dense                           */
+    void* dx;          /* host out: dX[M,K] in out_dtype (train)                         */
+    void* dw;          /* host out: dW[N,K] in out_dtype (train)                         */
+    int64_t M;
+    int64_t N;
+    int64_t K;
+    int32_t train;     /* 1: forward and backward; 0: forward only (row-only quantizer)   */
+    mxfp4_out_dtype out_dtype;
+} mxfp4_linear_host_task;
+
+/* Bytes of device workspace mxfp4_linear_step_host needs for these tasks (the device
+ * copies of the inputs, every blob, and the device results).  count in 1..MXFP4_MAX_BATCH. */
+mxfp4_status mxfp4_linear_workspace_bytes(int32_t count, const mxfp4_linear_host_task* tasks,
+                                          size_t* bytes);
+
+/* Enqueues one step of `count` linears: host-to-device copies of every input, the
+ * library's quantizer and GEMM kernels, and device-to-host copies of every result.
+ *   workspace        caller-owned device memory of at least mxfp4_linear_workspace_bytes
+ *                    (256-byte aligned); its contents are scratch between calls
+ *   stream           the kernels run on it; the copies run on two streams the library
+ *                    creates once per device (never freed), ordered against `stream` with
+ *                    events, so copies overlap the kernels of other linears and the
+ *                    quantizer of each linear waits only for its own inputs.  When the call
+ *                    returns, `stream` is ordered after every copy: synchronizing it makes
+ *                    the results visible in host memory.
+ * Host buffers should be pinned (page-locked) for the copies to be asynchronous.  All
+ * arguments are checked before anything is enqueued; a CUDA failure after that returns
+ * MXFP4_ERR_CUDA and may leave part of the step enqueued.  Calls from several host threads
+ * are serialized by the library (they share the copy streams). */
+mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task* tasks,
+                                    void* workspace, size_t workspace_bytes, mxfp4_stream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the device error word of the current
  * device: MXFP4_ERR_TIMEOUT if a bounded wait in any kernel of this library ran out
- * since the last call, MXFP4_ERR_CUDA if the synchronization itself failed, else OK. */
+ * since the last call, else MXFP4_ERR_NONFINITE if a tensorwise FP8 quantization met a
+ * non-finite amax; MXFP4_ERR_CUDA if the synchronization itself failed; else OK. */
 mxfp4_status mxfp4_last_device_error(mxfp4_stream_t stream);
 
 /* Diagnostic for the bounded-wait machinery: launches one warp that waits on a barrier

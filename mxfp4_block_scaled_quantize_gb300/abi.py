@@ -18,6 +18,7 @@ MXFP4_ERR_MISALIGNED = 2
 MXFP4_ERR_UNSUPPORTED_DEVICE = 3
 MXFP4_ERR_CUDA = 4
 MXFP4_ERR_TIMEOUT = 5
+MXFP4_ERR_NONFINITE = 6
 
 MXFP4_SCALE_PLAIN = 0
 MXFP4_SCALE_TC = 1
@@ -57,6 +58,14 @@ class Fp8GemmTask(ctypes.Structure):
                 ("out_dtype", ctypes.c_int)]
 
 
+class LinearHostTask(ctypes.Structure):
+    """mxfp4_linear_host_task of include/mxfp4.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("w", ctypes.c_void_p), ("dy", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("dx", ctypes.c_void_p), ("dw", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("train", ctypes.c_int32), ("out_dtype", ctypes.c_int)]
+
+
 EXPORTED = (
     "mxfp4_quantize_sizes",
     "mxfp4_quantize",
@@ -70,6 +79,8 @@ EXPORTED = (
     "mxfp4_fp8_quantize_tw_batch",
     "mxfp4_fp8_gemm",
     "mxfp4_fp8_gemm_batch",
+    "mxfp4_linear_workspace_bytes",
+    "mxfp4_linear_step_host",
     "mxfp4_last_device_error",
     "mxfp4_selftest_bounded_wait",
     "mxfp4_status_string",
@@ -109,6 +120,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_fp8_quantize_tw_batch.argtypes = [i32, ctypes.POINTER(Fp8QuantizeTask), vp]
     lib.mxfp4_fp8_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_fp8_gemm_batch.argtypes = [i32, ctypes.POINTER(Fp8GemmTask), vp]
+    lib.mxfp4_linear_workspace_bytes.argtypes = [i32, ctypes.POINTER(LinearHostTask),
+                                                 ctypes.POINTER(ctypes.c_size_t)]
+    lib.mxfp4_linear_step_host.argtypes = [i32, ctypes.POINTER(LinearHostTask), vp, ctypes.c_size_t, vp]
     lib.mxfp4_last_device_error.argtypes = [vp]
     lib.mxfp4_selftest_bounded_wait.argtypes = [i64, vp]
     lib.mxfp4_status_string.argtypes = [i32]
@@ -235,8 +249,31 @@ def mxfp4_fp8_gemm_batch(tasks, stream=None) -> None:
     _check(load().mxfp4_fp8_gemm_batch(len(tasks), arr, _stream(stream)), "mxfp4_fp8_gemm_batch")
 
 
+def _host_tasks(tasks):
+    """tasks: sequence of (x, w, dy, y, dx, dw, M, N, K, train, out_dtype) with host
+    buffers (tensors or addresses; dy, dx, dw may be None when train is 0)."""
+    arr = (LinearHostTask * max(1, len(tasks)))()
+    for i, (x, w, dy, y, dx, dw, M, N, K, train, od) in enumerate(tasks):
+        arr[i] = LinearHostTask(_ptr(x), _ptr(w), _ptr(dy), _ptr(y), _ptr(dx), _ptr(dw), M, N, K,
+                                int(bool(train)), od)
+    return arr
+
+
+def mxfp4_linear_workspace_bytes(tasks) -> int:
+    n = ctypes.c_size_t()
+    _check(load().mxfp4_linear_workspace_bytes(len(tasks), _host_tasks(tasks), ctypes.byref(n)),
+           "mxfp4_linear_workspace_bytes")
+    return n.value
+
+
+def mxfp4_linear_step_host(tasks, workspace, workspace_bytes: int, stream=None) -> None:
+    _check(load().mxfp4_linear_step_host(len(tasks), _host_tasks(tasks), _ptr(workspace),
+                                         workspace_bytes, _stream(stream)), "mxfp4_linear_step_host")
+
+
 def mxfp4_last_device_error(stream=None) -> int:
-    """Returns the status (does not raise): MXFP4_ERR_TIMEOUT if a bounded wait ran out."""
+    """Returns the status (does not raise): MXFP4_ERR_TIMEOUT if a bounded wait ran out,
+    MXFP4_ERR_NONFINITE if a tensorwise FP8 quantization met a non-finite input."""
     return int(load().mxfp4_last_device_error(_stream(stream)))
 
 

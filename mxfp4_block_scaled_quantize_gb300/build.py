@@ -15,7 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmxfp4_gb300.so")
-SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_pair.cu", "quantize_fp8.cu", "gemm_fp8.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemm.cu", "gemm_pair.cu", "quantize_fp8.cu", "gemm_fp8.cu",
+           "host_step.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -390,25 +390,32 @@ mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     // Problems of more than one 128-row tile share one CTA-pair launch; the others run on
-    // the one-CTA kernel, one launch each.
+    // the one-CTA kernel, one launch each.  Every task's arguments and tensor maps are
+    // prepared before the first launch, so a failing task leaves nothing enqueued.
     const int max_clusters = mxfp4::gemm_pair_max_clusters();
     mxfp4::GemmPairBatch b;
     std::memset(&b, 0, sizeof(b));
+    struct Single {
+        mxfp4::GemmArgs g;
+        CUtensorMap amap, bmap, cmap;
+    };
+    Single singles[MXFP4_MAX_BATCH];
+    int n_single = 0;
     for (int j = 0; j < count; ++j) {
         const mxfp4_gemm_task& t = tasks[j];
         if (t.M > mxfp4::kGemmBM && max_clusters > 0) {
             st = gemm_fill_pair(t, dev, &b);
         } else {
-            mxfp4::GemmArgs g;
-            CUtensorMap amap, bmap, cmap;
-            st = gemm_fill(t, dev, &g, &amap, &bmap, &cmap, mxfp4::kGemmBN);
-            if (st == MXFP4_OK) {
-                const int64_t tiles = static_cast<int64_t>(g.tiles_m) * g.tiles_n;
-                const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
-                st = mxfp4::launch_gemm(amap, bmap, cmap, g, grid, s) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
-            }
+            Single& o = singles[n_single++];
+            st = gemm_fill(t, dev, &o.g, &o.amap, &o.bmap, &o.cmap, mxfp4::kGemmBN);
         }
         if (st != MXFP4_OK) return st;
+    }
+    for (int i = 0; i < n_single; ++i) {
+        const Single& o = singles[i];
+        const int64_t tiles = static_cast<int64_t>(o.g.tiles_m) * o.g.tiles_n;
+        const int grid = static_cast<int>(tiles < dev->sms ? tiles : dev->sms);
+        if (mxfp4::launch_gemm(o.amap, o.bmap, o.cmap, o.g, grid, s) != cudaSuccess) return MXFP4_ERR_CUDA;
     }
     if (b.count == 0) return MXFP4_OK;
     const int64_t pair_tiles = b.tile_end[b.count - 1];
@@ -446,6 +453,7 @@ mxfp4_status mxfp4_fp8_quantize_tw_batch(int32_t count, const mxfp4_fp8_quantize
         b.tile_end[j] = tiles;
     }
     b.count = count;
+    b.err = dev->err;
     return mxfp4::launch_fp8_quantize(b, dev->sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MXFP4_OK
                : MXFP4_ERR_CUDA;
@@ -498,7 +506,7 @@ mxfp4_status mxfp4_last_device_error(mxfp4_stream_t stream) {
     if (word != 0) {
         const uint32_t zero = 0;
         if (cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MXFP4_ERR_CUDA;
-        return MXFP4_ERR_TIMEOUT;
+        return (word & mxfp4::kErrWaitBits) ? MXFP4_ERR_TIMEOUT : MXFP4_ERR_NONFINITE;
     }
     return MXFP4_OK;
 }
@@ -523,6 +531,8 @@ const char* mxfp4_status_string(mxfp4_status status) {
             return "MXFP4_ERR_UNSUPPORTED_DEVICE: the current device is not compute capability 10.3 (sm_103)";
         case MXFP4_ERR_CUDA: return "MXFP4_ERR_CUDA: a CUDA call or kernel launch failed";
         case MXFP4_ERR_TIMEOUT: return "MXFP4_ERR_TIMEOUT: a kernel's bounded wait ran out";
+        case MXFP4_ERR_NONFINITE:
+            return "MXFP4_ERR_NONFINITE: a tensorwise FP8 quantization met a NaN or infinite input";
     }
     return "MXFP4: unknown status";
 }

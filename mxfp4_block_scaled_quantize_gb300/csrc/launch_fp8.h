@@ -31,6 +31,7 @@ struct Fp8QuantBatch {
     int64_t row_end[kMaxFp8Tasks];
     int64_t tile_end[kMaxFp8Tasks];
     int32_t count;
+    uint32_t* err;       // device error word (non-finite amax)
 };
 
 cudaError_t launch_fp8_quantize(const Fp8QuantBatch& b, int sms, cudaStream_t stream);

@@ -21,7 +21,9 @@ enum : uint32_t {
     kErrGemmEpilogue = 1u << 4,
     kErrGemmDrain = 1u << 5,
     kErrSelftest = 1u << 6,
+    kErrNonFinite = 1u << 7,   // not a wait: a tensorwise FP8 amax was NaN or inf
 };
+constexpr uint32_t kErrWaitBits = kErrNonFinite - 1;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -20,6 +20,7 @@
 #include <cstdint>
 
 #include "launch_fp8.h"
+#include "ptx.cuh"
 
 namespace mxfp4 {
 namespace {
@@ -120,6 +121,8 @@ __global__ void __launch_bounds__(kFThreads) fp8_quantize_kernel(const __grid_co
     __shared__ __align__(16) uint8_t tile[kFt][kFt + 16];
     if (blockIdx.x == 0 && static_cast<int>(threadIdx.x) < B.count) {
         const Fp8QuantArgs& a = B.t[threadIdx.x];
+        // amax is the fp32 pattern of a bf16 magnitude: NaN and inf sit at and above 0x7F800000
+        if (*reinterpret_cast<const uint32_t*>(a.amax) >= 0x7F800000u) atomicOr(B.err, kErrNonFinite);
         *a.scale_inv = __fdiv_rn(1.0f, tensor_scale(*a.amax));
     }
     const int t = threadIdx.x;

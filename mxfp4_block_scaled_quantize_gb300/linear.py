@@ -221,3 +221,72 @@ class MXFP4Linear:
         if self.fp8_backward:
             return 2 + 3 + 1   # X+W, fwd; FP8 quantization of dY, X, W (zero, amax, convert); the GEMMs
         return 4 if self.train else 2
+
+
+class MXFP4Block:
+    """The MXFP4 linears of one transformer block, stepped in the order of a training step:
+    every forward in order, then every backward in reverse order (Flux-12B's single-stream
+    block: linear1 and linear2 forward, linear2 and linear1 backward; the pages' Flux-12B
+    campaign of Primus PR #1107 runs its MXFP4 linears this way, block after block).  In
+    this data path each linear's inputs are given, so the linears share no buffer.
+
+    shapes: sequence of (name, M, N, K).  Options as MXFP4Linear."""
+
+    def __init__(self, shapes, train: bool = True, device="cuda", out_dtype=torch.bfloat16,
+                 backward: str = "mxfp4"):
+        self.names = [s[0] for s in shapes]
+        self.train = train
+        self.layers = [MXFP4Linear(M, N, K, train=train, device=device, out_dtype=out_dtype,
+                                   backward=backward) for _, M, N, K in shapes]
+        self._ws = None
+
+    def ops(self, inputs, bias=None, sr_seed=None):
+        """One step as a list of (name, callable, launches): each callable enqueues one
+        stage of the step on the current stream.  inputs: per linear a dict with "X", "W"
+        (and "dY" when training) CUDA bf16 tensors; bias: per linear a bf16 vector or None."""
+        bias = bias or [None] * len(self.layers)
+        out = []
+        for name, L, t, b in zip(self.names, self.layers, inputs, bias):
+            kind = "row" if (not self.train or L.fp8_backward) else "dual"
+            out.append((f"{name}.quant_{kind}_XW", lambda L=L, t=t: L.quantize_xw(t["X"], t["W"]), 1))
+            out.append((f"{name}.gemm_fwd", lambda L=L, b=b: L.fwd_gemm(bias=b), 1))
+        if self.train:
+            for name, L, t in reversed(list(zip(self.names, self.layers, inputs))):
+                if L.fp8_backward:
+                    out.append((f"{name}.quant_fp8_dY_X_W", lambda L=L, t=t: L.quantize_fp8_bwd(t["dY"]), 3))
+                    out.append((f"{name}.gemm_fp8_dgrad_wgrad", lambda L=L: L.fp8_bwd_gemms(), 1))
+                else:
+                    out.append((f"{name}.quant_dual_dY",
+                                lambda L=L, t=t: L.quantize_dy(t["dY"], sr_seed=sr_seed), 1))
+                    out.append((f"{name}.gemm_dgrad_wgrad", lambda L=L: L.bwd_gemms(), 1))
+        return out
+
+    def step(self, inputs, bias=None, sr_seed=None):
+        for _, fn, _ in self.ops(inputs, bias, sr_seed):
+            fn()
+        return [(L.y, L.dx, L.dw) if self.train else (L.y,) for L in self.layers]
+
+    def host_tasks(self, host_inputs, host_outputs):
+        code = abi.MXFP4_OUT_F32 if self.layers[0].y.dtype == torch.float32 else abi.MXFP4_OUT_BF16
+        tasks = []
+        for L, t, o in zip(self.layers, host_inputs, host_outputs):
+            tasks.append((t["X"], t["W"], t.get("dY"), o[0], o[1] if self.train else None,
+                          o[2] if self.train else None, L.M, L.N, L.K, self.train, code))
+        return tasks
+
+    def step_host(self, host_inputs, host_outputs, stream=None):
+        """One step from host buffers to host buffers through the library's own host step
+        (mxfp4_linear_step_host): the copies run on the library's copy streams, overlapped
+        with the kernels.  host_outputs: per linear (Y, dX, dW) (or (Y,) forward-only) host
+        tensors, pinned for asynchrony.  Returns when the step is enqueued; the current
+        stream is ordered after every copy."""
+        assert not any(L.fp8_backward for L in self.layers), "the host step runs the MXFP4 backward"
+        tasks = self.host_tasks(host_inputs, host_outputs)
+        need = abi.mxfp4_linear_workspace_bytes(tasks)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=self.layers[0].y.device)
+        abi.mxfp4_linear_step_host(tasks, self._ws, self._ws.numel(), stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        return sum(L.launches_per_step for L in self.layers)

@@ -7,6 +7,9 @@ The comparisons follow the accuracy contract of the library:
     or, for outputs that nearly cancel (where the fp32 accumulation the hardware performs
     is itself allowed 1e-5 * sum_k |a_k b_k|), within that bound plus one bf16 ulp.
 """
+import json
+import os
+
 import numpy as np
 import torch
 
@@ -14,6 +17,19 @@ import oracle
 from mxfp4_block_scaled_quantize_gb300 import abi, workloads
 
 FP32_REL = 1e-5
+# At most this fraction of a bf16 GEMM's outputs may pass only through the near-cancel
+# clause (more than 1 ulp from the rounded oracle, within 1e-5 * sum|ab| + 1 ulp of it):
+# those are outputs whose sum cancels so deeply that the fp32 accumulation error reaches
+# half a bf16 ulp of the result, which random inputs make rare.
+MAX_NEAR_CANCEL_FRAC = 0.01
+
+
+def log_stats(what: str, stats: dict) -> None:
+    """Appends one JSON line of comparison statistics to $MXFP4_PARITY_LOG, when set."""
+    path = os.environ.get("MXFP4_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"what": what, **stats}) + "\n")
 
 
 def to_gpu(x_cpu: torch.Tensor, device="cuda:0") -> torch.Tensor:
@@ -84,6 +100,20 @@ def check_quantized_sampled(x_cpu: torch.Tensor, outs, dual: bool, what: str, n_
                            f"{what} col s (sampled)")
 
 
+def check_rows_cols(x_cpu: torch.Tensor, outs, rows, cols, what: str) -> None:
+    """The row blob at the given rows and the col blob at the given columns of X equal the
+    oracle's (scales read from the tensor-core layout)."""
+    xb = workloads.bf16_bits(x_cpu)
+    rows = np.unique(np.asarray(rows))
+    cols = np.unique(np.asarray(cols))
+    rq, rs = oracle.quantize_row(np.ascontiguousarray(xb[rows]))
+    assert_bytes_equal(outs[0][torch.as_tensor(rows, device=outs[0].device)].cpu().numpy(), rq, f"{what} row q")
+    assert_bytes_equal(gather_tc_rows(outs[1].cpu().numpy(), rows, rs.shape[1]), rs, f"{what} row s")
+    cq, cs = oracle.quantize_col(np.ascontiguousarray(xb[:, cols]))
+    assert_bytes_equal(outs[2][torch.as_tensor(cols, device=outs[2].device)].cpu().numpy(), cq, f"{what} col q")
+    assert_bytes_equal(gather_tc_rows(outs[3].cpu().numpy(), cols, cs.shape[1]), cs, f"{what} col s")
+
+
 def tc_to_plain(s_tc: np.ndarray, R: int, KB: int) -> np.ndarray:
     return gather_tc_rows(s_tc, np.arange(R), KB)
 
@@ -113,7 +143,9 @@ def check_gemm(c_gpu: torch.Tensor, c_ref: np.ndarray, cabs: np.ndarray, what: s
             i = np.argwhere(bad)[0]
             raise AssertionError(f"{what}: {bad.sum()} fp32 outputs out of bound; first {tuple(i)}: "
                                  f"gpu {g[tuple(i)]!r} oracle {c_ref[tuple(i)]!r} bound {bound[tuple(i)]!r}")
-        return {"max_err_over_bound": float(np.max(err / np.maximum(bound, 1e-300)))}
+        stats = {"n": int(err.size), "max_err_over_bound": float(np.max(err / np.maximum(bound, 1e-300)))}
+        log_stats(what, stats)
+        return stats
     assert c_gpu.dtype == torch.bfloat16
     gbits = c_gpu.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     rbits = oracle.round_to_bf16(c_ref)
@@ -125,8 +157,13 @@ def check_gemm(c_gpu: torch.Tensor, c_ref: np.ndarray, cabs: np.ndarray, what: s
         i = tuple(np.argwhere(bad)[0])
         raise AssertionError(f"{what}: {bad.sum()} bf16 outputs off by more than 1 ulp; first {i}: "
                              f"gpu {g[i]!r} oracle {c_ref[i]!r} ({ulps[i]} ulp)")
-    return {"within_1ulp": int(np.sum(ulps <= 1)), "near_cancel": int(np.sum(ulps > 1)),
-            "exact": int(np.sum(ulps == 0)), "n": int(ulps.size)}
+    stats = {"within_1ulp": int(np.sum(ulps <= 1)), "near_cancel": int(np.sum(ulps > 1)),
+             "exact": int(np.sum(ulps == 0)), "n": int(ulps.size)}
+    log_stats(what, stats)
+    # (a fraction says nothing about a handful of outputs: applied from 1000 outputs up)
+    assert stats["n"] < 1000 or stats["near_cancel"] <= MAX_NEAR_CANCEL_FRAC * stats["n"], (
+        f"{what}: {stats['near_cancel']} of {stats['n']} bf16 outputs pass only as near-cancelling sums")
+    return stats
 
 
 def oracle_gemm_rows(a_q, a_s_plain, b_q, b_s_plain, rows):

@@ -141,10 +141,62 @@ def test_no_usable_device_fails_loudly(lib):
     assert lib.mxfp4_gemm_bias(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x60000, 0x50000, 4, 0, None) in bad
     assert lib.mxfp4_fp8_quantize_tw(0x10000, 4, 8, 8, 0x20000, None, 0x30000, 0x30004, None) in bad
     assert lib.mxfp4_fp8_gemm(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x50000, 4, 0, None) in bad
+    task = (abi.LinearHostTask * 1)(abi.LinearHostTask(0x1000, 0x2000, 0, 0x4000, 0, 0, 4, 8, 16, 0, 0))
+    assert lib.mxfp4_linear_step_host(1, task, 0x100000, 1 << 20, None) in bad
     assert lib.mxfp4_last_device_error(None) in bad
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         assert abi.status_string(code).startswith("MXFP4_")
     assert "unknown" in abi.status_string(99)
+
+
+def _host_task(M=4, N=8, K=16, train=0, od=0, x=0x1000, w=0x2000, dy=0x3000, y=0x4000, dx=0x5000, dw=0x6000):
+    return abi.LinearHostTask(x, w, dy, y, dx, dw, M, N, K, train, od)
+
+
+def test_linear_workspace_bytes(lib):
+    # Forward-only M 4, N 8, K 16, bf16 out: device X (4 x 16 bf16 = 128 B), W (256 B), X row
+    # blob (4 x 64 B codes; 128 padded rows x 4 scale bytes), W row blob (8 x 64 B; 512 B),
+    # Y (4 x 8 bf16 = 64 B), every piece rounded up to 256 bytes.
+    n = ctypes.c_size_t()
+    arr = (abi.LinearHostTask * 1)(_host_task())
+    assert lib.mxfp4_linear_workspace_bytes(1, arr, ctypes.byref(n)) == abi.MXFP4_OK
+    assert n.value == 256 + 256 + 256 + 512 + 512 + 512 + 256
+    # training adds dY (4 x 8 bf16), the col blobs of X, W and both blobs of dY, dX, dW;
+    # K = 12 is padded to a row pitch of 16 elements for the device copies of X and W.
+    arr = (abi.LinearHostTask * 1)(_host_task(M=4, N=8, K=12, train=1))
+    assert lib.mxfp4_linear_workspace_bytes(1, arr, ctypes.byref(n)) == abi.MXFP4_OK
+    fwd = 256 + 256 + 256 + 512 + 512 + 512 + 256
+    dy = 256
+    x_col = 12 * 64 + 128 * 4          # [12, Mp/2 = 64] codes, 128 x (Mp/32 = 4) scales
+    w_col = 12 * 64 + 128 * 4
+    dy_row = 4 * 64 + 128 * 4
+    dy_col = 8 * 64 + 128 * 4
+    dxdw = 256 + 256                   # 4 x 12 and 8 x 12 bf16, each under 256 bytes
+    r = lambda b: (b + 255) // 256 * 256
+    want = fwd + dy + r(12 * 64) + 512 + r(12 * 64) + 512 + r(4 * 64) + 512 + r(8 * 64) + 512 + dxdw
+    assert n.value == want
+    # two tasks: the sum of both
+    arr2 = (abi.LinearHostTask * 2)(_host_task(), _host_task(M=4, N=8, K=12, train=1))
+    assert lib.mxfp4_linear_workspace_bytes(2, arr2, ctypes.byref(n)) == abi.MXFP4_OK
+    assert n.value == fwd + want
+
+
+def test_linear_step_host_argument_checks(lib):
+    T = abi.LinearHostTask
+    ok = (T * 5)(*([_host_task()] * 5))
+    n = ctypes.c_size_t()
+    assert lib.mxfp4_linear_workspace_bytes(0, ok, ctypes.byref(n)) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_linear_workspace_bytes(5, ok, ctypes.byref(n)) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_linear_workspace_bytes(1, ok, None) == abi.MXFP4_ERR_INVALID_ARG
+    for bad in (_host_task(M=0), _host_task(od=3), _host_task(train=2), _host_task(x=0),
+                _host_task(train=1, dy=0), _host_task(train=1, dw=0)):
+        arr = (T * 2)(_host_task(), bad)
+        assert lib.mxfp4_linear_workspace_bytes(2, arr, ctypes.byref(n)) == abi.MXFP4_ERR_INVALID_ARG
+        assert lib.mxfp4_linear_step_host(2, arr, 0x100000, 1 << 20, None) == abi.MXFP4_ERR_INVALID_ARG
+    one = (T * 1)(_host_task())
+    assert lib.mxfp4_linear_step_host(1, one, None, 1 << 20, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_linear_step_host(1, one, 0x100000, 100, None) == abi.MXFP4_ERR_INVALID_ARG   # too small
+    assert lib.mxfp4_linear_step_host(1, one, 0x100010, 1 << 20, None) == abi.MXFP4_ERR_MISALIGNED

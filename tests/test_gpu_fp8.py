@@ -187,3 +187,20 @@ def test_fp8_quantize_batch_equals_single_calls():
                 assert (g is None) == (w is None)
                 if g is not None:
                     assert torch.equal(g.view(torch.uint8).cpu(), w.view(torch.uint8).cpu())
+
+
+@pytest.mark.parametrize("bad", [float("inf"), float("-inf"), float("nan")])
+def test_fp8_non_finite_input_is_reported(bad):
+    # A non-finite element makes the tensor's amax non-finite: the conversion records it in
+    # the device error word, which reads back as MXFP4_ERR_NONFINITE once and is then clear;
+    # a finite tensor quantized afterwards is unaffected.
+    x = workloads.normal((130, 200), 1.0, 5)
+    x[77, 123] = bad
+    abi.fp8_quantize(x.cuda())
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_ERR_NONFINITE
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    y = workloads.normal((130, 200), 1.0, 6)
+    qr, qc, amax, inv = abi.fp8_quantize(y.cuda())
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    want_qr, want_qc, want_amax, want_inv = oracle.fp8_quantize_tw(workloads.bf16_bits(y))
+    assert_bytes_equal(qr.cpu().numpy(), want_qr, "finite tensor after a non-finite one")

@@ -95,6 +95,44 @@ def test_step_from_host_matches_device_step():
             assert torch.equal(got.view(torch.int16), exp.view(torch.int16))
 
 
+def test_block_host_step_matches_device_step():
+    # The library's host-buffer step (mxfp4_linear_step_host) over three linears -- two
+    # training, one forward-only; bf16 and fp32 outputs; K = 1001 needs a pitched device copy
+    # -- gives the bytes of the device step of each linear, twice in a row (workspace and
+    # copy streams reused).
+    from mxfp4_block_scaled_quantize_gb300.linear import MXFP4Block
+    shapes = [("a", 300, 520, 200, True, torch.bfloat16), ("b", 257, 136, 1001, True, torch.float32),
+              ("c", 130, 264, 384, False, torch.bfloat16)]
+    host_in, want = [], []
+    for i, (_, M, N, K, train, od) in enumerate(shapes):
+        t = {"X": workloads.student_t3((M, K), 1.0, 71 + i), "W": workloads.normal((N, K), 0.3, 81 + i)}
+        if train:
+            t["dY"] = workloads.normal((M, N), 0.01, 91 + i)
+        host_in.append({k: v.pin_memory() for k, v in t.items()})
+        ref = MXFP4Linear(M, N, K, train=train, out_dtype=od)
+        outs = ref.step(pitched(t["X"]), pitched(t["W"]), pitched(t["dY"]) if train else None)
+        want.append([o.cpu() for o in outs])
+    torch.cuda.synchronize()
+    tasks = []
+    for (_, M, N, K, train, od), hi in zip(shapes, host_in):
+        code = abi.MXFP4_OUT_F32 if od == torch.float32 else abi.MXFP4_OUT_BF16
+        tasks.append([hi["X"], hi["W"], hi.get("dY"), None, None, None, M, N, K, train, code])
+    need = abi.mxfp4_linear_workspace_bytes(tasks)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        got = []
+        for tk, w_ in zip(tasks, want):
+            outs = [torch.full(o.shape, float("nan"), dtype=o.dtype).pin_memory() for o in w_]
+            tk[3:3 + len(outs)] = outs
+            got.append(outs)
+        abi.mxfp4_linear_step_host([tuple(t) for t in tasks], ws, need)
+        torch.cuda.current_stream().synchronize()
+        assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+        for g_, w_ in zip(got, want):
+            for a, b in zip(g_, w_):
+                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 8, 32), (200, 300, 40), (129, 257, 384),
                                    (128, 256, 256), (300, 520, 1000), (64, 1000, 4600),
                                    (256, 128, 128), (384, 768, 640), (513, 255, 2048)])

@@ -12,7 +12,8 @@ import torch
 
 import oracle
 from mxfp4_block_scaled_quantize_gb300 import abi, workloads
-from parity import (assert_bytes_equal, check_quantized_full, check_quantized_sampled)
+from parity import (assert_bytes_equal, check_quantized_full, check_quantized_sampled,
+                    check_rows_cols)
 
 pytestmark = pytest.mark.gpu
 
@@ -175,19 +176,21 @@ def test_outputs_written_exactly():
         check_quantized_full(x.cpu(), outs, layout, True, f"guarded layout {layout}")
 
 
-@pytest.mark.parametrize("M,K", [(4608, 3072), (4600, 3072), (4608, 12288), (18432, 3072),
-                                 (4600, 15360)])
+@pytest.mark.parametrize("M", workloads.SWEEP_M)
+@pytest.mark.parametrize("K", workloads.SWEEP_K)
 @pytest.mark.parametrize("scale", workloads.SWEEP_SCALE)
 def test_sweep_sampled(M, K, scale):
+    # The whole bandwidth/edge sweep: every M x K pair at every scale, Student-t(3) values
+    # with all-subnormal, mixed, near-bf16-max and all-zero blocks along both packings, in
+    # the launch configuration of the full-size call; sampled rows and whole columns.
     x = workloads.sweep_tensor(M, K, scale)
     outs = quant(x, True, abi.MXFP4_SCALE_TC)
-    check_quantized_sampled(x, outs, True, f"sweep {M}x{K}x{scale}")
-
-
-def test_sweep_largest_sampled():
-    x = workloads.sweep_tensor(18432, 15360, 1.0)
-    outs = quant(x, True, abi.MXFP4_SCALE_TC)
-    check_quantized_sampled(x, outs, True, "sweep 18432x15360", n_rows=16, n_cols=16)
+    n = 16 if M * K > 10**8 else 48
+    check_quantized_sampled(x, outs, True, f"sweep {M}x{K}x{scale}", n_rows=n, n_cols=n)
+    # the injected edge blocks sit in rows 7 + 13i and columns 11 + 17i: always compared
+    edge_rows = np.array([(7 + 13 * i) % M for i in range(4)])
+    edge_cols = np.array([(11 + 17 * i) % K for i in range(4)])
+    check_rows_cols(x, outs, edge_rows, edge_cols, f"sweep {M}x{K}x{scale} edge blocks")
 
 
 @pytest.mark.parametrize("wname", ["flux12b_qkv_fwd_4608x9216x3072",

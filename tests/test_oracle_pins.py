@@ -640,3 +640,36 @@ def test_2d_blocks_hand_worked():
     assert rq[0, 0] & 0xF == 3
     assert (rq[5, 3] >> 4) == 7
     assert rq[9, 1] & 0xF == 0x8
+
+
+def test_scale_to_tc_hand_placed_positions():
+    # Each cell's scale byte lands at the offset placed by hand from the tcgen05 scale-factor
+    # layout (tests/golden/tc_scale_atom.json, with its source): one marked cell at a time,
+    # every other byte zero.
+    with open(os.path.join(GOLDEN, "tc_scale_atom.json")) as f:
+        g = json.load(f)
+    R, KB = g["R"], g["KB"]
+    for cell in g["cells"]:
+        s = np.zeros((R, KB), np.uint8)
+        s[cell["r"], cell["kb"]] = 0xA7
+        out = oracle.scale_to_tc(s)
+        assert np.flatnonzero(out).tolist() == [cell["offset"]], cell
+
+
+def test_scale_to_tc_atom_in_copy_order():
+    # A 128 x 4 piece written out in the order the 32x128b copy reads it: for each of the
+    # 32 lines, the rows line, line+32, line+64, line+96, each with its 4 K blocks.
+    rng = np.random.default_rng(5)
+    s = rng.integers(1, 255, size=(128, 4), dtype=np.uint8)
+    want = []
+    for line in range(32):
+        for group in range(4):
+            for k in range(4):
+                want.append(s[32 * group + line, k])
+    assert oracle.scale_to_tc(s).tolist() == [int(v) for v in want]
+    # two pieces along K follow each other; a second row group follows both
+    s2 = rng.integers(1, 255, size=(256, 8), dtype=np.uint8)
+    out = oracle.scale_to_tc(s2)
+    for piece, (r0, k0) in enumerate([(0, 0), (0, 4), (128, 0), (128, 4)]):
+        assert out[512 * piece:512 * (piece + 1)].tolist() == oracle.scale_to_tc(
+            np.ascontiguousarray(s2[r0:r0 + 128, k0:k0 + 4])).tolist()
