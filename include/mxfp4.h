@@ -294,7 +294,8 @@ typedef struct {
 } mxfp4_linear_host_task;
 
 /* Bytes of device workspace mxfp4_linear_step_host needs for these tasks (the device
- * copies of the inputs, every blob, and the device results).  count in 1..MXFP4_MAX_BATCH. */
+ * copies of the inputs, every blob, and the device results).  count in 1..MXFP4_MAX_BATCH;
+ * only the shapes, out_dtype and train of each task are read (the pointers may be NULL). */
 mxfp4_status mxfp4_linear_workspace_bytes(int32_t count, const mxfp4_linear_host_task* tasks,
                                           size_t* bytes);
 

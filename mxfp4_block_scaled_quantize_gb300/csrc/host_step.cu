@@ -78,7 +78,8 @@ size_t carve(const mxfp4_linear_host_task& t, uint8_t* base, Carve* c) {
     return off;
 }
 
-mxfp4_status check_tasks(int32_t count, const mxfp4_linear_host_task* tasks) {
+// Shapes, dtype and mode of every task; with `pointers`, also the host buffers.
+mxfp4_status check_tasks(int32_t count, const mxfp4_linear_host_task* tasks, bool pointers) {
     if (count < 1 || count > MXFP4_MAX_BATCH || tasks == nullptr) return MXFP4_ERR_INVALID_ARG;
     for (int i = 0; i < count; ++i) {
         const mxfp4_linear_host_task& t = tasks[i];
@@ -86,8 +87,8 @@ mxfp4_status check_tasks(int32_t count, const mxfp4_linear_host_task* tasks) {
             return MXFP4_ERR_INVALID_ARG;
         if (t.out_dtype != MXFP4_OUT_BF16 && t.out_dtype != MXFP4_OUT_F32) return MXFP4_ERR_INVALID_ARG;
         if (t.train != 0 && t.train != 1) return MXFP4_ERR_INVALID_ARG;
-        if (!t.x || !t.w || !t.y) return MXFP4_ERR_INVALID_ARG;
-        if (t.train && (!t.dy || !t.dx || !t.dw)) return MXFP4_ERR_INVALID_ARG;
+        if (pointers && (!t.x || !t.w || !t.y)) return MXFP4_ERR_INVALID_ARG;
+        if (pointers && t.train && (!t.dy || !t.dx || !t.dw)) return MXFP4_ERR_INVALID_ARG;
     }
     return MXFP4_OK;
 }
@@ -143,7 +144,7 @@ mxfp4_status copy_streams(CopyStreams** out) {
 extern "C" {
 
 mxfp4_status mxfp4_linear_workspace_bytes(int32_t count, const mxfp4_linear_host_task* tasks, size_t* bytes) {
-    MX_TRY_ST(check_tasks(count, tasks));
+    MX_TRY_ST(check_tasks(count, tasks, false));
     if (bytes == nullptr) return MXFP4_ERR_INVALID_ARG;
     *bytes = total_bytes(count, tasks);
     return MXFP4_OK;
@@ -151,7 +152,7 @@ mxfp4_status mxfp4_linear_workspace_bytes(int32_t count, const mxfp4_linear_host
 
 mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task* tasks, void* workspace,
                                     size_t workspace_bytes, mxfp4_stream_t stream) {
-    MX_TRY_ST(check_tasks(count, tasks));
+    MX_TRY_ST(check_tasks(count, tasks, true));
     if (workspace == nullptr || workspace_bytes < total_bytes(count, tasks)) return MXFP4_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MXFP4_ERR_MISALIGNED;
     std::lock_guard<std::mutex> lock(g_host_mutex);

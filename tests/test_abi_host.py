@@ -191,10 +191,14 @@ def test_linear_step_host_argument_checks(lib):
     assert lib.mxfp4_linear_workspace_bytes(0, ok, ctypes.byref(n)) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_linear_workspace_bytes(5, ok, ctypes.byref(n)) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_linear_workspace_bytes(1, ok, None) == abi.MXFP4_ERR_INVALID_ARG
-    for bad in (_host_task(M=0), _host_task(od=3), _host_task(train=2), _host_task(x=0),
-                _host_task(train=1, dy=0), _host_task(train=1, dw=0)):
+    for bad in (_host_task(M=0), _host_task(od=3), _host_task(train=2)):
         arr = (T * 2)(_host_task(), bad)
         assert lib.mxfp4_linear_workspace_bytes(2, arr, ctypes.byref(n)) == abi.MXFP4_ERR_INVALID_ARG
+        assert lib.mxfp4_linear_step_host(2, arr, 0x100000, 1 << 20, None) == abi.MXFP4_ERR_INVALID_ARG
+    # the size query reads shapes only; the step needs every host buffer of its mode
+    for bad in (_host_task(x=0), _host_task(y=0), _host_task(train=1, dy=0), _host_task(train=1, dw=0)):
+        arr = (T * 2)(_host_task(), bad)
+        assert lib.mxfp4_linear_workspace_bytes(2, arr, ctypes.byref(n)) == abi.MXFP4_OK
         assert lib.mxfp4_linear_step_host(2, arr, 0x100000, 1 << 20, None) == abi.MXFP4_ERR_INVALID_ARG
     one = (T * 1)(_host_task())
     assert lib.mxfp4_linear_step_host(1, one, None, 1 << 20, None) == abi.MXFP4_ERR_INVALID_ARG
