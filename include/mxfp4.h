@@ -116,9 +116,26 @@ mxfp4_status mxfp4_quantize_dual_sr(const void* x, int64_t M, int64_t K, int64_t
                                     mxfp4_scale_layout layout, uint64_t seed,
                                     mxfp4_stream_t stream);
 
+/* Dual quantizer with 2-D block scales: the weight quantization of `_quantize_weight_dual`
+ * in primus_turbo_mxfp4_local.py (`rowwise_use_2d_block` and `colwise_use_2d_block` set,
+ * every other recipe flag off).  The pages name the flags only; what it computes here: X
+ * is cut into 32 x 32 blocks (padding +0), each block gets one E8M0 scale byte from the
+ * amax of its 1024 elements by the rule above, and every element of the block is encoded
+ * with that scale in both packings -- so the row blob's scale of (row r, block kb) and the
+ * col blob's scale of (column k, block mb) are the scale of the 2-D block that holds them,
+ * and the two blobs dequantize to exact transposes of each other.  Scale bytes of padding
+ * rows of the tensor-core layout are 0x00, as for the 1-D blobs.  Arguments, layouts and
+ * errors as mxfp4_quantize_dual. */
+mxfp4_status mxfp4_quantize_dual_2d(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                    void* q_row, void* s_row, void* q_col, void* s_col,
+                                    mxfp4_scale_layout layout, mxfp4_stream_t stream);
+
+/* Bits of mxfp4_quantize_task::flags. */
+#define MXFP4_QUANT_2D_BLOCKS 1   /* 32 x 32 blocks, as mxfp4_quantize_dual_2d (row-only too) */
+
 /* One tensor of a batched quantization: bf16 x[rows, k] with row pitch ldx elements and
  * its output buffers, as for mxfp4_quantize / mxfp4_quantize_dual (q_col and s_col are
- * read only for the dual quantizer). */
+ * read only for the dual quantizer); flags: 0 or MXFP4_QUANT_2D_BLOCKS. */
 typedef struct {
     const void* x;
     int64_t rows;
@@ -128,12 +145,14 @@ typedef struct {
     void* s_row;
     void* q_col;
     void* s_col;
+    int32_t flags;
 } mxfp4_quantize_task;
 
 #define MXFP4_MAX_BATCH 4
 
 /* Quantizes 1..MXFP4_MAX_BATCH independent tensors in one launch, each with exactly the
- * output of mxfp4_quantize (dual == 0) or mxfp4_quantize_dual (dual != 0).  Same
+ * output of mxfp4_quantize (dual == 0) or mxfp4_quantize_dual (dual != 0), or with 2-D
+ * blocks (task flag MXFP4_QUANT_2D_BLOCKS) that of mxfp4_quantize_dual_2d.  Same
  * operation as those two (the per-tensor `quantize_mxfp4` / `_quantize_mxfp4_dual_op`
  * calls of primus_turbo_mxfp4_local.py); one launch lets a small tensor share the GPU with
  * a large one instead of paying its own ramp-up and tail (the forward step quantizes X and

@@ -41,7 +41,10 @@ class QuantizeTask(ctypes.Structure):
     """mxfp4_quantize_task of include/mxfp4.h."""
     _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("k", ctypes.c_int64),
                 ("ldx", ctypes.c_int64), ("q_row", ctypes.c_void_p), ("s_row", ctypes.c_void_p),
-                ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p)]
+                ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p), ("flags", ctypes.c_int32)]
+
+
+MXFP4_QUANT_2D_BLOCKS = 1
 
 class Fp8QuantizeTask(ctypes.Structure):
     """mxfp4_fp8_quantize_task of include/mxfp4.h."""
@@ -71,6 +74,7 @@ EXPORTED = (
     "mxfp4_quantize",
     "mxfp4_quantize_dual",
     "mxfp4_quantize_dual_sr",
+    "mxfp4_quantize_dual_2d",
     "mxfp4_quantize_batch",
     "mxfp4_gemm",
     "mxfp4_gemm_bias",
@@ -112,6 +116,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_quantize.argtypes = [vp, i64, i64, i64, vp, vp, i32, vp]
     lib.mxfp4_quantize_dual.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, vp]
     lib.mxfp4_quantize_dual_sr.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, ctypes.c_uint64, vp]
+    lib.mxfp4_quantize_dual_2d.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, vp]
     lib.mxfp4_quantize_batch.argtypes = [i32, ctypes.POINTER(QuantizeTask), i32, i32, vp]
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_gemm_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i32, vp]
@@ -189,13 +194,22 @@ def mxfp4_quantize_dual_sr(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=MXFP
            "mxfp4_quantize_dual_sr")
 
 
+def mxfp4_quantize_dual_2d(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=MXFP4_SCALE_TC,
+                           stream=None) -> None:
+    _check(load().mxfp4_quantize_dual_2d(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
+                                         _ptr(s_col), layout, _stream(stream)),
+           "mxfp4_quantize_dual_2d")
+
+
 def mxfp4_quantize_batch(tasks, dual: bool, layout=MXFP4_SCALE_TC, stream=None) -> None:
-    """tasks: sequence of (x, rows, k, ldx, q_row, s_row, q_col, s_col); q_col / s_col may
-    be None for the row-only quantizer."""
+    """tasks: sequence of (x, rows, k, ldx, q_row, s_row, q_col, s_col[, flags]); q_col /
+    s_col may be None for the row-only quantizer; flags 0 or MXFP4_QUANT_2D_BLOCKS."""
     arr = (QuantizeTask * max(1, len(tasks)))()
-    for i, (x, rows, k, ldx, q_row, s_row, q_col, s_col) in enumerate(tasks):
+    for i, t in enumerate(tasks):
+        x, rows, k, ldx, q_row, s_row, q_col, s_col = t[:8]
+        flags = t[8] if len(t) > 8 else 0
         arr[i] = QuantizeTask(_ptr(x), rows, k, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
-                              _ptr(s_col))
+                              _ptr(s_col), flags)
     _check(load().mxfp4_quantize_batch(len(tasks), arr, int(bool(dual)), layout, _stream(stream)),
            "mxfp4_quantize_batch")
 
@@ -304,13 +318,24 @@ def alloc_blob(rows: int, k: int, layout: int = MXFP4_SCALE_TC, device="cuda"):
     return q, s
 
 
-def quantize(x, dual: bool = True, layout: int = MXFP4_SCALE_TC, stream=None, sr_seed=None):
+def quantize(x, dual: bool = True, layout: int = MXFP4_SCALE_TC, stream=None, sr_seed=None,
+             block_2d: bool = False):
     """bf16 X[M,K] (CUDA, row pitch a multiple of 8) -> (row_q, row_s[, col_q, col_s]);
-    with sr_seed (dual only) the elements are stochastically rounded."""
+    with sr_seed (dual only) the elements are stochastically rounded; with block_2d the
+    scales are those of 32 x 32 blocks."""
     import torch
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     rq, rs = alloc_blob(M, K, layout, x.device)
+    if block_2d:
+        assert sr_seed is None, "the 2-D block recipe is for weights, stochastic rounding for gradients"
+        if not dual:
+            mxfp4_quantize_batch([(x, M, K, x.stride(0), rq, rs, None, None, MXFP4_QUANT_2D_BLOCKS)], False,
+                                 layout, stream)
+            return rq, rs
+        cq, cs = alloc_blob(K, M, layout, x.device)
+        mxfp4_quantize_dual_2d(x, M, K, x.stride(0), rq, rs, cq, cs, layout, stream)
+        return rq, rs, cq, cs
     if not dual:
         assert sr_seed is None, "stochastic rounding is a mode of the dual quantizer"
         mxfp4_quantize(x, M, K, x.stride(0), rq, rs, layout, stream)

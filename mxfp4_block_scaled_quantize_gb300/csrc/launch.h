@@ -23,6 +23,7 @@ struct QuantArgs {
     int64_t kb_col;      // Mp / 32
     int32_t tc_layout;   // 1: tensor-core scale layout, 0: plain
     uint64_t seed;       // Philox key of the stochastic-rounding instance (unused otherwise)
+    int32_t block_2d;    // 1: 32 x 32 blocks (one scale per block in both packings)
     uint32_t* err;       // device error word
 };
 

@@ -25,8 +25,19 @@
 // (Measured on GB300: whole-sector stores took the dY quantization of the Flux MLP step
 // from 35.4 to 30.7 us.)  The swizzle makes both access patterns bank-conflict free.
 // Consumer warps never wait
-// for each other: each warp waits for the stage itself, stores its codes and scale bytes
-// straight to global memory, and releases the stage with its own barrier arrival.
+// for each other (except for 2-D blocks, below): each warp waits for the stage itself,
+// stores its codes and scale bytes straight to global memory, and releases the stage with
+// its own barrier arrival.
+//
+// 2-D blocks (the weight recipe of `_quantize_weight_dual`, `rowwise_use_2d_block` and
+// `colwise_use_2d_block`): X is cut into 32 x 32 blocks, each gets one scale byte from the
+// amax of its 1024 elements by the same rule, and both packings encode every element of the
+// block with it.  A 128 x 128 tile holds 16 whole blocks: each rowwise thread's 1 x 32 amax
+// is folded over the 4 lanes of its warp that share the block and written per warp to
+// shared memory; after one named barrier of the consumer warps every thread takes the
+// block's maximum over the 8 warps, for its row blocks and, in the columnwise pass, for
+// its column pair (both columns lie in one block).  Scale bytes of padding rows of the
+// tensor-core layout stay 0x00, as in the 1-D packings.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -47,8 +58,12 @@ struct QuantSmem {
     uint8_t tile[kQStages][kQTileBytes];       // per stage: two 64-column swizzled boxes
     uint64_t full[kQStages];
     uint64_t empty[kQStages];                  // one arrival per consumer warp
+    // 2-D blocks: per tile parity, per consumer warp, per block (row group Q, block column
+    // b): the warp's largest magnitude (bf16 bits) in that block
+    uint32_t part[2][kQConsumerWarps][16];
     int abort;
 };
+constexpr uint32_t kBarConsumers = 1;          // named barrier of the consumer warps
 
 constexpr int kQBoxBytes = kQT * 128;          // 128 rows x 64 bf16 columns
 
@@ -266,7 +281,9 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     return v;
 }
 
-template <bool kDual, bool kSR>
+// k2D: some task of the launch has 2-D blocks (QuantArgs::block_2d); such a task's tiles
+// take the 2-D path, the others the 1-D one.
+template <bool kDual, bool kSR, bool k2D>
 __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     quantize_kernel(const __grid_constant__ QuantBatch P) {
     extern __shared__ uint8_t smem_raw[];
@@ -350,45 +367,73 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
         //      L = 4w..4w+3 (rows L, L+32, L+64, L+96) and all four block columns, so each
         //      store instruction writes whole 32-byte sectors of 16 rows, and each quarter
         //      warp's 16-byte shared reads hit 8 distinct swizzled chunks.
+        const bool blk2d = k2D && p.block_2d;
+        const int L = 4 * warp + (lane & 3);
+        const int Q = lane >> 3;
+        const int r = Q * 32 + L;
+        const int64_t row = m0 + r;
+        uint4 v[2][4];
+        uint32_t bm[2];
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            const int L = 4 * warp + (lane & 3);
-            const int Q = lane >> 3;
             const int b = ((lane >> 2) & 1) + 2 * i;
-            const int r = Q * 32 + L;
             const uint32_t box = tile + (b >> 1) * kQBoxBytes;
             const int j0 = (b & 1) * 4;
-            const uint4 v0 = lds128(box + swz(r, j0 + 0));
-            const uint4 v1 = lds128(box + swz(r, j0 + 1));
-            const uint4 v2 = lds128(box + swz(r, j0 + 2));
-            const uint4 v3 = lds128(box + swz(r, j0 + 3));
-            uint32_t m = absmax2(absmax2(absmax2(v0.x, v0.y), absmax2(v0.z, v0.w)),
-                                 absmax2(absmax2(v1.x, v1.y), absmax2(v1.z, v1.w)));
-            m = absmax2(m, absmax2(absmax2(absmax2(v2.x, v2.y), absmax2(v2.z, v2.w)),
-                                   absmax2(absmax2(v3.x, v3.y), absmax2(v3.z, v3.w))));
-            m = absmax2(m, m >> 16);
-            const uint32_t byte = scale_byte(m);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) v[i][c] = lds128(box + swz(r, j0 + c));
+            uint32_t m = absmax2(absmax2(absmax2(v[i][0].x, v[i][0].y), absmax2(v[i][0].z, v[i][0].w)),
+                                 absmax2(absmax2(v[i][1].x, v[i][1].y), absmax2(v[i][1].z, v[i][1].w)));
+            m = absmax2(m, absmax2(absmax2(absmax2(v[i][2].x, v[i][2].y), absmax2(v[i][2].z, v[i][2].w)),
+                                   absmax2(absmax2(v[i][3].x, v[i][3].y), absmax2(v[i][3].z, v[i][3].w))));
+            m = absmax2(m, m >> 16) & 0x7FFFu;   // the block's largest magnitude, bf16 bits
+            bm[i] = m;
+        }
+        const int par = it & 1;
+        if (blk2d) {
+            // fold over the 4 lanes of the warp that share (Q, b), then one word per warp
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                bm[i] = max(bm[i], __shfl_xor_sync(0xFFFFFFFFu, bm[i], 1));
+                bm[i] = max(bm[i], __shfl_xor_sync(0xFFFFFFFFu, bm[i], 2));
+                if ((lane & 3) == 0) sm.part[par][warp][Q * 4 + ((lane >> 2) & 1) + 2 * i] = bm[i];
+            }
+            named_barrier(kBarConsumers, kQConsumers);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int b = ((lane >> 2) & 1) + 2 * i;
+                uint32_t m = 0;
+#pragma unroll
+                for (int w = 0; w < kQConsumerWarps; ++w) m = max(m, sm.part[par][w][Q * 4 + b]);
+                bm[i] = m;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int b = ((lane >> 2) & 1) + 2 * i;
+            const uint32_t byte = scale_byte(bm[i]);
             const uint32_t inv = inv_scale_bits(byte);
-            const int64_t row = m0 + r;
             uint4 q;
             if (kSR) {
                 const float invf = __uint_as_float(inv);
                 const uint32_t c0 = static_cast<uint32_t>((k0 + 32 * b) >> 3), a = static_cast<uint32_t>(row);
-                q = make_uint4(encode8_sr(v0, invf, philox4x32_10(c0 + 0, a, 0u, p.seed)),
-                               encode8_sr(v1, invf, philox4x32_10(c0 + 1, a, 0u, p.seed)),
-                               encode8_sr(v2, invf, philox4x32_10(c0 + 2, a, 0u, p.seed)),
-                               encode8_sr(v3, invf, philox4x32_10(c0 + 3, a, 0u, p.seed)));
+                q = make_uint4(encode8_sr(v[i][0], invf, philox4x32_10(c0 + 0, a, 0u, p.seed)),
+                               encode8_sr(v[i][1], invf, philox4x32_10(c0 + 1, a, 0u, p.seed)),
+                               encode8_sr(v[i][2], invf, philox4x32_10(c0 + 2, a, 0u, p.seed)),
+                               encode8_sr(v[i][3], invf, philox4x32_10(c0 + 3, a, 0u, p.seed)));
             } else {
                 const uint64_t s2 = pack2(inv, inv);
-                q = make_uint4(encode8(v0.x, v0.y, v0.z, v0.w, s2), encode8(v1.x, v1.y, v1.z, v1.w, s2),
-                               encode8(v2.x, v2.y, v2.z, v2.w, s2), encode8(v3.x, v3.y, v3.z, v3.w, s2));
+                q = make_uint4(encode8(v[i][0].x, v[i][0].y, v[i][0].z, v[i][0].w, s2),
+                               encode8(v[i][1].x, v[i][1].y, v[i][1].z, v[i][1].w, s2),
+                               encode8(v[i][2].x, v[i][2].y, v[i][2].z, v[i][2].w, s2),
+                               encode8(v[i][3].x, v[i][3].y, v[i][3].z, v[i][3].w, s2));
             }
             if (row < p.M) {
                 *reinterpret_cast<uint4*>(p.q_row + row * p.ldq_row + ((k0 + 32 * b) >> 1)) = q;
                 if (!p.tc_layout) p.s_row[row * p.kb_row + (k0 >> 5) + b] = static_cast<uint8_t>(byte);
             }
-            // Padding rows of the tensor-core layout get their (zero) byte too.
-            if (p.tc_layout) atom_row[L * 16 + Q * 4 + b] = static_cast<uint8_t>(byte);
+            // Padding rows of the tensor-core layout get the byte 0x00 (a 1-D padding
+            // block's own amax is 0; a 2-D block's rows past M do not carry its scale).
+            if (p.tc_layout) atom_row[L * 16 + Q * 4 + b] = static_cast<uint8_t>(row < p.M ? byte : 0u);
         }
 
         // ---- columnwise: thread owns columns (2pc, 2pc+1) of the 32-row block rb; a warp
@@ -413,10 +458,20 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
             uint32_t w[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) w[i] = lds32(toff[i & 7] + (i & ~7) * 128);
-            uint32_t m = w[0];
+            uint32_t byte0, byte1;
+            if (blk2d) {
+                // both columns lie in block column pc / 16 of row group rb
+                uint32_t m = 0;
 #pragma unroll
-            for (int i = 1; i < 32; ++i) m = absmax2(m, w[i]);
-            const uint32_t byte0 = scale_byte(m), byte1 = scale_byte(m >> 16);
+                for (int w2 = 0; w2 < kQConsumerWarps; ++w2) m = max(m, sm.part[par][w2][rb * 4 + (pc >> 4)]);
+                byte0 = byte1 = scale_byte(m);
+            } else {
+                uint32_t m = w[0];
+#pragma unroll
+                for (int i = 1; i < 32; ++i) m = absmax2(m, w[i]);
+                byte0 = scale_byte(m);
+                byte1 = scale_byte(m >> 16);
+            }
             const uint64_t s2 = pack2(inv_scale_bits(byte0), inv_scale_bits(byte1));
             const uint32_t sel = 0x3210u ^ (0x1111u * static_cast<uint32_t>(rb));
             const int64_t kc = k0 + 2 * pc;
@@ -447,9 +502,9 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
                 if (!p.tc_layout) p.s_col[(kc + 1) * p.kb_col + (m0 >> 5) + rb] = static_cast<uint8_t>(byte1);
             }
             const int kl0 = 2 * pc, kl1 = 2 * pc + 1;
-            if (p.tc_layout) {
-                atom_col[(kl0 & 31) * 16 + (kl0 >> 5) * 4 + rb] = static_cast<uint8_t>(byte0);
-                atom_col[(kl1 & 31) * 16 + (kl1 >> 5) * 4 + rb] = static_cast<uint8_t>(byte1);
+            if (p.tc_layout) {   // padding rows (columns of X past K) keep 0x00
+                atom_col[(kl0 & 31) * 16 + (kl0 >> 5) * 4 + rb] = static_cast<uint8_t>(kc < p.K ? byte0 : 0u);
+                atom_col[(kl1 & 31) * 16 + (kl1 >> 5) * 4 + rb] = static_cast<uint8_t>(kc + 1 < p.K ? byte1 : 0u);
             }
         }
 
@@ -467,7 +522,12 @@ int quantize_ctas_per_sm() { return kQCtasPerSm; }
 cudaError_t launch_quantize(const QuantBatch& b, bool dual, bool sr, int grid, cudaStream_t stream) {
     const size_t smem = quantize_smem_bytes();
     if (sr && !dual) return cudaErrorInvalidValue;
-    auto k = sr ? quantize_kernel<true, true> : dual ? quantize_kernel<true, false> : quantize_kernel<false, false>;
+    bool b2d = false;
+    for (int j = 0; j < b.count; ++j) b2d = b2d || b.args[j].block_2d != 0;
+    if (sr && b2d) return cudaErrorInvalidValue;
+    auto k = sr    ? quantize_kernel<true, true, false>
+             : b2d ? (dual ? quantize_kernel<true, false, true> : quantize_kernel<false, false, true>)
+                   : (dual ? quantize_kernel<true, false, false> : quantize_kernel<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];

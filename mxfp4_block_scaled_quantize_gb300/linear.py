@@ -8,7 +8,9 @@ Follows the dataflow of `MXFP4LinearFunction` in primus_turbo_mxfp4_local.py:
             quantizer's `use_sr`), dX = dY_row . (W_col)^T, dW = dY_col . (X_col)^T;
             or, with backward="fp8", the pages' hybrid backward (tensorwise E5M2 of dY,
             X, W and FP8 GEMMs)
-The other recipe flags (2-D weight blocks, Hadamard transform, shuffles) are off.  In the
+With weight_2d, W is quantized with one scale per 32 x 32 block in both packings (the
+weight recipe of `_quantize_weight_dual`, `rowwise_use_2d_block` / `colwise_use_2d_block`).
+The other recipe flags (Hadamard transform, shuffles) are off.  In the
 MXFP4 backward only the column blobs of X and W live from forward to backward; bf16 X
 and W are not kept.  All buffers are allocated once (torch as the allocator) and reused,
 so an MXFP4 step is four launches on one stream: X and W quantized together, the forward
@@ -27,9 +29,10 @@ class MXFP4Linear:
     column blobs would only feed an MXFP4 backward."""
 
     def __init__(self, M: int, N: int, K: int, train: bool = True, device="cuda",
-                 out_dtype=torch.bfloat16, backward: str = "mxfp4"):
+                 out_dtype=torch.bfloat16, backward: str = "mxfp4", weight_2d: bool = False):
         assert backward in ("mxfp4", "fp8")
         self.M, self.N, self.K, self.train = M, N, K, train
+        self.weight_2d = weight_2d
         self.fp8_backward = train and backward == "fp8"
         L = abi.MXFP4_SCALE_TC
         self.x_row = abi.alloc_blob(M, K, L, device)
@@ -64,11 +67,13 @@ class MXFP4Linear:
 
     def quantize_w(self, w, stream=None):
         N, K = self.N, self.K
-        if self.train:
-            abi.mxfp4_quantize_dual(w, N, K, w.stride(0), *self.w_row, *self.w_col,
-                                    abi.MXFP4_SCALE_TC, stream)
+        if self.train and not self.fp8_backward:
+            quant = abi.mxfp4_quantize_dual_2d if self.weight_2d else abi.mxfp4_quantize_dual
+            quant(w, N, K, w.stride(0), *self.w_row, *self.w_col, abi.MXFP4_SCALE_TC, stream)
         else:
-            abi.mxfp4_quantize(w, N, K, w.stride(0), *self.w_row, abi.MXFP4_SCALE_TC, stream)
+            flags = abi.MXFP4_QUANT_2D_BLOCKS if self.weight_2d else 0
+            abi.mxfp4_quantize_batch([(w, N, K, w.stride(0), *self.w_row, None, None, flags)], False,
+                                     abi.MXFP4_SCALE_TC, stream)
 
     def quantize_dy(self, dy, stream=None, sr_seed=None):
         """dY's two blobs; with sr_seed, stochastically rounded (the gradient quantizer's
@@ -110,12 +115,13 @@ class MXFP4Linear:
         M, N, K = self.M, self.N, self.K
         if self.fp8_backward:
             self._saved = (x, w)   # the hybrid backward re-quantizes the bf16 tensors
+        wf = abi.MXFP4_QUANT_2D_BLOCKS if self.weight_2d else 0
         if self.train and not self.fp8_backward:
             tasks = [(x, M, K, x.stride(0), *self.x_row, *self.x_col),
-                     (w, N, K, w.stride(0), *self.w_row, *self.w_col)]
+                     (w, N, K, w.stride(0), *self.w_row, *self.w_col, wf)]
         else:
             tasks = [(x, M, K, x.stride(0), *self.x_row, None, None),
-                     (w, N, K, w.stride(0), *self.w_row, None, None)]
+                     (w, N, K, w.stride(0), *self.w_row, None, None, wf)]
         abi.mxfp4_quantize_batch(tasks, self.train and not self.fp8_backward, abi.MXFP4_SCALE_TC, stream)
 
     def forward(self, x, w, stream=None, bias=None):

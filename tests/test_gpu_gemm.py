@@ -345,3 +345,26 @@ def test_repeated_steps_are_bit_identical(backward):
         for a, b in zip(outs, first):
             assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_tiny_step_with_2d_weight_blocks(out_dtype):
+    # The layer with the weight recipe (32 x 32 blocks for W in both packings): forward and
+    # dgrad read W's 2-D blobs, wgrad is unchanged; every GEMM against the oracle's GEMM over
+    # the oracle's 2-D blobs.
+    wl = workloads.TINY
+    lin = wl.linears[0]
+    t = wl.tensors(0)
+    layer = MXFP4Linear(lin.M, lin.N, lin.K, train=True, out_dtype=out_dtype, weight_2d=True)
+    y, dx, dw = layer.step(t["X"].cuda(), t["W"].cuda(), t["dY"].cuda())
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    xb, wb, dyb = (workloads.bf16_bits(t[k]) for k in ("X", "W", "dY"))
+    X, DY = oracle.quantize_dual(xb), oracle.quantize_dual(dyb)
+    wr, wc = oracle.quantize_row_2d(wb), oracle.quantize_col_2d(wb)
+    c, cabs = oracle.gemm(X[0], X[1], *wr)
+    check_gemm(y, c, cabs, "tiny fwd, 2-D W")
+    c, cabs = oracle.gemm(DY[0], DY[1], *wc)
+    check_gemm(dx, c, cabs, "tiny dgrad, 2-D W")
+    c, cabs = oracle.gemm(DY[2], DY[3], X[2], X[3])
+    check_gemm(dw, c, cabs, "tiny wgrad")

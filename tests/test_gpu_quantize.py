@@ -311,3 +311,97 @@ def test_sr_flux_dy_sampled():
     cq, cs = oracle.quantize_col_sr(np.ascontiguousarray(xb[:, cols]), seed, col_ids=cols)
     assert_bytes_equal(outs[2][torch.as_tensor(cols, device="cuda")].cpu().numpy(), cq, "sr dY col q")
     assert_bytes_equal(gather_tc_rows(outs[3].cpu().numpy(), cols, cs.shape[1]), cs, "sr dY col s")
+
+
+# --- 2-D (32 x 32) block scales (the weight recipe of `_quantize_weight_dual`) -----------
+
+def check_2d_full(x_cpu, outs, layout, dual, what):
+    xb = workloads.bf16_bits(x_cpu)
+    rq, rs = oracle.quantize_row_2d(xb)
+    tc = layout == abi.MXFP4_SCALE_TC
+    assert_bytes_equal(outs[0].cpu().numpy(), rq, f"{what} row q")
+    assert_bytes_equal(outs[1].cpu().numpy().reshape(-1), (oracle.scale_to_tc(rs) if tc else rs).reshape(-1),
+                       f"{what} row s")
+    if dual:
+        cq, cs = oracle.quantize_col_2d(xb)
+        assert_bytes_equal(outs[2].cpu().numpy(), cq, f"{what} col q")
+        assert_bytes_equal(outs[3].cpu().numpy().reshape(-1), (oracle.scale_to_tc(cs) if tc else cs).reshape(-1),
+                           f"{what} col s")
+
+
+def quant_2d(x_cpu, dual, layout, ldx=None):
+    M, K = x_cpu.shape
+    if ldx is not None and ldx != K:
+        wide = torch.zeros((M, ldx), dtype=torch.bfloat16)
+        wide[:, :K] = x_cpu
+        xg = wide.cuda()[:, :K]
+    else:
+        xg = x_cpu.cuda()
+    outs = abi.quantize(xg, dual=dual, layout=layout, block_2d=True)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    return outs
+
+
+@pytest.mark.parametrize("M,K,ldx", [(1, 8, 8), (32, 32, 32), (33, 40, 40), (100, 40, 40), (130, 200, 200),
+                                     (257, 33, 40), (256, 512, 520), (129, 129, 136), (640, 384, 384),
+                                     (4600, 256, 256)])
+def test_2d_blocks_ragged_shapes(M, K, ldx):
+    # Every byte of both blobs (and of the row-only blob) equals the oracle's 2-D block
+    # quantization, edge blocks and ragged 32 x 32 blocks at the right and bottom included.
+    x = _edge_input(M, K, 5 * M + K)
+    for layout in LAYOUTS:
+        check_2d_full(x, quant_2d(x, True, layout, ldx), layout, True, f"2d dual {M}x{K}")
+        check_2d_full(x, quant_2d(x, False, layout, ldx), layout, False, f"2d row {M}x{K}")
+
+
+def test_2d_blocks_every_finite_bf16_pattern():
+    b = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    b = np.where((b & 0x7F80) != 0x7F80, b, 0).astype(np.uint16)
+    rng = np.random.default_rng(9)
+    b = b[rng.permutation(b.size)].reshape(256, 256)
+    x = _bits_to_bf16(b)
+    for layout in LAYOUTS:
+        check_2d_full(x, quant_2d(x, True, layout), layout, True, "2d all bf16 patterns")
+
+
+def test_2d_blocks_mixed_batch_equals_single_calls():
+    # X with 1 x 32 blocks and W with 32 x 32 blocks in one launch (the layer's forward
+    # quantization with the weight recipe) give the bytes of their own calls.
+    x = _edge_input(300, 200, 41)
+    w = _edge_input(520, 200, 43)
+    sx = quant(x, True, abi.MXFP4_SCALE_TC)
+    sw = quant_2d(w, True, abi.MXFP4_SCALE_TC)
+    bx = [abi.alloc_blob(300, 200), abi.alloc_blob(200, 300)]
+    bw = [abi.alloc_blob(520, 200), abi.alloc_blob(200, 520)]
+    xg, wg = x.cuda(), w.cuda()
+    abi.mxfp4_quantize_batch([(xg, 300, 200, 200, *bx[0], *bx[1], 0),
+                              (wg, 520, 200, 200, *bw[0], *bw[1], abi.MXFP4_QUANT_2D_BLOCKS)], True)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    for got, want in zip([*bx[0], *bx[1]], sx):
+        assert torch.equal(got.cpu(), want.cpu())
+    for got, want in zip([*bw[0], *bw[1]], sw):
+        assert torch.equal(got.cpu(), want.cpu())
+
+
+@pytest.mark.parametrize("li", [0, 1])
+def test_2d_blocks_flux_weights_sampled(li):
+    # The single-stream block's weights W1 [21504, 3072] and W2 [3072, 15360]: whole 32-row
+    # bands (row blob) and 32-column bands (col blob) quantized by the oracle at their true
+    # positions.
+    w = workloads.FLUX_SINGLE_BLOCK.tensors(li)["W"]
+    outs = quant_2d(w, True, abi.MXFP4_SCALE_TC)
+    wb = workloads.bf16_bits(w)
+    N, K = wb.shape
+    from parity import gather_tc_rows
+    for band in (0, (N // 32) // 2, N // 32 - 1):
+        rows = np.arange(32 * band, min(N, 32 * band + 32))
+        rq, rs = oracle.quantize_row_2d(np.ascontiguousarray(wb[rows]))
+        assert_bytes_equal(outs[0][torch.as_tensor(rows, device="cuda")].cpu().numpy(), rq, f"W{li + 1} 2d row q")
+        assert_bytes_equal(gather_tc_rows(outs[1].cpu().numpy(), rows, rs.shape[1]), rs, f"W{li + 1} 2d row s")
+    for band in (0, (K // 32) // 2, K // 32 - 1):
+        cols = np.arange(32 * band, min(K, 32 * band + 32))
+        cq, cs = oracle.quantize_col_2d(np.ascontiguousarray(wb[:, cols]))
+        assert_bytes_equal(outs[2][torch.as_tensor(cols, device="cuda")].cpu().numpy(), cq, f"W{li + 1} 2d col q")
+        assert_bytes_equal(gather_tc_rows(outs[3].cpu().numpy(), cols, cs.shape[1]), cs, f"W{li + 1} 2d col s")
