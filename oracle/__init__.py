@@ -74,6 +74,10 @@ def _load():
         for fn in (lib.oracle_quantize_row_sr, lib.oracle_quantize_col_sr):
             fn.argtypes = [vp, i64, i64, i64, vp, vp, ctypes.c_uint64, vp]
             fn.restype = ctypes.c_int
+        lib.oracle_rht16.argtypes = [vp, ctypes.c_uint32]
+        lib.oracle_rht16.restype = None
+        lib.oracle_quantize_col_rht.argtypes = [vp, i64, i64, i64, ctypes.c_uint32, vp, vp]
+        lib.oracle_quantize_col_rht.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -366,4 +370,25 @@ def quantize_col_2d(x_bits):
     s = np.empty((K, Mp // BLOCK), np.uint8)
     if _load().oracle_quantize_col_2d(_ptr(x_bits), M, K, K, _ptr(q), _ptr(s)):
         raise ValueError("non-finite input")
+    return q, s
+
+
+# --- Hadamard transform of the column blobs (`colwise_use_rht`) -------------------------
+
+def rht16(v, signs):
+    """The 16-point transform (1/4) H16 diag(s) of 16 values, in fp32 (returns float32)."""
+    a = np.ascontiguousarray(np.asarray(v, dtype=np.float32).reshape(16)).copy()
+    _load().oracle_rht16(_ptr(a), int(signs) & 0xFFFF)
+    return a
+
+
+def quantize_col_rht(x_bits, signs):
+    """Col blob of X[M,K] with the 16-point transform applied along M (plain scale layout)."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    Mp = padded(M)
+    q = np.empty((K, Mp // 2), np.uint8)
+    s = np.empty((K, Mp // BLOCK), np.uint8)
+    if _load().oracle_quantize_col_rht(_ptr(x_bits), M, K, K, int(signs) & 0xFFFF, _ptr(q), _ptr(s)):
+        raise ValueError("non-finite input or transform")
     return q, s

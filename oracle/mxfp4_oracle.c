@@ -559,3 +559,64 @@ int oracle_quantize_col_2d(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
     free(s2d);
     return 0;
 }
+
+/* ---------------------------------------------------------------------------------------
+ * Hadamard transform of the column blobs: `_quantize_input_dual` and `_quantize_grad_dual`
+ * in primus_turbo_mxfp4_local.py set `colwise_use_rht` for activations and gradients (the
+ * weights use 2-D blocks instead).  Those column blobs are exactly the two operands of the
+ * wgrad GEMM dW = dY^T . X, whose reduction runs over M.  The pages name the flag only;
+ * reading taken (each point listed in the design notes as well):
+ *   - T = (1/4) H16 diag(s) is applied to every group of 16 consecutive elements of a
+ *     zero-padded column of X (rows 16g .. 16g + 15, g = 0 .. Mp/16 - 1), H16 the Sylvester
+ *     Hadamard matrix (H[i][j] = (-1)^popcount(i & j)) and s a sign vector given by the
+ *     caller as a 16-bit mask (bit j set: s_j = -1), the same for every group, both
+ *     operands of a GEMM and every tensor of a step.  T^T T = I exactly (1/4 is a power of
+ *     two), so (T dY)^T (T X) = dY^T X in exact arithmetic.
+ *   - Order of the arithmetic, in fp32 with round-to-nearest-even at every step: each
+ *     element is converted from bf16 (exact) and its sign flipped by s (exact); then the
+ *     Walsh-Hadamard butterflies for h = 1, 2, 4, 8 in turn, each pair (j, j + h) with bit h
+ *     of j clear becoming (v_j + v_{j+h}, v_j - v_{j+h}); then a multiplication by 0.25.
+ *   - The 32-element MX blocks of the transformed column (two groups each) are quantized by
+ *     the 1 x 32 rule above from these fp32 values.  Padding positions (rows M .. Mp - 1)
+ *     are quantized from their transformed values too: a group that straddles M spreads its
+ *     zeros, and keeping them makes the wgrad sum over all Mp positions equal the sum over
+ *     the M real ones.
+ *   - The transformed values must be finite (|x| < 2^124 is enough); otherwise the
+ *     quantizer returns -1.
+ * -------------------------------------------------------------------------------------- */
+
+/* The 16-point transform of v, in place (order and precision as described above). */
+void oracle_rht16(float v[16], uint32_t signs) {
+    for (int j = 0; j < 16; ++j)
+        if ((signs >> j) & 1u) v[j] = -v[j];
+    for (int h = 1; h < 16; h <<= 1)
+        for (int j = 0; j < 16; ++j)
+            if (!(j & h)) {
+                float a = v[j], b = v[j + h];
+                v[j] = a + b;
+                v[j + h] = a - b;
+            }
+    for (int j = 0; j < 16; ++j) v[j] = v[j] * 0.25f;
+}
+
+/* Col blob of X[M,K] with the transform applied along M; layout as oracle_quantize_col. */
+int oracle_quantize_col_rht(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint32_t signs, uint8_t* q,
+                            uint8_t* s) {
+    int64_t Mp = cdiv64(M, PAD) * PAD, MBp = Mp / BLOCK;
+    float* col = (float*)malloc((size_t)Mp * sizeof(float));
+    if (!col) return -2;
+    for (int64_t k = 0; k < K; ++k) {
+        for (int64_t m = 0; m < Mp; ++m) col[m] = (m < M) ? (float)oracle_bf16_to_f64(x[m * ldx + k]) : 0.0f;
+        for (int64_t g = 0; g < Mp / 16; ++g) oracle_rht16(col + 16 * g, signs);
+        for (int64_t mb = 0; mb < MBp; ++mb) {
+            double v[BLOCK];
+            for (int i = 0; i < BLOCK; ++i) v[i] = (double)col[mb * BLOCK + i];
+            if (quantize_block(v, q + k * (Mp / 2) + mb * (BLOCK / 2), &s[k * MBp + mb])) {
+                free(col);
+                return -1;
+            }
+        }
+    }
+    free(col);
+    return 0;
+}

@@ -673,3 +673,144 @@ def test_scale_to_tc_atom_in_copy_order():
     for piece, (r0, k0) in enumerate([(0, 0), (0, 4), (128, 0), (128, 4)]):
         assert out[512 * piece:512 * (piece + 1)].tolist() == oracle.scale_to_tc(
             np.ascontiguousarray(s2[r0:r0 + 128, k0:k0 + 4])).tolist()
+
+
+# --- Hadamard transform of the column blobs (`colwise_use_rht`) -------------------------
+
+def _sylvester16():
+    """H16 from its definition, H[i][j] = (-1)^popcount(i & j)."""
+    i = np.arange(16)
+    pc = np.array([[bin(a & b).count("1") for b in i] for a in i])
+    return np.where(pc % 2 == 0, 1.0, -1.0)
+
+
+def _sign_vector(mask):
+    return np.array([-1.0 if (mask >> j) & 1 else 1.0 for j in range(16)])
+
+
+SIGN_MASKS = (0x0000, 0xFFFF, 0x8001, 0xA5C3, 0x1234)
+
+
+@pytest.mark.parametrize("mask", SIGN_MASKS)
+def test_rht16_columns_are_the_scaled_signed_hadamard(mask):
+    # Transforming basis vector e_j gives column j of (1/4) H16 diag(s): every entry of the
+    # matrix is checked against the definition of H16 and of the sign mask.
+    H, sv = _sylvester16(), _sign_vector(mask)
+    for j in range(16):
+        e = np.zeros(16)
+        e[j] = 1.0
+        got = oracle.rht16(e, mask).astype(np.float64)
+        assert np.array_equal(got, 0.25 * H[:, j] * sv[j]), j
+
+
+@pytest.mark.parametrize("mask", SIGN_MASKS)
+def test_rht16_equals_the_matrix_product_on_exact_inputs(mask):
+    # Small integers keep every butterfly sum exact in fp32: the result is exactly
+    # (1/4) H16 (s * x) computed in fp64.
+    rng = np.random.default_rng(mask)
+    H, sv = _sylvester16(), _sign_vector(mask)
+    for _ in range(50):
+        x = rng.integers(-64, 65, 16).astype(np.float64)
+        assert np.array_equal(oracle.rht16(x, mask).astype(np.float64), 0.25 * H @ (sv * x))
+
+
+def test_rht16_is_orthogonal_on_exact_inputs():
+    # (Ta).(Tb) = a.b and T^T (T a) = a: the wgrad product is unchanged by transforming both
+    # operands.
+    rng = np.random.default_rng(3)
+    H, sv = _sylvester16(), _sign_vector(0xA5C3)
+    T = 0.25 * H * sv[None, :]
+    assert np.array_equal(T.T @ T, np.eye(16))
+    for _ in range(50):
+        a = rng.integers(-32, 33, 16).astype(np.float64)
+        b = rng.integers(-32, 33, 16).astype(np.float64)
+        ta = oracle.rht16(a, 0xA5C3).astype(np.float64)
+        tb = oracle.rht16(b, 0xA5C3).astype(np.float64)
+        assert float(ta @ tb) == float(a @ b)
+        assert np.array_equal(T.T @ ta, a)
+
+
+def test_rht16_rounding_stays_within_the_fp32_bound():
+    # General bf16 inputs over many binades: four butterfly levels of fp32 rounding, each at
+    # most half an fp32 ulp of a partial sum bounded by sum |x|.
+    rng = np.random.default_rng(11)
+    H = _sylvester16()
+    for mask in SIGN_MASKS:
+        sv = _sign_vector(mask)
+        for _ in range(200):
+            bits = (rng.integers(0, 2, 16) << 15) | (rng.integers(90, 160, 16) << 7) | rng.integers(0, 128, 16)
+            x = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            got = oracle.rht16(x, mask).astype(np.float64)
+            exact = 0.25 * H @ (sv * x)
+            bound = 0.25 * 4 * 2.0 ** -24 * np.sum(np.abs(x))
+            assert np.all(np.abs(got - exact) <= bound)
+
+
+E2M1_GRID = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+
+
+def _preimage_column(rng, mask, nblocks):
+    """A column x (bf16-exact) whose transform y = T x is, block by block, E2M1 grid values
+    times 2^e with a 4 or 6 present: y = T x exactly, and the expected MX codes and scale
+    bytes of y follow from the OCP rule by hand."""
+    H, sv = _sylvester16(), _sign_vector(mask)
+    ys, codes, scales = [], [], []
+    for _ in range(nblocks):
+        e = int(rng.integers(-10, 11))
+        idx = rng.integers(0, 8, 32)
+        idx[rng.integers(0, 32)] = rng.choice([6, 7])        # amax in [4, 8) * 2^e
+        # a zero of the transform is a sum like a + (-a), which is +0 under round-to-nearest
+        sign = np.where(idx == 0, 0, rng.integers(0, 2, 32))
+        y = np.where(sign == 1, -1.0, 1.0) * E2M1_GRID[idx] * 2.0 ** e
+        ys.append(y)
+        codes.append((sign << 3) | idx)
+        scales.append(e + 127)
+    y = np.concatenate(ys)
+    x = np.concatenate([0.25 * sv * (H @ y[16 * g:16 * g + 16]) for g in range(len(y) // 16)])   # T^T y
+    return x, np.concatenate(codes), np.array(scales)
+
+
+@pytest.mark.parametrize("mask", SIGN_MASKS)
+def test_quantize_col_rht_codes_of_transform_preimages(mask):
+    # X's columns are chosen so that their transforms are exactly MX-representable: the col
+    # blob must hold exactly those codes (sign of the grid value, then its index) and scale
+    # bytes (e + 127), for every column of a [128, 6] tensor.
+    rng = np.random.default_rng(100 + mask)
+    M, K = 128, 6
+    X = np.zeros((M, K))
+    want_codes, want_scales = [], []
+    for k in range(K):
+        x, c, s = _preimage_column(rng, mask, M // 32)
+        X[:, k] = x
+        want_codes.append(c)
+        want_scales.append(s)
+    bits = (X.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64), X)   # bf16-exact
+    q, s = oracle.quantize_col_rht(bits, mask)
+    for k in range(K):
+        codes = np.empty(M, np.uint8)
+        codes[0::2], codes[1::2] = q[k] & 0xF, q[k] >> 4
+        assert np.array_equal(codes, want_codes[k]), k
+        assert np.array_equal(s[k], want_scales[k]), k
+
+
+def test_quantize_col_rht_padding_and_wgrad_sum():
+    # M = 40: the group of rows 32..47 straddles M, later groups are all padding.  Padding
+    # blocks past the last straddling group are zero codes with scale 0x00; over the whole
+    # padded length the transformed columns keep the exact inner product of the real rows.
+    rng = np.random.default_rng(5)
+    M, K = 40, 3
+    a = rng.integers(-8, 9, (M, K)).astype(np.float32)
+    b = rng.integers(-8, 9, (M, K)).astype(np.float32)
+    bits = lambda v: (v.view(np.uint32) >> 16).astype(np.uint16)
+    q, s = oracle.quantize_col_rht(bits(a), 0x5A5A)
+    assert q.shape == (K, 64) and s.shape == (K, 4)
+    assert np.all(q[:, 24:] == 0) and np.all(s[:, 2:] == 0)        # rows 48..127
+    for k in range(K):
+        pa = np.zeros(128, np.float32)
+        pb = np.zeros(128, np.float32)
+        pa[:M], pb[:M] = a[:, k], b[:, k]
+        ta = np.concatenate([oracle.rht16(pa[16 * g:16 * g + 16], 0x5A5A) for g in range(8)]).astype(np.float64)
+        tb = np.concatenate([oracle.rht16(pb[16 * g:16 * g + 16], 0x5A5A) for g in range(8)]).astype(np.float64)
+        assert np.any(ta[M:48] != 0)                          # the straddling group spreads
+        assert float(ta @ tb) == float(a[:, k].astype(np.float64) @ b[:, k].astype(np.float64))
