@@ -130,12 +130,34 @@ mxfp4_status mxfp4_quantize_dual_2d(const void* x, int64_t M, int64_t K, int64_t
                                     void* q_row, void* s_row, void* q_col, void* s_col,
                                     mxfp4_scale_layout layout, mxfp4_stream_t stream);
 
+/* Dual quantizer with the Hadamard transform of the column blob: the activation and
+ * gradient quantization of `_quantize_input_dual` / `_quantize_grad_dual` in
+ * primus_turbo_mxfp4_local.py with `colwise_use_rht` set (every other recipe flag off).
+ * The pages name the flag only; what it computes here: the row blob exactly as
+ * mxfp4_quantize_dual; for the col blob, every group of 16 consecutive elements along M of
+ * a zero-padded column of X (rows 16g .. 16g + 15 up to Mp) becomes T x with
+ * T = (1/4) H16 diag(s) -- H16 the Sylvester Hadamard matrix, H[i][j] = (-1)^popcount(i & j),
+ * s_j = -1 where bit j of `signs` is set -- computed in fp32 with round-to-nearest-even:
+ * signs applied, butterflies (v_j, v_j+h) -> (v_j + v_j+h, v_j - v_j+h) for h = 1, 2, 4, 8
+ * in turn, then x 0.25; each 32-element block of the transformed column is quantized by
+ * the rule above from those fp32 values, padding positions included (a group straddling M
+ * spreads its zeros; keeping them makes a GEMM over all Mp positions exact).  T^T T = I,
+ * so dW = dY^T . X is unchanged in exact arithmetic when both col blobs use the same
+ * signs.  Transformed values must be finite (|x| < 2^124 suffices).  Arguments, layouts
+ * and errors as mxfp4_quantize_dual; signs: bits 0..15. */
+mxfp4_status mxfp4_quantize_dual_rht(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                     void* q_row, void* s_row, void* q_col, void* s_col,
+                                     mxfp4_scale_layout layout, uint32_t signs,
+                                     mxfp4_stream_t stream);
+
 /* Bits of mxfp4_quantize_task::flags. */
 #define MXFP4_QUANT_2D_BLOCKS 1   /* 32 x 32 blocks, as mxfp4_quantize_dual_2d (row-only too) */
+#define MXFP4_QUANT_RHT_COL 2     /* col blob transformed, as mxfp4_quantize_dual_rht (dual only) */
 
 /* One tensor of a batched quantization: bf16 x[rows, k] with row pitch ldx elements and
  * its output buffers, as for mxfp4_quantize / mxfp4_quantize_dual (q_col and s_col are
- * read only for the dual quantizer); flags: 0 or MXFP4_QUANT_2D_BLOCKS. */
+ * read only for the dual quantizer); flags: 0, MXFP4_QUANT_2D_BLOCKS or
+ * MXFP4_QUANT_RHT_COL (not both); rht_signs: the sign mask of MXFP4_QUANT_RHT_COL. */
 typedef struct {
     const void* x;
     int64_t rows;
@@ -146,13 +168,14 @@ typedef struct {
     void* q_col;
     void* s_col;
     int32_t flags;
+    uint32_t rht_signs;
 } mxfp4_quantize_task;
 
 #define MXFP4_MAX_BATCH 4
 
 /* Quantizes 1..MXFP4_MAX_BATCH independent tensors in one launch, each with exactly the
- * output of mxfp4_quantize (dual == 0) or mxfp4_quantize_dual (dual != 0), or with 2-D
- * blocks (task flag MXFP4_QUANT_2D_BLOCKS) that of mxfp4_quantize_dual_2d.  Same
+ * output of mxfp4_quantize (dual == 0) or mxfp4_quantize_dual (dual != 0), or with a task
+ * flag that of mxfp4_quantize_dual_2d / mxfp4_quantize_dual_rht.  Same
  * operation as those two (the per-tensor `quantize_mxfp4` / `_quantize_mxfp4_dual_op`
  * calls of primus_turbo_mxfp4_local.py); one launch lets a small tensor share the GPU with
  * a large one instead of paying its own ramp-up and tail (the forward step quantizes X and

@@ -41,10 +41,12 @@ class QuantizeTask(ctypes.Structure):
     """mxfp4_quantize_task of include/mxfp4.h."""
     _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("k", ctypes.c_int64),
                 ("ldx", ctypes.c_int64), ("q_row", ctypes.c_void_p), ("s_row", ctypes.c_void_p),
-                ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p), ("flags", ctypes.c_int32)]
+                ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p), ("flags", ctypes.c_int32),
+                ("rht_signs", ctypes.c_uint32)]
 
 
 MXFP4_QUANT_2D_BLOCKS = 1
+MXFP4_QUANT_RHT_COL = 2
 
 class Fp8QuantizeTask(ctypes.Structure):
     """mxfp4_fp8_quantize_task of include/mxfp4.h."""
@@ -75,6 +77,7 @@ EXPORTED = (
     "mxfp4_quantize_dual",
     "mxfp4_quantize_dual_sr",
     "mxfp4_quantize_dual_2d",
+    "mxfp4_quantize_dual_rht",
     "mxfp4_quantize_batch",
     "mxfp4_gemm",
     "mxfp4_gemm_bias",
@@ -117,6 +120,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_quantize_dual.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, vp]
     lib.mxfp4_quantize_dual_sr.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, ctypes.c_uint64, vp]
     lib.mxfp4_quantize_dual_2d.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, vp]
+    lib.mxfp4_quantize_dual_rht.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, ctypes.c_uint32, vp]
     lib.mxfp4_quantize_batch.argtypes = [i32, ctypes.POINTER(QuantizeTask), i32, i32, vp]
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_gemm_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i32, vp]
@@ -201,15 +205,24 @@ def mxfp4_quantize_dual_2d(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=MXFP
            "mxfp4_quantize_dual_2d")
 
 
+def mxfp4_quantize_dual_rht(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=MXFP4_SCALE_TC,
+                            signs=0, stream=None) -> None:
+    _check(load().mxfp4_quantize_dual_rht(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
+                                          _ptr(s_col), layout, int(signs) & 0xFFFF, _stream(stream)),
+           "mxfp4_quantize_dual_rht")
+
+
 def mxfp4_quantize_batch(tasks, dual: bool, layout=MXFP4_SCALE_TC, stream=None) -> None:
-    """tasks: sequence of (x, rows, k, ldx, q_row, s_row, q_col, s_col[, flags]); q_col /
-    s_col may be None for the row-only quantizer; flags 0 or MXFP4_QUANT_2D_BLOCKS."""
+    """tasks: sequence of (x, rows, k, ldx, q_row, s_row, q_col, s_col[, flags[, rht_signs]]);
+    q_col / s_col may be None for the row-only quantizer; flags 0, MXFP4_QUANT_2D_BLOCKS or
+    MXFP4_QUANT_RHT_COL."""
     arr = (QuantizeTask * max(1, len(tasks)))()
     for i, t in enumerate(tasks):
         x, rows, k, ldx, q_row, s_row, q_col, s_col = t[:8]
         flags = t[8] if len(t) > 8 else 0
+        signs = t[9] if len(t) > 9 else 0
         arr[i] = QuantizeTask(_ptr(x), rows, k, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
-                              _ptr(s_col), flags)
+                              _ptr(s_col), flags, int(signs) & 0xFFFF)
     _check(load().mxfp4_quantize_batch(len(tasks), arr, int(bool(dual)), layout, _stream(stream)),
            "mxfp4_quantize_batch")
 
@@ -319,14 +332,20 @@ def alloc_blob(rows: int, k: int, layout: int = MXFP4_SCALE_TC, device="cuda"):
 
 
 def quantize(x, dual: bool = True, layout: int = MXFP4_SCALE_TC, stream=None, sr_seed=None,
-             block_2d: bool = False):
+             block_2d: bool = False, rht_signs=None):
     """bf16 X[M,K] (CUDA, row pitch a multiple of 8) -> (row_q, row_s[, col_q, col_s]);
     with sr_seed (dual only) the elements are stochastically rounded; with block_2d the
-    scales are those of 32 x 32 blocks."""
+    scales are those of 32 x 32 blocks; with rht_signs (dual only) the col blob is that of
+    the Hadamard-transformed columns."""
     import torch
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     rq, rs = alloc_blob(M, K, layout, x.device)
+    if rht_signs is not None:
+        assert dual and sr_seed is None and not block_2d
+        cq, cs = alloc_blob(K, M, layout, x.device)
+        mxfp4_quantize_dual_rht(x, M, K, x.stride(0), rq, rs, cq, cs, layout, rht_signs, stream)
+        return rq, rs, cq, cs
     if block_2d:
         assert sr_seed is None, "the 2-D block recipe is for weights, stochastic rounding for gradients"
         if not dual:

@@ -98,7 +98,7 @@ mxfp4_status quantize_check(const void* x, int64_t M, int64_t K, int64_t ldx, co
 // Fills slot j of the batch (tensor map and arguments) for a checked task.
 mxfp4_status quantize_task(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* s_row,
                            void* q_col, void* s_col, mxfp4_scale_layout layout, DeviceState* dev,
-                           mxfp4::QuantBatch* b, int j, int32_t flags = 0) {
+                           mxfp4::QuantBatch* b, int j, int32_t flags = 0, uint32_t rht_signs = 0) {
     if (!encode_2d(&b->maps[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(K),
                    static_cast<uint64_t>(M), static_cast<uint64_t>(ldx) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return MXFP4_ERR_CUDA;
@@ -118,6 +118,8 @@ mxfp4_status quantize_task(const void* x, int64_t M, int64_t K, int64_t ldx, voi
     a.tc_layout = layout == MXFP4_SCALE_TC ? 1 : 0;
     a.seed = 0;
     a.block_2d = (flags & MXFP4_QUANT_2D_BLOCKS) ? 1 : 0;
+    a.rht = (flags & MXFP4_QUANT_RHT_COL) ? 1 : 0;
+    a.rht_signs = rht_signs & 0xFFFFu;
     a.err = dev->err;
     const int64_t before = j > 0 ? b->tile_end[j - 1] : 0;
     const int64_t end = before + static_cast<int64_t>(a.tiles_m) * a.tiles_k;
@@ -137,7 +139,8 @@ mxfp4_status launch_batch(const mxfp4::QuantBatch& b, bool dual, DeviceState* de
 
 mxfp4_status quantize_common(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* s_row,
                              void* q_col, void* s_col, mxfp4_scale_layout layout, bool dual,
-                             cudaStream_t stream, bool sr = false, uint64_t seed = 0, int32_t flags = 0) {
+                             cudaStream_t stream, bool sr = false, uint64_t seed = 0, int32_t flags = 0,
+                             uint32_t rht_signs = 0) {
     mxfp4_status st = quantize_check(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, dual);
     if (st != MXFP4_OK) return st;
     DeviceState* dev = nullptr;
@@ -145,7 +148,7 @@ mxfp4_status quantize_common(const void* x, int64_t M, int64_t K, int64_t ldx, v
     if (st != MXFP4_OK) return st;
     mxfp4::QuantBatch b;
     std::memset(&b, 0, sizeof(b));
-    st = quantize_task(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, dev, &b, 0, flags);
+    st = quantize_task(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, dev, &b, 0, flags, rht_signs);
     if (st != MXFP4_OK) return st;
     b.args[0].seed = seed;
     return launch_batch(b, dual, dev, stream, sr);
@@ -348,6 +351,13 @@ mxfp4_status mxfp4_quantize_dual_2d(const void* x, int64_t M, int64_t K, int64_t
                            reinterpret_cast<cudaStream_t>(stream), false, 0, MXFP4_QUANT_2D_BLOCKS);
 }
 
+mxfp4_status mxfp4_quantize_dual_rht(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row, void* s_row,
+                                     void* q_col, void* s_col, mxfp4_scale_layout layout, uint32_t signs,
+                                     mxfp4_stream_t stream) {
+    return quantize_common(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, true,
+                           reinterpret_cast<cudaStream_t>(stream), false, 0, MXFP4_QUANT_RHT_COL, signs);
+}
+
 mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* tasks, int32_t dual,
                                   mxfp4_scale_layout layout, mxfp4_stream_t stream) {
     if (count < 1 || count > MXFP4_MAX_BATCH || tasks == nullptr) return MXFP4_ERR_INVALID_ARG;
@@ -357,7 +367,9 @@ mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* task
         const mxfp4_status st = quantize_check(t.x, t.rows, t.k, t.ldx, t.q_row, t.s_row, t.q_col, t.s_col,
                                                layout, d);
         if (st != MXFP4_OK) return st;
-        if ((t.flags & ~MXFP4_QUANT_2D_BLOCKS) != 0) return MXFP4_ERR_INVALID_ARG;
+        if ((t.flags & ~(MXFP4_QUANT_2D_BLOCKS | MXFP4_QUANT_RHT_COL)) != 0 ||
+            t.flags == (MXFP4_QUANT_2D_BLOCKS | MXFP4_QUANT_RHT_COL) || ((t.flags & MXFP4_QUANT_RHT_COL) && !d))
+            return MXFP4_ERR_INVALID_ARG;
     }
     DeviceState* dev = nullptr;
     mxfp4_status st = device_ready(&dev);
@@ -367,7 +379,7 @@ mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* task
     for (int j = 0; j < count; ++j) {
         const mxfp4_quantize_task& t = tasks[j];
         st = quantize_task(t.x, t.rows, t.k, t.ldx, t.q_row, t.s_row, t.q_col, t.s_col, layout, dev, &b, j,
-                           t.flags);
+                           t.flags, t.rht_signs);
         if (st != MXFP4_OK) return st;
     }
     return launch_batch(b, d, dev, reinterpret_cast<cudaStream_t>(stream));

@@ -200,8 +200,8 @@ mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task*
         const int64_t ldk = round8(t.K);
         MX_TRY(cudaStreamWaitEvent(comp, ev_xw(i), 0));
         const mxfp4_quantize_task q[2] = {
-            {b.xd, t.M, t.K, ldk, b.xrq, b.xrs, b.xcq, b.xcs, 0},
-            {b.wd, t.N, t.K, ldk, b.wrq, b.wrs, b.wcq, b.wcs, 0},
+            {b.xd, t.M, t.K, ldk, b.xrq, b.xrs, b.xcq, b.xcs, 0, 0},
+            {b.wd, t.N, t.K, ldk, b.wrq, b.wrs, b.wcq, b.wcs, 0, 0},
         };
         MX_TRY_ST(mxfp4_quantize_batch(2, q, t.train, MXFP4_SCALE_TC, stream));
         MX_TRY_ST(mxfp4_gemm(b.xrq, b.xrs, b.wrq, b.wrs, t.M, t.N, t.K, b.y, t.N, t.out_dtype, stream));

@@ -38,6 +38,15 @@
 // block's maximum over the 8 warps, for its row blocks and, in the columnwise pass, for
 // its column pair (both columns lie in one block).  Scale bytes of padding rows of the
 // tensor-core layout stay 0x00, as in the 1-D packings.
+//
+// Hadamard transform of the column blob (the `colwise_use_rht` flag of the activation and
+// gradient quantizers): before the columnwise pass quantizes a column, each group of 16
+// consecutive rows becomes (1/4) H16 diag(s) of itself, s a sign mask of the task, computed
+// in fp32 -- signs, butterflies for h = 1, 2, 4, 8, then x 0.25 -- and the 32-row MX block is
+// quantized from these fp32 values.  The thread's rows sit in its registers in the order
+// r ^ 2rb; butterfly partners are XOR pairs in either order, and where the order swaps which
+// partner is the lower one (h = 2, 4, by the bits of rb) the sum and the difference (taken
+// lower minus upper in row order) land in each other's register.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -267,6 +276,55 @@ __device__ __forceinline__ void encode_cols8_sr(const uint32_t* w, float inv0, f
     *q1 = pack_e2m1x8(f1);
 }
 
+// One column of a 32-row block with the Hadamard transform: kHi picks the column of the
+// column pair (high or low halves of w); register i of w holds row (i & ~7) | ((i & 7) ^ 2rb)
+// and bit (i & 15) of psigns is the sign of that row's position in its 16-row group.  Gives
+// the block's scale byte from the transformed values and the codes, word g byte j holding
+// registers 8g + 2j (low nibble) and 8g + 2j + 1, like encode_cols8.
+template <int kHi>
+__device__ __forceinline__ void rht_column(const uint32_t* w, uint32_t rb, uint32_t psigns, uint32_t* byte,
+                                           uint32_t* q) {
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const float v = kHi ? bf16_hi(w[i]) : bf16_lo(w[i]);
+        f[i] = ((psigns >> (i & 15)) & 1u) ? -v : v;
+    }
+    const bool sw2 = (rb & 1u) != 0, sw4 = ((rb >> 1) & 1u) != 0;
+#pragma unroll
+    for (int g = 0; g < 32; g += 16) {
+#pragma unroll
+        for (int h = 1; h < 16; h <<= 1) {
+            // register order swaps the partners' roles for h = 2 (bit 0 of rb), h = 4 (bit 1)
+            const bool sw = (h == 2 && sw2) || (h == 4 && sw4);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (i & h) continue;
+                // lo / hi: the partners in row order (the difference is taken in that order:
+                // x - x is +0, so negating the other order's difference would give -0)
+                const float lo = sw ? f[g + i + h] : f[g + i], hi = sw ? f[g + i] : f[g + i + h];
+                const float s = __fadd_rn(lo, hi), d = __fsub_rn(lo, hi);
+                f[g + i] = sw ? d : s;
+                f[g + i + h] = sw ? s : d;
+            }
+        }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        f[i] = __fmul_rn(f[i], 0.25f);
+        amax = fmaxf(amax, fabsf(f[i]));
+    }
+    const uint32_t ef = (__float_as_uint(amax) >> 23) & 0xFFu;   // floor(log2) + 127 of a normal amax
+    const uint32_t b = max(ef, 2u) - 2u;
+    *byte = b;
+    const float inv = __uint_as_float(inv_scale_bits(b));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(f[i], inv);
+#pragma unroll
+    for (int gw = 0; gw < 4; ++gw) q[gw] = pack_e2m1x8(&f[8 * gw]);
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
@@ -281,9 +339,9 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     return v;
 }
 
-// k2D: some task of the launch has 2-D blocks (QuantArgs::block_2d); such a task's tiles
-// take the 2-D path, the others the 1-D one.
-template <bool kDual, bool kSR, bool k2D>
+// kRecipes: some task of the launch has 2-D blocks (QuantArgs::block_2d) or the Hadamard
+// transform of its column blob (QuantArgs::rht); such a task's tiles take those paths.
+template <bool kDual, bool kSR, bool kRecipes>
 __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     quantize_kernel(const __grid_constant__ QuantBatch P) {
     extern __shared__ uint8_t smem_raw[];
@@ -367,7 +425,7 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
         //      L = 4w..4w+3 (rows L, L+32, L+64, L+96) and all four block columns, so each
         //      store instruction writes whole 32-byte sectors of 16 rows, and each quarter
         //      warp's 16-byte shared reads hit 8 distinct swizzled chunks.
-        const bool blk2d = k2D && p.block_2d;
+        const bool blk2d = kRecipes && p.block_2d;
         const int L = 4 * warp + (lane & 3);
         const int Q = lane >> 3;
         const int r = Q * 32 + L;
@@ -458,7 +516,24 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
             uint32_t w[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) w[i] = lds32(toff[i & 7] + (i & ~7) * 128);
+            const uint32_t sel = 0x3210u ^ (0x1111u * static_cast<uint32_t>(rb));
+            const int64_t kc = k0 + 2 * pc;
             uint32_t byte0, byte1;
+            uint32_t q0[4], q1[4];
+            if (kRecipes && p.rht) {
+                // sign of register position r of a 16-row group: bit (r & 8) | ((r & 7) ^ 2rb)
+                uint32_t psigns = 0;
+#pragma unroll
+                for (int r2 = 0; r2 < 16; ++r2)
+                    psigns |= ((p.rht_signs >> ((r2 & 8) | ((r2 & 7) ^ (2 * rb)))) & 1u) << r2;
+                rht_column<0>(w, static_cast<uint32_t>(rb), psigns, &byte0, q0);
+                rht_column<1>(w, static_cast<uint32_t>(rb), psigns, &byte1, q1);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    q0[j] = __byte_perm(q0[j], 0, sel);
+                    q1[j] = __byte_perm(q1[j], 0, sel);
+                }
+            } else {
             if (blk2d) {
                 // both columns lie in block column pc / 16 of row group rb
                 uint32_t m = 0;
@@ -473,9 +548,6 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
                 byte1 = scale_byte(m >> 16);
             }
             const uint64_t s2 = pack2(inv_scale_bits(byte0), inv_scale_bits(byte1));
-            const uint32_t sel = 0x3210u ^ (0x1111u * static_cast<uint32_t>(rb));
-            const int64_t kc = k0 + 2 * pc;
-            uint32_t q0[4], q1[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (kSR) {
@@ -490,6 +562,7 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
                 }
                 q0[j] = __byte_perm(q0[j], 0, sel);
                 q1[j] = __byte_perm(q1[j], 0, sel);
+            }
             }
             const int64_t off = (m0 + rb * 32) >> 1;
             if (kc < p.K) {
@@ -523,7 +596,7 @@ cudaError_t launch_quantize(const QuantBatch& b, bool dual, bool sr, int grid, c
     const size_t smem = quantize_smem_bytes();
     if (sr && !dual) return cudaErrorInvalidValue;
     bool b2d = false;
-    for (int j = 0; j < b.count; ++j) b2d = b2d || b.args[j].block_2d != 0;
+    for (int j = 0; j < b.count; ++j) b2d = b2d || b.args[j].block_2d != 0 || b.args[j].rht != 0;
     if (sr && b2d) return cudaErrorInvalidValue;
     auto k = sr    ? quantize_kernel<true, true, false>
              : b2d ? (dual ? quantize_kernel<true, false, true> : quantize_kernel<false, false, true>)

@@ -9,8 +9,10 @@ Follows the dataflow of `MXFP4LinearFunction` in primus_turbo_mxfp4_local.py:
             or, with backward="fp8", the pages' hybrid backward (tensorwise E5M2 of dY,
             X, W and FP8 GEMMs)
 With weight_2d, W is quantized with one scale per 32 x 32 block in both packings (the
-weight recipe of `_quantize_weight_dual`, `rowwise_use_2d_block` / `colwise_use_2d_block`).
-The other recipe flags (Hadamard transform, shuffles) are off.  In the
+weight recipe of `_quantize_weight_dual`, `rowwise_use_2d_block` / `colwise_use_2d_block`);
+with rht_signs, the column blobs of X and dY -- the two wgrad operands -- are those of their
+Hadamard-transformed columns, with the same signs (`colwise_use_rht` of
+`_quantize_input_dual` / `_quantize_grad_dual`).  The shuffle flags are off.  In the
 MXFP4 backward only the column blobs of X and W live from forward to backward; bf16 X
 and W are not kept.  All buffers are allocated once (torch as the allocator) and reused,
 so an MXFP4 step is four launches on one stream: X and W quantized together, the forward
@@ -29,10 +31,13 @@ class MXFP4Linear:
     column blobs would only feed an MXFP4 backward."""
 
     def __init__(self, M: int, N: int, K: int, train: bool = True, device="cuda",
-                 out_dtype=torch.bfloat16, backward: str = "mxfp4", weight_2d: bool = False):
+                 out_dtype=torch.bfloat16, backward: str = "mxfp4", weight_2d: bool = False,
+                 rht_signs=None):
         assert backward in ("mxfp4", "fp8")
         self.M, self.N, self.K, self.train = M, N, K, train
         self.weight_2d = weight_2d
+        self.rht_signs = rht_signs
+        assert rht_signs is None or backward == "mxfp4", "the transform belongs to the MXFP4 wgrad"
         self.fp8_backward = train and backward == "fp8"
         L = abi.MXFP4_SCALE_TC
         self.x_row = abi.alloc_blob(M, K, L, device)
@@ -59,7 +64,10 @@ class MXFP4Linear:
     # -- steps a1..a4 of the path ---------------------------------------------------------
     def quantize_x(self, x, stream=None):
         M, K = self.M, self.K
-        if self.train:
+        if self.train and self.rht_signs is not None:
+            abi.mxfp4_quantize_dual_rht(x, M, K, x.stride(0), *self.x_row, *self.x_col,
+                                        abi.MXFP4_SCALE_TC, self.rht_signs, stream)
+        elif self.train:
             abi.mxfp4_quantize_dual(x, M, K, x.stride(0), *self.x_row, *self.x_col,
                                     abi.MXFP4_SCALE_TC, stream)
         else:
@@ -77,8 +85,13 @@ class MXFP4Linear:
 
     def quantize_dy(self, dy, stream=None, sr_seed=None):
         """dY's two blobs; with sr_seed, stochastically rounded (the gradient quantizer's
-        `use_sr`, the layer's `mxfp4_gradient_stochastic_rounding` option)."""
-        if sr_seed is None:
+        `use_sr`, the layer's `mxfp4_gradient_stochastic_rounding` option); with the layer's
+        rht_signs, the col blob of the transformed columns."""
+        if self.rht_signs is not None:
+            assert sr_seed is None, "stochastic rounding and the transform are not combined"
+            abi.mxfp4_quantize_dual_rht(dy, self.M, self.N, dy.stride(0), *self.dy_row, *self.dy_col,
+                                        abi.MXFP4_SCALE_TC, self.rht_signs, stream)
+        elif sr_seed is None:
             abi.mxfp4_quantize_dual(dy, self.M, self.N, dy.stride(0), *self.dy_row, *self.dy_col,
                                     abi.MXFP4_SCALE_TC, stream)
         else:
@@ -117,7 +130,8 @@ class MXFP4Linear:
             self._saved = (x, w)   # the hybrid backward re-quantizes the bf16 tensors
         wf = abi.MXFP4_QUANT_2D_BLOCKS if self.weight_2d else 0
         if self.train and not self.fp8_backward:
-            tasks = [(x, M, K, x.stride(0), *self.x_row, *self.x_col),
+            xf = abi.MXFP4_QUANT_RHT_COL if self.rht_signs is not None else 0
+            tasks = [(x, M, K, x.stride(0), *self.x_row, *self.x_col, xf, self.rht_signs or 0),
                      (w, N, K, w.stride(0), *self.w_row, *self.w_col, wf)]
         else:
             tasks = [(x, M, K, x.stride(0), *self.x_row, None, None),

@@ -405,3 +405,91 @@ def test_2d_blocks_flux_weights_sampled(li):
         cq, cs = oracle.quantize_col_2d(np.ascontiguousarray(wb[:, cols]))
         assert_bytes_equal(outs[2][torch.as_tensor(cols, device="cuda")].cpu().numpy(), cq, f"W{li + 1} 2d col q")
         assert_bytes_equal(gather_tc_rows(outs[3].cpu().numpy(), cols, cs.shape[1]), cs, f"W{li + 1} 2d col s")
+
+
+# --- Hadamard transform of the column blob (`colwise_use_rht`) ---------------------------
+
+RHT_MASKS = (0x0000, 0xA5C3, 0xFFFF, 0x8001)
+
+
+def _rht_input(M, K, seed):
+    """Student-t values with subnormal, mixed and zero blocks (edge kinds), magnitudes kept
+    below 2^100 so that no 16-row sum can overflow."""
+    x = _edge_input(M, K, seed).float()
+    x = torch.where(x.abs() > 2.0 ** 100, x * 2.0 ** -120, x)
+    return x.to(torch.bfloat16)
+
+
+def check_rht_full(x_cpu, outs, layout, signs, what):
+    xb = workloads.bf16_bits(x_cpu)
+    tc = layout == abi.MXFP4_SCALE_TC
+    rq, rs = oracle.quantize_row(xb)
+    assert_bytes_equal(outs[0].cpu().numpy(), rq, f"{what} row q")
+    assert_bytes_equal(outs[1].cpu().numpy().reshape(-1), (oracle.scale_to_tc(rs) if tc else rs).reshape(-1),
+                       f"{what} row s")
+    cq, cs = oracle.quantize_col_rht(xb, signs)
+    assert_bytes_equal(outs[2].cpu().numpy(), cq, f"{what} col q")
+    assert_bytes_equal(outs[3].cpu().numpy().reshape(-1), (oracle.scale_to_tc(cs) if tc else cs).reshape(-1),
+                       f"{what} col s")
+
+
+@pytest.mark.parametrize("M,K,ldx", [(1, 8, 8), (16, 32, 32), (40, 40, 40), (100, 40, 40), (130, 200, 200),
+                                     (257, 33, 40), (256, 512, 520), (640, 384, 384), (4600, 256, 256)])
+@pytest.mark.parametrize("signs", RHT_MASKS)
+def test_rht_ragged_shapes(M, K, ldx, signs):
+    # Row blob as the plain dual quantizer, col blob as the oracle's transformed columns,
+    # byte for byte (groups straddling M included).
+    x = _rht_input(M, K, 3 * M + 5 * K)
+    for layout in LAYOUTS:
+        wide = torch.zeros((M, ldx), dtype=torch.bfloat16)
+        wide[:, :K] = x
+        outs = abi.quantize(wide.cuda()[:, :K], dual=True, layout=layout, rht_signs=signs)
+        torch.cuda.synchronize()
+        assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+        check_rht_full(x, outs, layout, signs, f"rht {M}x{K} signs {signs:#06x}")
+
+
+def test_rht_every_bf16_pattern_below_overflow():
+    b = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    b = np.where((b & 0x7F80) < (200 << 7), b, 0).astype(np.uint16)    # exponent field < 200
+    rng = np.random.default_rng(13)
+    x = _bits_to_bf16(b[rng.permutation(b.size)].reshape(256, 256))
+    for signs in RHT_MASKS:
+        outs = abi.quantize(x.cuda(), dual=True, layout=abi.MXFP4_SCALE_TC, rht_signs=signs)
+        torch.cuda.synchronize()
+        check_rht_full(x, outs, abi.MXFP4_SCALE_TC, signs, f"rht all patterns {signs:#06x}")
+
+
+def test_rht_flux_activation_sampled():
+    # Flux X [4608, 3072] and the GELU-like H [4608, 15360]: whole sampled columns of the col
+    # blob against the oracle's transform of those columns.
+    from parity import gather_tc_rows
+    for li in (0, 1):
+        x = workloads.FLUX_SINGLE_BLOCK.tensors(li)["X"]
+        outs = abi.quantize(x.cuda(), dual=True, layout=abi.MXFP4_SCALE_TC, rht_signs=0xA5C3)
+        torch.cuda.synchronize()
+        xb = workloads.bf16_bits(x)
+        K = xb.shape[1]
+        cols = np.unique(np.concatenate([np.random.default_rng(li).choice(K, 24, replace=False), [0, K - 1]]))
+        cq, cs = oracle.quantize_col_rht(np.ascontiguousarray(xb[:, cols]), 0xA5C3)
+        assert_bytes_equal(outs[2][torch.as_tensor(cols, device="cuda")].cpu().numpy(), cq, f"flux {li} rht col q")
+        assert_bytes_equal(gather_tc_rows(outs[3].cpu().numpy(), cols, cs.shape[1]), cs, f"flux {li} rht col s")
+
+
+def test_recipes_mixed_batch_equals_single_calls():
+    # The layer's forward quantization with both recipes: X with the transformed col blob and
+    # W with 2-D blocks in one launch give the bytes of their own calls.
+    x = _rht_input(300, 200, 51)
+    w = _edge_input(520, 200, 53)
+    sx = abi.quantize(x.cuda(), dual=True, rht_signs=0x1357)
+    sw = quant_2d(w, True, abi.MXFP4_SCALE_TC)
+    bx = [abi.alloc_blob(300, 200), abi.alloc_blob(200, 300)]
+    bw = [abi.alloc_blob(520, 200), abi.alloc_blob(200, 520)]
+    abi.mxfp4_quantize_batch([(x.cuda(), 300, 200, 200, *bx[0], *bx[1], abi.MXFP4_QUANT_RHT_COL, 0x1357),
+                              (w.cuda(), 520, 200, 200, *bw[0], *bw[1], abi.MXFP4_QUANT_2D_BLOCKS)], True)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    for got, want in zip([*bx[0], *bx[1]], sx):
+        assert torch.equal(got.cpu(), want.cpu())
+    for got, want in zip([*bw[0], *bw[1]], sw):
+        assert torch.equal(got.cpu(), want.cpu())
