@@ -44,6 +44,7 @@ SPEC_HBM_GBS = 8000.0            # HBM3e, nominal (~8 TB/s)
 MMA_MXF4_ISSUE_TFLOPS = 9690.0   # back-to-back kind::mxf4 M256 N256 K64 on all SMs (measured)
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+RHT_SIGNS = 0xA5C3                       # sign mask of the column-blob transform (--recipes)
 DUAL_BYTES = 2 + 2 * (0.5 + 1 / 32)      # per element: bf16 read, two blobs written
 ROW_BYTES = 2 + 0.5 + 1 / 32
 
@@ -227,8 +228,11 @@ def run_ours(args, rank, world, local_rank):
         raise SystemExit("--sr is a mode of the MXFP4 backward, not of --fp8-backward")
     host_t = [wl.tensors(i) for i in range(len(lins))]
     inputs = [{k: v.to(dev) for k, v in t.items()} for t in host_t]
+    if args.recipes and (fp8_bwd or args.sr):
+        raise SystemExit("--recipes is a mode of the MXFP4 backward without stochastic rounding")
     block = MXFP4Block([(l.name, l.M, l.N, l.K) for l in lins], train=train, device=dev,
-                       backward="fp8" if fp8_bwd else "mxfp4")
+                       backward="fp8" if fp8_bwd else "mxfp4", weight_2d=args.recipes,
+                       rht_signs=RHT_SIGNS if (args.recipes and train) else None)
     bias = ([workloads.normal((l.N,), 0.02, 977 + i).to(dev) for i, l in enumerate(lins)]
             if args.bias else None)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -345,7 +349,7 @@ def run_ours(args, rank, world, local_rank):
     total_ms = reduce_max_over_ranks(sum(step_ms), world, dev)
 
     # ---- end to end: inputs from pinned host memory, results back to pinned host memory
-    plain = not (fp8_bwd or args.sr or args.bias)
+    plain = not (fp8_bwd or args.sr or args.bias or args.recipes)
     hin = [{k: v.pin_memory() for k, v in t.items()} for t in host_t]
     houts = []
     for L in block.layers:
@@ -421,7 +425,9 @@ def run_ours(args, rank, world, local_rank):
                    "gemm_mxf4_pair_kernel" if min(l.M for l in lins) > 128 else "gemm_mxf4_kernel")
     traffic = profiled_traffic(gemm_kernel, args.workload)
     mode = ("; backward fp8 (tensorwise E5M2 of dY, X, W; fp8 dgrad + wgrad)" if fp8_bwd else
-            "; dY stochastically rounded" if args.sr else "") + ("; bias fused" if args.bias else "")
+            "; dY stochastically rounded" if args.sr else "") + ("; bias fused" if args.bias else "") + (
+            f"; recipes: W in 32x32 blocks, col blobs of X and dY Hadamard-transformed (signs {RHT_SIGNS:#06x})"
+            if args.recipes else "")
 
     line = {
         "metric": METRIC,
@@ -724,6 +730,9 @@ def main():
     ap.add_argument("--fp8-backward", action="store_true",
                     help="the hybrid backward: dY, X, W quantized tensorwise to FP8 E5M2 and "
                          "dgrad / wgrad as FP8 GEMMs (the layer's mxfp4_backward_precision 'fp8')")
+    ap.add_argument("--recipes", action="store_true",
+                    help="the pages' quantization recipes: W with one scale per 32x32 block in both "
+                         "packings, the col blobs of X and dY Hadamard-transformed")
     ap.add_argument("--bias", action="store_true",
                     help="the forward adds the layer's bf16 bias inside the GEMM (the "
                          "`output + bias` that follows the GEMM in the layer's forward)")

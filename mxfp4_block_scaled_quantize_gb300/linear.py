@@ -253,11 +253,12 @@ class MXFP4Block:
     shapes: sequence of (name, M, N, K).  Options as MXFP4Linear."""
 
     def __init__(self, shapes, train: bool = True, device="cuda", out_dtype=torch.bfloat16,
-                 backward: str = "mxfp4"):
+                 backward: str = "mxfp4", weight_2d: bool = False, rht_signs=None):
         self.names = [s[0] for s in shapes]
         self.train = train
         self.layers = [MXFP4Linear(M, N, K, train=train, device=device, out_dtype=out_dtype,
-                                   backward=backward) for _, M, N, K in shapes]
+                                   backward=backward, weight_2d=weight_2d, rht_signs=rht_signs)
+                       for _, M, N, K in shapes]
         self._ws = None
 
     def ops(self, inputs, bias=None, sr_seed=None):
@@ -300,7 +301,8 @@ class MXFP4Block:
         with the kernels.  host_outputs: per linear (Y, dX, dW) (or (Y,) forward-only) host
         tensors, pinned for asynchrony.  Returns when the step is enqueued; the current
         stream is ordered after every copy."""
-        assert not any(L.fp8_backward for L in self.layers), "the host step runs the MXFP4 backward"
+        assert not any(L.fp8_backward or L.weight_2d or L.rht_signs is not None for L in self.layers), \
+            "the host step runs the plain MXFP4 recipe"
         tasks = self.host_tasks(host_inputs, host_outputs)
         need = abi.mxfp4_linear_workspace_bytes(tasks)
         if self._ws is None or self._ws.numel() < need:
