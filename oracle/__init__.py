@@ -78,6 +78,8 @@ def _load():
         lib.oracle_rht16.restype = None
         lib.oracle_quantize_col_rht.argtypes = [vp, i64, i64, i64, ctypes.c_uint32, vp, vp]
         lib.oracle_quantize_col_rht.restype = ctypes.c_int
+        lib.oracle_quantize_col_rht_sr.argtypes = [vp, i64, i64, i64, ctypes.c_uint32, vp, vp, ctypes.c_uint64, vp]
+        lib.oracle_quantize_col_rht_sr.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -390,5 +392,21 @@ def quantize_col_rht(x_bits, signs):
     q = np.empty((K, Mp // 2), np.uint8)
     s = np.empty((K, Mp // BLOCK), np.uint8)
     if _load().oracle_quantize_col_rht(_ptr(x_bits), M, K, K, int(signs) & 0xFFFF, _ptr(q), _ptr(s)):
+        raise ValueError("non-finite input or transform")
+    return q, s
+
+
+def quantize_col_rht_sr(x_bits, signs, seed, col_ids=None):
+    """Col blob of X[M,K] with the 16-point transform applied along M and stochastically
+    rounded elements (the gradient recipe with `use_sr`); col_ids: each column's index in
+    the full tensor when x_bits holds sampled columns."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, K = x_bits.shape
+    Mp = padded(M)
+    q = np.empty((K, Mp // 2), np.uint8)
+    s = np.empty((K, Mp // BLOCK), np.uint8)
+    ids = _ids(col_ids, K)
+    if _load().oracle_quantize_col_rht_sr(_ptr(x_bits), M, K, K, int(signs) & 0xFFFF, _ptr(q), _ptr(s),
+                                          int(seed) & (2**64 - 1), None if ids is None else _ptr(ids)):
         raise ValueError("non-finite input or transform")
     return q, s

@@ -620,3 +620,33 @@ int oracle_quantize_col_rht(const uint16_t* x, int64_t M, int64_t K, int64_t ldx
     free(col);
     return 0;
 }
+
+/* The gradient recipe of `_quantize_grad_dual` with `use_sr` set: `colwise_use_rht` and
+ * `colwise_use_sr` together.  Col blob of X[M,K] with the transform applied along M as in
+ * oracle_quantize_col_rht, each 32-element block of the transformed column then quantized
+ * with stochastic rounding as in oracle_quantize_col_sr: the scale byte from the block's
+ * transformed values by the round-to-nearest rule, each scaled transformed element
+ * rounded up or down by its 16 random bits, which are those of the blob position (row a =
+ * column of X, column b = position along the padded M; packing 1).  col_ids (may be NULL):
+ * the column index of each of the K columns in the full tensor. */
+int oracle_quantize_col_rht_sr(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint32_t signs, uint8_t* q,
+                               uint8_t* s, uint64_t seed, const int64_t* col_ids) {
+    int64_t Mp = cdiv64(M, PAD) * PAD, MBp = Mp / BLOCK;
+    float* col = (float*)malloc((size_t)Mp * sizeof(float));
+    if (!col) return -2;
+    for (int64_t k = 0; k < K; ++k) {
+        for (int64_t m = 0; m < Mp; ++m) col[m] = (m < M) ? (float)oracle_bf16_to_f64(x[m * ldx + k]) : 0.0f;
+        for (int64_t g = 0; g < Mp / 16; ++g) oracle_rht16(col + 16 * g, signs);
+        for (int64_t mb = 0; mb < MBp; ++mb) {
+            double v[BLOCK];
+            for (int i = 0; i < BLOCK; ++i) v[i] = (double)col[mb * BLOCK + i];
+            if (quantize_block_sr(v, q + k * (Mp / 2) + mb * (BLOCK / 2), &s[k * MBp + mb], seed,
+                                  col_ids ? col_ids[k] : k, mb * BLOCK, 1)) {
+                free(col);
+                return -1;
+            }
+        }
+    }
+    free(col);
+    return 0;
+}

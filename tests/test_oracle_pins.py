@@ -814,3 +814,118 @@ def test_quantize_col_rht_padding_and_wgrad_sum():
         tb = np.concatenate([oracle.rht16(pb[16 * g:16 * g + 16], 0x5A5A) for g in range(8)]).astype(np.float64)
         assert np.any(ta[M:48] != 0)                          # the straddling group spreads
         assert float(ta @ tb) == float(a[:, k].astype(np.float64) @ b[:, k].astype(np.float64))
+
+
+# --- the gradient recipe with `use_sr`: transform and stochastic rounding together --------
+
+def _integer_columns(M, K, seed):
+    """bf16 X with small integer entries: every transformed value (1/4) H16 diag(s) x is then
+    exact in fp32, so the fp64 matrix product is the transform's exact result."""
+    rng = np.random.default_rng(seed)
+    a = rng.integers(-40, 41, (M, K)).astype(np.float32)
+    return (a.view(np.uint32) >> 16).astype(np.uint16), a.astype(np.float64)
+
+
+def _exact_transform(a, mask):
+    """Columns of a (zero-padded to 128 rows) transformed group by group with the matrix
+    (1/4) H16 diag(s) written out from its definition."""
+    M, K = a.shape
+    Mp = oracle.padded(M)
+    p = np.zeros((Mp, K))
+    p[:M] = a
+    T = 0.25 * _sylvester16() * _sign_vector(mask)[None, :]
+    return np.concatenate([T @ p[16 * g:16 * g + 16] for g in range(Mp // 16)])   # [Mp, K]
+
+
+def test_rht_sr_scales_are_the_round_to_nearest_rht_scales():
+    # Stochastic rounding changes elements only: the scale bytes are those of the
+    # round-to-nearest transformed col blob, for any seed.
+    bits, _ = _integer_columns(100, 7, 3)
+    _, s = oracle.quantize_col_rht(bits, 0xA5C3)
+    for seed in (0, 9, 2**50 + 3):
+        _, ss = oracle.quantize_col_rht_sr(bits, 0xA5C3, seed)
+        assert np.array_equal(ss, s)
+
+
+@pytest.mark.parametrize("mask", (0x0000, 0xA5C3))
+def test_rht_sr_codes_of_transform_preimages_for_every_seed(mask):
+    # Transforms that land exactly on MX grid values leave stochastic rounding nothing to
+    # round: the codes and scales are the hand-derived ones for every seed.
+    rng = np.random.default_rng(300 + mask)
+    M, K = 64, 3
+    X = np.zeros((M, K))
+    want_codes, want_scales = [], []
+    for k in range(K):
+        x, c, s = _preimage_column(rng, mask, M // 32)
+        X[:, k] = x
+        want_codes.append(c)
+        want_scales.append(s)
+    bits = (X.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    for seed in (1, 77, 2**33):
+        q, s = oracle.quantize_col_rht_sr(bits, mask, seed)
+        for k in range(K):
+            codes = np.empty(oracle.padded(M), np.uint8)
+            codes[0::2], codes[1::2] = q[k] & 0xF, q[k] >> 4
+            assert np.array_equal(codes[:M], want_codes[k]), (seed, k)
+            assert np.array_equal(s[k][:M // 32], want_scales[k]), (seed, k)
+
+
+def test_rht_sr_elements_are_neighbours_of_the_exact_transform_and_unbiased():
+    # Against the transform written out as a matrix: each dequantized element is within one
+    # grid gap of the exact transformed value, and the mean over seeds approaches it (below
+    # the saturation point).
+    M, K, mask = 48, 4, 0x1234
+    bits, a = _integer_columns(M, K, 8)
+    t = _exact_transform(a, mask).T                      # [K, Mp]: the col blob's rows
+    n = 600
+    acc = np.zeros(t.shape)
+    acc2 = np.zeros(t.shape)
+    for seed in range(n):
+        q, s = oracle.quantize_col_rht_sr(bits, mask, 5000 + seed)
+        d = oracle.dequantize(q, s)
+        scale = np.ldexp(1.0, s.astype(np.int64) - 127).repeat(32, axis=1)
+        y = np.abs(t) / scale
+        gap = np.where(y < 2, 0.5, np.where(y < 4, 1.0, 2.0)) * scale
+        assert np.all(np.abs(d - t) < gap + (t == 0))
+        acc += d
+        acc2 += d * d
+    mean = acc / n
+    sd = np.sqrt(np.maximum(acc2 / n - mean * mean, 0.0))
+    tol = 5 * sd / np.sqrt(n) + 2 * scale * 2.0 ** -16
+    unsat = y < 6                                        # 6 and above saturate to 6
+    assert np.all(np.abs(mean - t)[unsat] <= tol[unsat])
+    assert np.any(sd[unsat] > 0)
+
+
+def test_rht_sr_random_bits_follow_the_blob_position():
+    # Sampled columns with their true indices give the full tensor's rows of the col blob;
+    # the same columns at other indices draw other bits.
+    bits, _ = _integer_columns(70, 9, 4)
+    q, s = oracle.quantize_col_rht_sr(bits, 0x8001, 42)
+    cols = np.array([8, 0, 5])
+    qs, ss = oracle.quantize_col_rht_sr(np.ascontiguousarray(bits[:, cols]), 0x8001, 42, col_ids=cols)
+    assert np.array_equal(qs, q[cols]) and np.array_equal(ss, s[cols])
+    qo, _ = oracle.quantize_col_rht_sr(np.ascontiguousarray(bits[:, cols]), 0x8001, 42)
+    assert not np.array_equal(qo, q[cols])
+
+
+def test_rht_sr_brute_force_from_the_pinned_parts():
+    # Element by element from the separately pinned pieces: the exact transform (matrix
+    # form), the round-to-nearest scale of each 32-block, the element's random bits at its
+    # col-blob position (row = column of X, column = position along padded M, packing 1)
+    # and the single-element stochastic rounding rule.
+    M, K, mask, seed = 40, 3, 0x5A5A, 2**35 + 11
+    bits, a = _integer_columns(M, K, 12)
+    t = _exact_transform(a, mask).T
+    q, s = oracle.quantize_col_rht_sr(bits, mask, seed)
+    for k in range(K):
+        for b in range(t.shape[1] // 32):
+            blk = t[k, 32 * b:32 * b + 32]
+            byte = oracle.e8m0_scale(float(np.max(np.abs(blk))))
+            assert s[k, b] == byte
+            for i in range(32):
+                m = 32 * b + i
+                r = oracle.sr_bits(seed, k, m, 1)
+                want = oracle.e2m1_encode_sr(float(np.ldexp(blk[i], 127 - byte)), r)
+                got = (q[k, m // 2] >> (4 * (m % 2))) & 0xF
+                assert got == want, (k, m)
