@@ -228,8 +228,8 @@ def run_ours(args, rank, world, local_rank):
         raise SystemExit("--sr is a mode of the MXFP4 backward, not of --fp8-backward")
     host_t = [wl.tensors(i) for i in range(len(lins))]
     inputs = [{k: v.to(dev) for k, v in t.items()} for t in host_t]
-    if args.recipes and (fp8_bwd or args.sr):
-        raise SystemExit("--recipes is a mode of the MXFP4 backward without stochastic rounding")
+    if args.recipes and fp8_bwd:
+        raise SystemExit("--recipes is a mode of the MXFP4 backward")
     block = MXFP4Block([(l.name, l.M, l.N, l.K) for l in lins], train=train, device=dev,
                        backward="fp8" if fp8_bwd else "mxfp4", weight_2d=args.recipes,
                        rht_signs=RHT_SIGNS if (args.recipes and train) else None)
@@ -732,7 +732,8 @@ def main():
                          "dgrad / wgrad as FP8 GEMMs (the layer's mxfp4_backward_precision 'fp8')")
     ap.add_argument("--recipes", action="store_true",
                     help="the pages' quantization recipes: W with one scale per 32x32 block in both "
-                         "packings, the col blobs of X and dY Hadamard-transformed")
+                         "packings, the col blobs of X and dY Hadamard-transformed (with --sr: dY "
+                         "stochastically rounded after the transform, the gradient recipe with use_sr)")
     ap.add_argument("--bias", action="store_true",
                     help="the forward adds the layer's bf16 bias inside the GEMM (the "
                          "`output + bias` that follows the GEMM in the layer's forward)")

@@ -150,6 +150,20 @@ mxfp4_status mxfp4_quantize_dual_rht(const void* x, int64_t M, int64_t K, int64_
                                      mxfp4_scale_layout layout, uint32_t signs,
                                      mxfp4_stream_t stream);
 
+/* The full gradient quantization of `_quantize_grad_dual` in primus_turbo_mxfp4_local.py
+ * with `use_sr` set: `rowwise_use_sr`, `colwise_use_sr` and `colwise_use_rht` together.
+ * The row blob exactly as mxfp4_quantize_dual_sr; the col blob transformed exactly as in
+ * mxfp4_quantize_dual_rht, each 32-element block of the transformed column then getting
+ * the round-to-nearest scale byte of its transformed values and stochastically rounded
+ * elements by the rule of mxfp4_quantize_dual_sr, with the random bits of the element's
+ * col-blob position (row a = column of X, column b = position along the padded M,
+ * packing 1).  Arguments, layouts and errors as mxfp4_quantize_dual; signs: bits 0..15;
+ * seed as mxfp4_quantize_dual_sr. */
+mxfp4_status mxfp4_quantize_dual_rht_sr(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                        void* q_row, void* s_row, void* q_col, void* s_col,
+                                        mxfp4_scale_layout layout, uint32_t signs, uint64_t seed,
+                                        mxfp4_stream_t stream);
+
 /* Bits of mxfp4_quantize_task::flags. */
 #define MXFP4_QUANT_2D_BLOCKS 1   /* 32 x 32 blocks, as mxfp4_quantize_dual_2d (row-only too) */
 #define MXFP4_QUANT_RHT_COL 2     /* col blob transformed, as mxfp4_quantize_dual_rht (dual only) */

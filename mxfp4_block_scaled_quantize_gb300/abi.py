@@ -78,6 +78,7 @@ EXPORTED = (
     "mxfp4_quantize_dual_sr",
     "mxfp4_quantize_dual_2d",
     "mxfp4_quantize_dual_rht",
+    "mxfp4_quantize_dual_rht_sr",
     "mxfp4_quantize_batch",
     "mxfp4_gemm",
     "mxfp4_gemm_bias",
@@ -121,6 +122,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_quantize_dual_sr.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, ctypes.c_uint64, vp]
     lib.mxfp4_quantize_dual_2d.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, vp]
     lib.mxfp4_quantize_dual_rht.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, ctypes.c_uint32, vp]
+    lib.mxfp4_quantize_dual_rht_sr.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, ctypes.c_uint32,
+                                               ctypes.c_uint64, vp]
     lib.mxfp4_quantize_batch.argtypes = [i32, ctypes.POINTER(QuantizeTask), i32, i32, vp]
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_gemm_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i32, vp]
@@ -210,6 +213,14 @@ def mxfp4_quantize_dual_rht(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=MXF
     _check(load().mxfp4_quantize_dual_rht(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
                                           _ptr(s_col), layout, int(signs) & 0xFFFF, _stream(stream)),
            "mxfp4_quantize_dual_rht")
+
+
+def mxfp4_quantize_dual_rht_sr(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=MXFP4_SCALE_TC,
+                               signs=0, seed=0, stream=None) -> None:
+    _check(load().mxfp4_quantize_dual_rht_sr(_ptr(x), M, K, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
+                                             _ptr(s_col), layout, int(signs) & 0xFFFF, int(seed) & (2**64 - 1),
+                                             _stream(stream)),
+           "mxfp4_quantize_dual_rht_sr")
 
 
 def mxfp4_quantize_batch(tasks, dual: bool, layout=MXFP4_SCALE_TC, stream=None) -> None:
@@ -336,15 +347,18 @@ def quantize(x, dual: bool = True, layout: int = MXFP4_SCALE_TC, stream=None, sr
     """bf16 X[M,K] (CUDA, row pitch a multiple of 8) -> (row_q, row_s[, col_q, col_s]);
     with sr_seed (dual only) the elements are stochastically rounded; with block_2d the
     scales are those of 32 x 32 blocks; with rht_signs (dual only) the col blob is that of
-    the Hadamard-transformed columns."""
+    the Hadamard-transformed columns (both: the gradient recipe with stochastic rounding)."""
     import torch
     assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1
     M, K = x.shape
     rq, rs = alloc_blob(M, K, layout, x.device)
     if rht_signs is not None:
-        assert dual and sr_seed is None and not block_2d
+        assert dual and not block_2d
         cq, cs = alloc_blob(K, M, layout, x.device)
-        mxfp4_quantize_dual_rht(x, M, K, x.stride(0), rq, rs, cq, cs, layout, rht_signs, stream)
+        if sr_seed is None:
+            mxfp4_quantize_dual_rht(x, M, K, x.stride(0), rq, rs, cq, cs, layout, rht_signs, stream)
+        else:
+            mxfp4_quantize_dual_rht_sr(x, M, K, x.stride(0), rq, rs, cq, cs, layout, rht_signs, sr_seed, stream)
         return rq, rs, cq, cs
     if block_2d:
         assert sr_seed is None, "the 2-D block recipe is for weights, stochastic rounding for gradients"

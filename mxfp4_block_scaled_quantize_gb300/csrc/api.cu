@@ -132,7 +132,7 @@ mxfp4_status quantize_task(const void* x, int64_t M, int64_t K, int64_t ldx, voi
 mxfp4_status launch_batch(const mxfp4::QuantBatch& b, bool dual, DeviceState* dev, cudaStream_t stream,
                           bool sr = false) {
     const int64_t tiles = b.tile_end[b.count - 1];
-    const int64_t cap = static_cast<int64_t>(dev->sms) * mxfp4::quantize_ctas_per_sm();
+    const int64_t cap = static_cast<int64_t>(dev->sms) * mxfp4::quantize_ctas_per_sm(sr);
     const int grid = static_cast<int>(tiles < cap ? tiles : cap);
     return mxfp4::launch_quantize(b, dual, sr, grid, stream) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
@@ -356,6 +356,13 @@ mxfp4_status mxfp4_quantize_dual_rht(const void* x, int64_t M, int64_t K, int64_
                                      mxfp4_stream_t stream) {
     return quantize_common(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, true,
                            reinterpret_cast<cudaStream_t>(stream), false, 0, MXFP4_QUANT_RHT_COL, signs);
+}
+
+mxfp4_status mxfp4_quantize_dual_rht_sr(const void* x, int64_t M, int64_t K, int64_t ldx, void* q_row,
+                                        void* s_row, void* q_col, void* s_col, mxfp4_scale_layout layout,
+                                        uint32_t signs, uint64_t seed, mxfp4_stream_t stream) {
+    return quantize_common(x, M, K, ldx, q_row, s_row, q_col, s_col, layout, true,
+                           reinterpret_cast<cudaStream_t>(stream), true, seed, MXFP4_QUANT_RHT_COL, signs);
 }
 
 mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* tasks, int32_t dual,

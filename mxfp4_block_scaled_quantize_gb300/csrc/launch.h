@@ -43,7 +43,7 @@ struct QuantBatch {
 
 // Shared memory one quantizer CTA needs, and how many CTAs share an SM.
 size_t quantize_smem_bytes();
-int quantize_ctas_per_sm();
+int quantize_ctas_per_sm(bool sr);
 
 // sr: elements stochastically rounded (dual only), with each task's seed.
 cudaError_t launch_quantize(const QuantBatch& b, bool dual, bool sr, int grid, cudaStream_t stream);

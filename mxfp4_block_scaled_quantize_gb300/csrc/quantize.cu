@@ -185,8 +185,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
     uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
-        const uint32_t hi0 = __umulhi(0xD2511F53u, x0), lo0 = 0xD2511F53u * x0;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, x2), lo1 = 0xCD9E8D57u * x2;
+        uint64_t p0, p1;   // full 64-bit products, one wide multiply each
+        asm("mul.wide.u32 %0, %1, 0xD2511F53;" : "=l"(p0) : "r"(x0));
+        asm("mul.wide.u32 %0, %1, 0xCD9E8D57;" : "=l"(p1) : "r"(x2));
+        const uint32_t hi0 = static_cast<uint32_t>(p0 >> 32), lo0 = static_cast<uint32_t>(p0);
+        const uint32_t hi1 = static_cast<uint32_t>(p1 >> 32), lo1 = static_cast<uint32_t>(p1);
         const uint32_t n0 = hi1 ^ x1 ^ k0, n2 = hi0 ^ x3 ^ k1;
         x0 = n0;
         x1 = lo1;
@@ -198,22 +201,25 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
     return make_uint4(x0, x1, x2, x3);
 }
 
-// A scaled element y onto the E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}: |y| >= 6 gives
-// 6; otherwise, between neighbours lo <= |y| < hi, hi when the 16 random bits r are below
-// floor((|y| - lo) / (hi - lo) * 2^16), else lo; the sign is kept.  Every step is exact in
-// fp32 (the gap is a power of two and |y| - lo loses no bits), so the result is exactly a
-// grid value and the round-to-nearest conversion below only encodes it.
-__device__ __forceinline__ float sr_round(float y, uint32_t r) {
-    const float a = fabsf(y);
-    float q = 6.0f;
-    if (a < 6.0f) {
-        const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-        const float inv_gap = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-        const float lo = floorf(a * inv_gap) * gap;
-        const uint32_t t = __float2uint_rz((a - lo) * inv_gap * 65536.0f);
-        q = r < t ? lo + gap : lo;
-    }
-    return copysignf(q, y);
+// Stochastic rounding of one element onto the E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}:
+// a = |y| (y the scaled element, |y| < 8 for a finite block), x: a value with y's sign bit,
+// r: 16 random bits.  |y| >= 6 gives 6; otherwise, between neighbours lo <= |y| < hi, hi
+// when r is below t = floor((|y| - lo) / g * 2^16) (g = hi - lo), else lo; the sign is kept.
+// Computed as floor_g(|y| + g * (65535 - r) / 2^16), which reaches hi exactly when t > r.  g
+// is 0.5 below 2, 1 in [2, 4) and 2 in [4, 8).  Two fp32 adds rounded toward zero do it:
+// s1 = |y| + g * (1 + (65535 - r) / 2^16), whose second operand is built from bits, then
+// s1 + g * 2^23, where the fp32 spacing is g, so the sum is g * 2^23 + floor_g(s1);
+// subtracting g * 2^23 + g leaves floor_g(|y| + noise).  Rounding s1 toward zero keeps its
+// floor on the g grid (a multiple of s1's own spacing).  A result of 8 (|y| in [6, 8)) is
+// left to the saturating conversion, which gives 6.
+__device__ __forceinline__ float sr_round(float a, float x, uint32_t r) {
+    const uint32_t e = max(__float_as_uint(a) >> 23, 127u);
+    const uint32_t gbits = (e - 1u) << 23;                               // g = 2^(e - 128)
+    const float noise = __uint_as_float(gbits | ((r ^ 0xFFFFu) << 7));   // g * (1 + (65535 - r) / 2^16)
+    const uint32_t cbits = gbits + (23u << 23);                          // g * 2^23
+    const float s2 = __fadd_rz(__fadd_rz(a, noise), __uint_as_float(cbits));
+    const float q = __fsub_rn(s2, __uint_as_float(cbits + 1u));          // - (g * 2^23 + g)
+    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -243,9 +249,22 @@ __device__ __forceinline__ uint32_t encode8_sr(uint4 v, float inv, uint4 rw) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
         const float x = (e & 1) ? bf16_hi(vw[e >> 1]) : bf16_lo(vw[e >> 1]);
-        f[e] = sr_round(__fmul_rn(x, inv), rnd16(r4[e >> 1], e & 1));
+        f[e] = sr_round(__fmul_rn(fabsf(x), inv), x, rnd16(r4[e >> 1], e & 1));
     }
     return pack_e2m1x8(f);
+}
+
+// The Philox words of an 8-row group of the column pass in register order: register k of
+// the group holds row k ^ 2rb, whose bits are in word (k / 2) ^ rb of the true order.
+__device__ __forceinline__ void words_in_register_order(uint4 r, uint32_t rb, uint32_t* o) {
+    uint32_t a0 = r.x, a1 = r.y, a2 = r.z, a3 = r.w;
+    if (rb & 1u) {
+        uint32_t t = a0; a0 = a1; a1 = t; t = a2; a2 = a3; a3 = t;
+    }
+    if (rb & 2u) {
+        uint32_t t = a0; a0 = a2; a2 = t; t = a1; a1 = a3; a3 = t;
+    }
+    o[0] = a0; o[1] = a1; o[2] = a2; o[3] = a3;
 }
 
 // encode_cols8 with stochastic rounding.  w[k] holds rows (k ^ 2rb) of the 8-row group
@@ -254,23 +273,15 @@ __device__ __forceinline__ uint32_t encode8_sr(uint4 v, float inv, uint4 rw) {
 // encode_cols8 gives them.
 __device__ __forceinline__ void encode_cols8_sr(const uint32_t* w, float inv0, float inv1, uint4 r0, uint4 r1,
                                                 uint32_t rb, uint32_t* q0, uint32_t* q1) {
-    // word (k / 2) ^ rb of the true order is the one for w[k]: permute once by rb
-    uint32_t a0 = r0.x, a1 = r0.y, a2 = r0.z, a3 = r0.w;
-    uint32_t b0 = r1.x, b1 = r1.y, b2 = r1.z, b3 = r1.w;
-    if (rb & 1u) {
-        uint32_t t = a0; a0 = a1; a1 = t; t = a2; a2 = a3; a3 = t;
-        t = b0; b0 = b1; b1 = t; t = b2; b2 = b3; b3 = t;
-    }
-    if (rb & 2u) {
-        uint32_t t = a0; a0 = a2; a2 = t; t = a1; a1 = a3; a3 = t;
-        t = b0; b0 = b2; b2 = t; t = b1; b1 = b3; b3 = t;
-    }
-    const uint32_t ra[4] = {a0, a1, a2, a3}, rbw[4] = {b0, b1, b2, b3};
+    uint32_t ra[4], rbw[4];
+    words_in_register_order(r0, rb, ra);
+    words_in_register_order(r1, rb, rbw);
     float f0[8], f1[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-        f0[k] = sr_round(__fmul_rn(bf16_lo(w[k]), inv0), rnd16(ra[k >> 1], k & 1));
-        f1[k] = sr_round(__fmul_rn(bf16_hi(w[k]), inv1), rnd16(rbw[k >> 1], k & 1));
+        const float x0 = bf16_lo(w[k]), x1 = bf16_hi(w[k]);
+        f0[k] = sr_round(__fmul_rn(fabsf(x0), inv0), x0, rnd16(ra[k >> 1], k & 1));
+        f1[k] = sr_round(__fmul_rn(fabsf(x1), inv1), x1, rnd16(rbw[k >> 1], k & 1));
     }
     *q0 = pack_e2m1x8(f0);
     *q1 = pack_e2m1x8(f1);
@@ -280,10 +291,12 @@ __device__ __forceinline__ void encode_cols8_sr(const uint32_t* w, float inv0, f
 // column pair (high or low halves of w); register i of w holds row (i & ~7) | ((i & 7) ^ 2rb)
 // and bit (i & 15) of psigns is the sign of that row's position in its 16-row group.  Gives
 // the block's scale byte from the transformed values and the codes, word g byte j holding
-// registers 8g + 2j (low nibble) and 8g + 2j + 1, like encode_cols8.
-template <int kHi>
+// registers 8g + 2j (low nibble) and 8g + 2j + 1, like encode_cols8.  kSR: the scaled
+// transformed elements are stochastically rounded with the col-blob bits of Philox counter
+// (c0 + g, a, 1, 0) for register group g (c0: the block's first row / 8, a: the column).
+template <int kHi, bool kSR>
 __device__ __forceinline__ void rht_column(const uint32_t* w, uint32_t rb, uint32_t psigns, uint32_t* byte,
-                                           uint32_t* q) {
+                                           uint32_t* q, uint64_t seed, uint32_t c0, uint32_t a) {
     float f[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -319,8 +332,21 @@ __device__ __forceinline__ void rht_column(const uint32_t* w, uint32_t rb, uint3
     const uint32_t b = max(ef, 2u) - 2u;
     *byte = b;
     const float inv = __uint_as_float(inv_scale_bits(b));
+    if (kSR) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(f[i], inv);
+        for (int gw = 0; gw < 4; ++gw) {
+            uint32_t pw[4];
+            words_in_register_order(philox4x32_10(c0 + gw, a, 1u, seed), rb, pw);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float y = f[8 * gw + i];
+                f[8 * gw + i] = sr_round(__fmul_rn(fabsf(y), inv), y, rnd16(pw[i >> 1], i & 1));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(f[i], inv);
+    }
 #pragma unroll
     for (int gw = 0; gw < 4; ++gw) q[gw] = pack_e2m1x8(&f[8 * gw]);
 }
@@ -341,8 +367,10 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 
 // kRecipes: some task of the launch has 2-D blocks (QuantArgs::block_2d) or the Hadamard
 // transform of its column blob (QuantArgs::rht); such a task's tiles take those paths.
+// The stochastic-rounding instance runs one CTA per SM, with the registers that leaves a
+// thread: at two CTAs per SM (96 registers) its Philox words spilled.
 template <bool kDual, bool kSR, bool kRecipes>
-__global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
+__global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
     quantize_kernel(const __grid_constant__ QuantBatch P) {
     extern __shared__ uint8_t smem_raw[];
     QuantSmem& sm = *reinterpret_cast<QuantSmem*>(
@@ -526,8 +554,11 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
 #pragma unroll
                 for (int r2 = 0; r2 < 16; ++r2)
                     psigns |= ((p.rht_signs >> ((r2 & 8) | ((r2 & 7) ^ (2 * rb)))) & 1u) << r2;
-                rht_column<0>(w, static_cast<uint32_t>(rb), psigns, &byte0, q0);
-                rht_column<1>(w, static_cast<uint32_t>(rb), psigns, &byte1, q1);
+                const uint32_t c0 = static_cast<uint32_t>((m0 + rb * 32) >> 3);
+                rht_column<0, kSR>(w, static_cast<uint32_t>(rb), psigns, &byte0, q0, p.seed, c0,
+                                   static_cast<uint32_t>(kc));
+                rht_column<1, kSR>(w, static_cast<uint32_t>(rb), psigns, &byte1, q1, p.seed, c0,
+                                   static_cast<uint32_t>(kc + 1));
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     q0[j] = __byte_perm(q0[j], 0, sel);
@@ -590,17 +621,20 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
 }  // namespace
 
 size_t quantize_smem_bytes() { return sizeof(QuantSmem) + 1024; }
-int quantize_ctas_per_sm() { return kQCtasPerSm; }
+int quantize_ctas_per_sm(bool sr) { return sr ? 1 : kQCtasPerSm; }
 
 cudaError_t launch_quantize(const QuantBatch& b, bool dual, bool sr, int grid, cudaStream_t stream) {
     const size_t smem = quantize_smem_bytes();
     if (sr && !dual) return cudaErrorInvalidValue;
-    bool b2d = false;
-    for (int j = 0; j < b.count; ++j) b2d = b2d || b.args[j].block_2d != 0 || b.args[j].rht != 0;
-    if (sr && b2d) return cudaErrorInvalidValue;
-    auto k = sr    ? quantize_kernel<true, true, false>
-             : b2d ? (dual ? quantize_kernel<true, false, true> : quantize_kernel<false, false, true>)
-                   : (dual ? quantize_kernel<true, false, false> : quantize_kernel<false, false, false>);
+    bool recipes = false, any_2d = false;
+    for (int j = 0; j < b.count; ++j) {
+        recipes = recipes || b.args[j].block_2d != 0 || b.args[j].rht != 0;
+        any_2d = any_2d || b.args[j].block_2d != 0;
+    }
+    if (sr && any_2d) return cudaErrorInvalidValue;   // 2-D blocks are a weight recipe, without SR
+    auto k = sr        ? (recipes ? quantize_kernel<true, true, true> : quantize_kernel<true, true, false>)
+             : recipes ? (dual ? quantize_kernel<true, false, true> : quantize_kernel<false, false, true>)
+                       : (dual ? quantize_kernel<true, false, false> : quantize_kernel<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];

@@ -86,9 +86,12 @@ class MXFP4Linear:
     def quantize_dy(self, dy, stream=None, sr_seed=None):
         """dY's two blobs; with sr_seed, stochastically rounded (the gradient quantizer's
         `use_sr`, the layer's `mxfp4_gradient_stochastic_rounding` option); with the layer's
-        rht_signs, the col blob of the transformed columns."""
-        if self.rht_signs is not None:
-            assert sr_seed is None, "stochastic rounding and the transform are not combined"
+        rht_signs, the col blob of the transformed columns (both together: the gradient
+        recipe of `_quantize_grad_dual` with `use_sr`)."""
+        if self.rht_signs is not None and sr_seed is not None:
+            abi.mxfp4_quantize_dual_rht_sr(dy, self.M, self.N, dy.stride(0), *self.dy_row, *self.dy_col,
+                                           abi.MXFP4_SCALE_TC, self.rht_signs, sr_seed, stream)
+        elif self.rht_signs is not None:
             abi.mxfp4_quantize_dual_rht(dy, self.M, self.N, dy.stride(0), *self.dy_row, *self.dy_col,
                                         abi.MXFP4_SCALE_TC, self.rht_signs, stream)
         elif sr_seed is None:

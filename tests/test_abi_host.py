@@ -82,6 +82,8 @@ def test_argument_checks_precede_any_device_use(lib):
     bad = (T * 1)(T(16, 4, 8, 8, 32, 48, 64, 80, 2, 7))            # transform without a col blob
     assert lib.mxfp4_quantize_batch(1, bad, 0, 1, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_quantize_dual_rht(16, 4, 8, 8, 32, 48, None, 64, 1, 7, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_quantize_dual_rht_sr(16, 4, 8, 8, 32, 48, None, 64, 1, 7, 9, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_quantize_dual_rht_sr(16, 4, 8, 8, 32, 48, 64, 80, 3, 7, 9, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_quantize_dual_2d(16, 4, 8, 8, 32, 48, None, 64, 1, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_quantize_dual_2d(18, 4, 8, 8, 32, 48, 64, 80, 1, None) == abi.MXFP4_ERR_MISALIGNED
     G = abi.GemmTask
@@ -148,6 +150,8 @@ def test_no_usable_device_fails_loudly(lib):
     assert lib.mxfp4_quantize_dual_sr(0x10000, 4, 8, 8, 0x20000, 0x30000, 0x40000, 0x50000, 1, 7, None) in bad
     assert lib.mxfp4_quantize_dual_2d(0x10000, 4, 8, 8, 0x20000, 0x30000, 0x40000, 0x50000, 1, None) in bad
     assert lib.mxfp4_quantize_dual_rht(0x10000, 4, 8, 8, 0x20000, 0x30000, 0x40000, 0x50000, 1, 7, None) in bad
+    assert lib.mxfp4_quantize_dual_rht_sr(0x10000, 4, 8, 8, 0x20000, 0x30000, 0x40000, 0x50000, 1, 7, 9,
+                                          None) in bad
     assert lib.mxfp4_gemm(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x50000, 4, 0, None) in bad
     assert lib.mxfp4_gemm_bias(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x60000, 0x50000, 4, 0, None) in bad
     assert lib.mxfp4_fp8_quantize_tw(0x10000, 4, 8, 8, 0x20000, None, 0x30000, 0x30004, None) in bad

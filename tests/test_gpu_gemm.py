@@ -371,23 +371,29 @@ def test_tiny_step_with_2d_weight_blocks(out_dtype):
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("shape", [(256, 256, 512), (200, 136, 264)])
-def test_step_with_both_recipes(shape, out_dtype):
+@pytest.mark.parametrize("shape,sr_seed", [((256, 256, 512), None), ((200, 136, 264), None),
+                                           ((256, 256, 512), 31), ((200, 136, 264), 2**40 + 1)])
+def test_step_with_both_recipes(shape, sr_seed, out_dtype):
     # The layer with the pages' recipes: W in 32 x 32 blocks, the col blobs of X and dY
-    # transformed (the same signs).  fwd and dgrad read W's 2-D blobs; wgrad multiplies the
-    # two transformed col blobs.  Every GEMM against the oracle's GEMM over the oracle's
-    # blobs of the same recipes.
+    # transformed (the same signs), and with a seed dY stochastically rounded (the gradient
+    # recipe with `use_sr`).  fwd and dgrad read W's 2-D blobs; wgrad multiplies the two
+    # transformed col blobs.  Every GEMM against the oracle's GEMM over the oracle's blobs
+    # of the same recipes.
     M, N, K = shape
     t = {"X": workloads.student_t3((M, K), 1.0, M + 1), "W": workloads.normal((N, K), 0.3, N + 2),
          "dY": workloads.normal((M, N), 0.01, K + 3)}
     layer = MXFP4Linear(M, N, K, train=True, out_dtype=out_dtype, weight_2d=True, rht_signs=0xA5C3)
-    y, dx, dw = layer.step(pitched(t["X"]), pitched(t["W"]), pitched(t["dY"]))
+    y, dx, dw = layer.step(pitched(t["X"]), pitched(t["W"]), pitched(t["dY"]), sr_seed=sr_seed)
     torch.cuda.synchronize()
     assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
     xb, wb, dyb = (workloads.bf16_bits(t[k]) for k in ("X", "W", "dY"))
-    xr, dyr = oracle.quantize_row(xb), oracle.quantize_row(dyb)
+    xr = oracle.quantize_row(xb)
     wr, wc = oracle.quantize_row_2d(wb), oracle.quantize_col_2d(wb)
-    xc, dyc = oracle.quantize_col_rht(xb, 0xA5C3), oracle.quantize_col_rht(dyb, 0xA5C3)
+    xc = oracle.quantize_col_rht(xb, 0xA5C3)
+    if sr_seed is None:
+        dyr, dyc = oracle.quantize_row(dyb), oracle.quantize_col_rht(dyb, 0xA5C3)
+    else:
+        dyr, dyc = oracle.quantize_row_sr(dyb, sr_seed), oracle.quantize_col_rht_sr(dyb, 0xA5C3, sr_seed)
     c, cabs = oracle.gemm(*xr, *wr)
     check_gemm(y, c, cabs, f"recipes fwd {shape}")
     c, cabs = oracle.gemm(*dyr, *wc)

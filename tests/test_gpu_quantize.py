@@ -493,3 +493,84 @@ def test_recipes_mixed_batch_equals_single_calls():
         assert torch.equal(got.cpu(), want.cpu())
     for got, want in zip([*bw[0], *bw[1]], sw):
         assert torch.equal(got.cpu(), want.cpu())
+
+
+# --- the gradient recipe with `use_sr`: transformed col blob, stochastic rounding ---------
+
+def check_rht_sr_full(x_cpu, outs, layout, signs, seed, what):
+    xb = workloads.bf16_bits(x_cpu)
+    tc = layout == abi.MXFP4_SCALE_TC
+    rq, rs = oracle.quantize_row_sr(xb, seed)
+    assert_bytes_equal(outs[0].cpu().numpy(), rq, f"{what} row q")
+    assert_bytes_equal(outs[1].cpu().numpy().reshape(-1), (oracle.scale_to_tc(rs) if tc else rs).reshape(-1),
+                       f"{what} row s")
+    cq, cs = oracle.quantize_col_rht_sr(xb, signs, seed)
+    assert_bytes_equal(outs[2].cpu().numpy(), cq, f"{what} col q")
+    assert_bytes_equal(outs[3].cpu().numpy().reshape(-1), (oracle.scale_to_tc(cs) if tc else cs).reshape(-1),
+                       f"{what} col s")
+
+
+@pytest.mark.parametrize("M,K,ldx", [(1, 8, 8), (40, 40, 40), (130, 200, 200), (257, 33, 40), (640, 384, 384),
+                                     (4600, 256, 256)])
+@pytest.mark.parametrize("signs,seed", [(0xA5C3, 7), (0x8001, 0x9E3779B97F4A7C15)])
+def test_rht_sr_ragged_shapes(M, K, ldx, signs, seed):
+    # Row blob as the stochastically rounded dual quantizer, col blob as the oracle's
+    # transformed and stochastically rounded columns, byte for byte.
+    x = _rht_input(M, K, 7 * M + K)
+    for layout in LAYOUTS:
+        wide = torch.zeros((M, ldx), dtype=torch.bfloat16)
+        wide[:, :K] = x
+        outs = abi.quantize(wide.cuda()[:, :K], dual=True, layout=layout, rht_signs=signs, sr_seed=seed)
+        torch.cuda.synchronize()
+        assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+        check_rht_sr_full(x, outs, layout, signs, seed, f"rht+sr {M}x{K}")
+
+
+def test_rht_sr_every_bf16_pattern_below_overflow():
+    b = np.arange(0x10000, dtype=np.uint32).astype(np.uint16)
+    b = np.where((b & 0x7F80) < (200 << 7), b, 0).astype(np.uint16)
+    rng = np.random.default_rng(17)
+    x = _bits_to_bf16(b[rng.permutation(b.size)].reshape(256, 256))
+    outs = abi.quantize(x.cuda(), dual=True, layout=abi.MXFP4_SCALE_TC, rht_signs=0x1234, sr_seed=99)
+    torch.cuda.synchronize()
+    check_rht_sr_full(x, outs, abi.MXFP4_SCALE_TC, 0x1234, 99, "rht+sr all patterns")
+
+
+def test_rht_sr_seed_behaviour():
+    # Same seed: identical bytes; another seed: other elements, the same scales, which are
+    # the round-to-nearest transformed ones.
+    x = workloads.normal((384, 640), 1.0, 79).cuda()
+    a = abi.quantize(x, dual=True, rht_signs=0xA5C3, sr_seed=5)
+    b = abi.quantize(x, dual=True, rht_signs=0xA5C3, sr_seed=5)
+    c = abi.quantize(x, dual=True, rht_signs=0xA5C3, sr_seed=6)
+    n = abi.quantize(x, dual=True, rht_signs=0xA5C3)
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+    assert not torch.equal(a[2], c[2])
+    assert torch.equal(a[1], n[1]) and torch.equal(a[3], n[3])
+
+
+def test_rht_sr_flux_dy_sampled():
+    # The single-stream block's two gradients dY [4608, 21504] and [4608, 3072] in the
+    # launch configuration of the backward step, on sampled rows and columns at their true
+    # positions.
+    from parity import gather_tc_rows
+    seed = 4242
+    for li in (0, 1):
+        dy = workloads.FLUX_SINGLE_BLOCK.tensors(li)["dY"]
+        outs = abi.quantize(dy.cuda(), dual=True, layout=abi.MXFP4_SCALE_TC, rht_signs=0xA5C3, sr_seed=seed)
+        torch.cuda.synchronize()
+        assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+        xb = workloads.bf16_bits(dy)
+        M, K = xb.shape
+        rng = np.random.default_rng(11 + li)
+        rows = np.unique(np.concatenate([rng.choice(M, 16, replace=False), [0, M - 1]]))
+        cols = np.unique(np.concatenate([rng.choice(K, 16, replace=False), [0, K - 1]]))
+        rq, rs = oracle.quantize_row_sr(np.ascontiguousarray(xb[rows]), seed, row_ids=rows)
+        assert_bytes_equal(outs[0][torch.as_tensor(rows, device="cuda")].cpu().numpy(), rq, f"dY{li} row q")
+        assert_bytes_equal(gather_tc_rows(outs[1].cpu().numpy(), rows, rs.shape[1]), rs, f"dY{li} row s")
+        cq, cs = oracle.quantize_col_rht_sr(np.ascontiguousarray(xb[:, cols]), 0xA5C3, seed, col_ids=cols)
+        assert_bytes_equal(outs[2][torch.as_tensor(cols, device="cuda")].cpu().numpy(), cq, f"dY{li} col q")
+        assert_bytes_equal(gather_tc_rows(outs[3].cpu().numpy(), cols, cs.shape[1]), cs, f"dY{li} col s")
+
