@@ -86,8 +86,8 @@ def load_peaks():
 
 KERNEL_SOURCES = {
     "gemm_mxf4_kernel": ("gemm.cu", "epilogue.cuh", "ptx.cuh", "launch.h"),
-    "gemm_mxf4_pair_kernel": ("gemm_pair.cu", "epilogue.cuh", "ptx.cuh", "launch.h"),
-    "quantize_kernel": ("quantize.cu", "ptx.cuh", "launch.h"),
+    "gemm_mxf4_pair_kernel": ("gemm_pair.cu", "epilogue.cuh", "mx_encode.cuh", "ptx.cuh", "launch.h"),
+    "quantize_kernel": ("quantize.cu", "mx_encode.cuh", "ptx.cuh", "launch.h"),
     "gemm_fp8_pair_kernel": ("gemm_fp8.cu", "epilogue.cuh", "ptx.cuh", "launch_fp8.h"),
 }
 
@@ -486,9 +486,10 @@ def run_ours(args, rank, world, local_rank):
 
 def run_extras(args, dev, flush_l2, head_start):
     """Lines for the other Flux configs, timed the same way: the QKV projection forward with
-    row-only quantization (X[4608,3072], W[9216,3072]) and the quantizer bandwidth sweep
+    row-only quantization (X[4608,3072], W[9216,3072]), the quantizer bandwidth sweep
     (dual quantization of M x K bf16 tensors for every M in {4608, 18432, 4600} and K in
-    {3072, 12288, 15360}; the largest, 18432 x 15360, moves 867 MB)."""
+    {3072, 12288, 15360}; the largest, 18432 x 15360, moves 867 MB) and the forward GEMM
+    that quantizes its own output against the GEMM plus a quantizer launch."""
     import torch
 
     from mxfp4_block_scaled_quantize_gb300 import abi, workloads
@@ -555,6 +556,52 @@ def run_extras(args, dev, flush_l2, head_start):
                                  "frac_of_spec_8tbs": round(gbs / SPEC_HBM_GBS, 4)}
             del x, outs
     out["quant_dual_sweep"] = sweep
+
+    # The forward GEMM whose epilogue writes its output's dual MXFP4 blobs (what the next
+    # layer's forward would quantize), against the GEMM followed by the dual quantizer over
+    # its output: the single-stream block's linear1, 4608 x 21504 x 3072.
+    wl = workloads.FLUX_SINGLE_BLOCK
+    lin = wl.linears[0]
+    t = wl.tensors(0)
+    aq, a_s = abi.quantize(t["X"].to(dev), dual=False)
+    bq, b_s = abi.quantize(t["W"].to(dev), dual=False)
+    del t
+    c = torch.empty((lin.M, lin.N), dtype=torch.bfloat16, device=dev)
+    rq, rs = abi.alloc_blob(lin.M, lin.N, device=dev)
+    cq, cs = abi.alloc_blob(lin.N, lin.M, device=dev)
+    args_g = (aq, a_s, bq, b_s, lin.M, lin.N, lin.K)
+
+    def fused():
+        abi.mxfp4_gemm_quantize(*args_g, None, c, lin.N, rq, rs, cq, cs)
+
+    def unfused():
+        abi.mxfp4_gemm(*args_g, c, lin.N, abi.MXFP4_OUT_BF16)
+        abi.mxfp4_quantize_dual(c, lin.M, lin.N, lin.N, rq, rs, cq, cs, abi.MXFP4_SCALE_TC)
+
+    def fused_row():
+        abi.mxfp4_gemm_quantize(*args_g, None, c, lin.N, rq, rs, None, None)
+
+    def plain():
+        abi.mxfp4_gemm(*args_g, c, lin.N, abi.MXFP4_OUT_BF16)
+    res = {}
+    for name, fn in (("gemm_only", plain), ("gemm_then_quantize", unfused), ("gemm_quantize_fused", fused),
+                     ("gemm_quantize_fused_row_only", fused_row)):
+        for _ in range(3):
+            fn()
+        ms = []
+        for _ in range(n):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ms.append((e0, e1))
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in ms]
+        res[name] = dict(summarize(ms), tflops=round(lin.flops_fwd / (statistics.median(ms) * 1e-3) / 1e12, 1))
+    res["shape"] = f"{lin.M}x{lin.N}x{lin.K}"
+    out["fwd_gemm_with_output_blobs"] = res
+    del aq, a_s, bq, b_s, c, rq, rs, cq, cs
     if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
         raise RuntimeError("device error word set during the extra lines")
     return out

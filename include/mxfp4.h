@@ -225,6 +225,26 @@ mxfp4_status mxfp4_gemm_bias(const void* a_q, const void* a_s, const void* b_q, 
                              int64_t M, int64_t N, int64_t K, const void* bias, void* c,
                              int64_t ldc, mxfp4_out_dtype out_dtype, mxfp4_stream_t stream);
 
+/* A forward GEMM whose epilogue also quantizes its output for the next linear layer: the
+ * "GEMM epilogue that emits the next layer's MXFP4 row blob" fusion of the layer chain
+ * (`MXFP4LinearFunction.forward` of primus_turbo_mxfp4_local.py feeds each layer's output
+ * to the next layer, whose forward starts with `_quantize_mxfp4_dual_op` of that output).
+ * Writes bf16 C = A . B^T (+ bias), exactly as mxfp4_gemm / mxfp4_gemm_bias with
+ * MXFP4_OUT_BF16, and the MXFP4 blobs of C's bf16 values exactly as
+ * mxfp4_quantize_dual(C) (q_col and s_col set) or mxfp4_quantize(C) (both NULL) with
+ * MXFP4_SCALE_TC would write them, padding included:
+ *   q_row [M, Np/2], s_row  the row blob of C (blocks of 32 along N), Np = ceil(N/128)*128
+ *   q_col [N, Mp/2], s_col  the col blob of C (blocks of 32 along M), Mp = ceil(M/128)*128
+ * C is not read back: the blobs come from the accumulator tile after its bf16 rounding,
+ * in the epilogue of the CTA-pair kernel (one extra launch, the quantizer over C, when M is
+ * at most 128).  bias: bf16[N] or NULL.  ldc: a multiple of 8 (MXFP4_ERR_MISALIGNED
+ * otherwise, as for an unaligned pointer); q_row, s_row not NULL, q_col and s_col both
+ * NULL or both set (MXFP4_ERR_INVALID_ARG).  Everything else as mxfp4_gemm. */
+mxfp4_status mxfp4_gemm_quantize(const void* a_q, const void* a_s, const void* b_q, const void* b_s,
+                                 int64_t M, int64_t N, int64_t K, const void* bias, void* c, int64_t ldc,
+                                 void* q_row, void* s_row, void* q_col, void* s_col,
+                                 mxfp4_stream_t stream);
+
 /* One GEMM of a batch: the arguments of mxfp4_gemm, and an optional bias (NULL: none;
  * otherwise as for mxfp4_gemm_bias). */
 typedef struct {

@@ -82,6 +82,7 @@ EXPORTED = (
     "mxfp4_quantize_batch",
     "mxfp4_gemm",
     "mxfp4_gemm_bias",
+    "mxfp4_gemm_quantize",
     "mxfp4_gemm_batch",
     "mxfp4_fp8_quantize_tw",
     "mxfp4_fp8_quantize_tw_batch",
@@ -128,6 +129,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_gemm_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i32, vp]
     lib.mxfp4_gemm_batch.argtypes = [i32, ctypes.POINTER(GemmTask), vp]
+    lib.mxfp4_gemm_quantize.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, vp, vp, vp, vp, vp]
     lib.mxfp4_fp8_quantize_tw.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp]
     lib.mxfp4_fp8_quantize_tw_batch.argtypes = [i32, ctypes.POINTER(Fp8QuantizeTask), vp]
     lib.mxfp4_fp8_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
@@ -247,6 +249,26 @@ def mxfp4_gemm_bias(a_q, a_s, b_q, b_s, M, N, K, bias, c, ldc, out_dtype=MXFP4_O
                     stream=None) -> None:
     _check(load().mxfp4_gemm_bias(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, _ptr(bias),
                                   _ptr(c), ldc, out_dtype, _stream(stream)), "mxfp4_gemm_bias")
+
+
+def mxfp4_gemm_quantize(a_q, a_s, b_q, b_s, M, N, K, bias, c, ldc, q_row, s_row, q_col=None, s_col=None,
+                        stream=None) -> None:
+    _check(load().mxfp4_gemm_quantize(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, _ptr(bias), _ptr(c),
+                                      ldc, _ptr(q_row), _ptr(s_row), _ptr(q_col), _ptr(s_col), _stream(stream)),
+           "mxfp4_gemm_quantize")
+
+
+def gemm_quantize(a_q, a_s, b_q, b_s, M, N, K, dual=True, out=None, bias=None, stream=None):
+    """bf16 C[M,N] = A . B^T (+ bias) and the MXFP4 blobs of C (tensor-core scale layout),
+    as quantize(C, dual) would give them: (C, row_q, row_s[, col_q, col_s])."""
+    import torch
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a_q.device)
+    assert out.dtype == torch.bfloat16 and out.stride(1) == 1
+    rq, rs = alloc_blob(M, N, MXFP4_SCALE_TC, out.device)
+    cq, cs = alloc_blob(N, M, MXFP4_SCALE_TC, out.device) if dual else (None, None)
+    mxfp4_gemm_quantize(a_q, a_s, b_q, b_s, M, N, K, bias, out, out.stride(0), rq, rs, cq, cs, stream)
+    return (out, rq, rs, cq, cs) if dual else (out, rq, rs)
 
 
 def mxfp4_gemm_batch(tasks, stream=None) -> None:

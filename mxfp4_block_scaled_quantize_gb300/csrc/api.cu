@@ -406,6 +406,46 @@ mxfp4_status mxfp4_gemm_bias(const void* a_q, const void* a_s, const void* b_q, 
     return mxfp4_gemm_batch(1, &t, stream);
 }
 
+mxfp4_status mxfp4_gemm_quantize(const void* a_q, const void* a_s, const void* b_q, const void* b_s, int64_t M,
+                                 int64_t N, int64_t K, const void* bias, void* c, int64_t ldc, void* q_row, void* s_row,
+                                 void* q_col, void* s_col, mxfp4_stream_t stream) {
+    const mxfp4_gemm_task t{a_q, a_s, b_q, b_s, M, N, K, c, ldc, MXFP4_OUT_BF16, bias};
+    mxfp4_status st = gemm_check(t);
+    if (st != MXFP4_OK) return st;
+    if (!q_row || !s_row || (q_col == nullptr) != (s_col == nullptr)) return MXFP4_ERR_INVALID_ARG;
+    if ((ldc % 8) != 0 || !aligned16(q_row) || !aligned16(s_row) || (q_col && !aligned16(q_col)) ||
+        (s_col && !aligned16(s_col)))
+        return MXFP4_ERR_MISALIGNED;
+    DeviceState* dev = nullptr;
+    st = device_ready(&dev);
+    if (st != MXFP4_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int max_clusters = mxfp4::gemm_pair_max_clusters();
+    if (M <= mxfp4::kGemmBM || max_clusters <= 0) {
+        // One 128-row tile: the one-CTA GEMM, then the quantizer over C (same bytes).
+        st = mxfp4_gemm_batch(1, &t, stream);
+        if (st != MXFP4_OK) return st;
+        return quantize_common(c, M, N, ldc, q_row, s_row, q_col, s_col, MXFP4_SCALE_TC, q_col != nullptr, s);
+    }
+    mxfp4::GemmPairBatch b;
+    std::memset(&b, 0, sizeof(b));
+    st = gemm_fill_pair(t, dev, &b);
+    if (st != MXFP4_OK) return st;
+    mxfp4::GemmArgs& g = b.args[0];
+    if (!g.c_tma) return MXFP4_ERR_CUDA;
+    g.qo_row = static_cast<uint8_t*>(q_row);
+    g.so_row = static_cast<uint8_t*>(s_row);
+    g.qo_col = static_cast<uint8_t*>(q_col);
+    g.so_col = static_cast<uint8_t*>(s_col);
+    g.ldqo_row = pad128(N) / 2;
+    g.ldqo_col = pad128(M) / 2;
+    g.kb4o_row = static_cast<int32_t>(pad128(N) / 128);
+    g.kb4o_col = static_cast<int32_t>(pad128(M) / 128);
+    const int64_t tiles = b.tile_end[0];
+    const int clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
+    return mxfp4::launch_gemm_pair(b, clusters, s, true) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
 mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4_stream_t stream) {
     if (count < 1 || count > MXFP4_MAX_BATCH || tasks == nullptr) return MXFP4_ERR_INVALID_ARG;
     for (int j = 0; j < count; ++j) {

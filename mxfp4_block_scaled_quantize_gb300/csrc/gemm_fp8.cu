@@ -32,6 +32,7 @@ constexpr int kBBytes = 128 * BKB;        // this CTA's 128 of the tile's 256 B 
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 8;
 constexpr int kEpi0 = 3;
+constexpr int kGroupM = 8;                // row tiles per group of the tile order
 constexpr int kThreads = (kEpi0 + kEpiWarps) * 32;
 constexpr uint32_t kBarHandoff = 1;
 constexpr uint32_t kBarEpilogue = 2;
@@ -39,6 +40,20 @@ constexpr uint32_t kAccCols = 256;
 constexpr uint32_t kTmemCols = 2 * kAccCols;   // two accumulators
 constexpr int kOutRowBytes = 64;
 constexpr int kOutBytes = 32 * kOutRowBytes;
+
+// Output tile lt of a problem, in groups of kGroupM 256-row tiles: within a group the row
+// tile runs fastest and the groups follow each other, so the CTA pairs at work at one time
+// share a few A row tiles and the B tiles of the group, which stay in L2 (row-fastest over
+// the whole problem made every wave stream all of A again).
+__device__ __forceinline__ void tile_coords(int lt, int tiles_m2, int tiles_n, int* mt2, int* nt) {
+    const int per_group = kGroupM * tiles_n;
+    const int grp = lt / per_group;
+    const int first = grp * kGroupM;
+    const int gm = min(tiles_m2 - first, kGroupM);
+    const int r = lt - grp * per_group;
+    *mt2 = first + r % gm;
+    *nt = r / gm;
+}
 
 struct Fp8Smem {
     uint8_t a[kStages][kABytes];          // 1024-byte aligned (128-byte swizzle atoms)
@@ -137,7 +152,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 int lt;
                 const int j = task_of(t, &lt);
                 const Fp8GemmArgs& g = P.args[j];
-                const int mt2 = lt % g.tiles_m2, nt = lt / g.tiles_m2;
+                int mt2, nt;
+                tile_coords(lt, g.tiles_m2, g.tiles_n, &mt2, &nt);
                 const int arow = mt2 * 256 + static_cast<int>(rank) * 128;
                 const int brow = nt * 256 + static_cast<int>(rank) * 128;
                 for (int ks = 0; ks < g.k_stages; ++ks, ++it) {
@@ -254,7 +270,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int lt;
             const int pj = task_of(t, &lt);
             const Fp8GemmArgs& g = P.args[pj];
-            const int mt2 = lt % g.tiles_m2, nt = lt / g.tiles_m2;
+            int mt2, nt;
+            tile_coords(lt, g.tiles_m2, g.tiles_n, &mt2, &nt);
             const int64_t row0 = static_cast<int64_t>(mt2) * 256 + rank * 128 + q * 32;
             const int64_t col0 = static_cast<int64_t>(nt) * 256 + h * 128;
             if (row0 >= g.M || col0 >= g.N) continue;

@@ -30,6 +30,7 @@
 
 #include "epilogue.cuh"
 #include "launch.h"
+#include "mx_encode.cuh"
 #include "ptx.cuh"
 
 namespace mxfp4 {
@@ -90,12 +91,78 @@ __device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t j) {
     return r * kOutRowBytes + ((j ^ ((r >> 1) & 3u)) << 4);
 }
 
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+// Output quantization of one staged 32 x 32 piece of bf16 C (rows row0 .. row0 + 31 of the
+// warp, columns col .. col + 31): w holds this lane's row of the piece (bf16 pairs, even
+// column low), `obuf` the same piece in shared memory (swz64 layout).  Row blob: the lane's
+// 32-element block, stored unless the row is past M; its scale byte (0 for a padding row)
+// goes to byte c of *srow.  Col blob (g.qo_col set): column col + lane, read back down the
+// 32 staged rows (rows past M count as 0), stored unless the column is past N, its scale
+// byte written straight into the tensor-core layout (0 for a padding column).  The
+// elements, scales and padding are those the quantizer gives for C's bf16 values.
+__device__ __forceinline__ void quantize_out_piece(const GemmArgs& g, const uint32_t* w, uint32_t obuf,
+                                                   int64_t row0, int64_t col, int c, int q, uint32_t lane,
+                                                   uint32_t* srow) {
+    const int64_t row = row0 + lane;
+    uint32_t m = w[0];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) m = absmax2(m, w[i]);
+    m = absmax2(m, m >> 16) & 0x7FFFu;   // even and odd columns folded: the block's amax
+    const uint32_t rbyte = row < g.M ? scale_byte(m) : 0u;
+    *srow |= rbyte << (8 * c);
+    if (row < g.M) {
+        const uint64_t s2 = pack2(inv_scale_bits(rbyte), inv_scale_bits(rbyte));
+        *reinterpret_cast<uint4*>(g.qo_row + row * g.ldqo_row + (col >> 1)) =
+            make_uint4(encode8(w[0], w[1], w[2], w[3], s2), encode8(w[4], w[5], w[6], w[7], s2),
+                       encode8(w[8], w[9], w[10], w[11], s2), encode8(w[12], w[13], w[14], w[15], s2));
+    }
+    if (g.qo_col == nullptr) return;
+    const int64_t n = col + lane;
+    const uint32_t base = obuf + ((lane & 7u) << 1);
+    uint32_t cw[16];
+    if (row0 + 32 <= g.M) {   // the usual case: every row of the block is a row of C
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+            cw[k] = lds_u16(base + swz64(2 * k, lane >> 3)) | (lds_u16(base + swz64(2 * k + 1, lane >> 3)) << 16);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            uint32_t lo = lds_u16(base + swz64(2 * k, lane >> 3));
+            uint32_t hi = lds_u16(base + swz64(2 * k + 1, lane >> 3));
+            if (row0 + 2 * k >= g.M) lo = 0;
+            if (row0 + 2 * k + 1 >= g.M) hi = 0;
+            cw[k] = lo | (hi << 16);
+        }
+    }
+    uint32_t mc = cw[0];
+#pragma unroll
+    for (int i = 1; i < 16; ++i) mc = absmax2(mc, cw[i]);
+    mc = absmax2(mc, mc >> 16) & 0x7FFFu;
+    const uint32_t cbyte = scale_byte(mc);
+    if (n < g.N) {
+        const uint64_t s2 = pack2(inv_scale_bits(cbyte), inv_scale_bits(cbyte));
+        *reinterpret_cast<uint4*>(g.qo_col + n * g.ldqo_col + (row0 >> 1)) =
+            make_uint4(encode8(cw[0], cw[1], cw[2], cw[3], s2), encode8(cw[4], cw[5], cw[6], cw[7], s2),
+                       encode8(cw[8], cw[9], cw[10], cw[11], s2), encode8(cw[12], cw[13], cw[14], cw[15], s2));
+    }
+    if (n < ((g.N + 127) & ~int64_t{127})) {
+        const int64_t atom = (n >> 7) * g.kb4o_col + (row0 >> 7);
+        g.so_col[atom * 512 + lane * 16 + c * 4 + q] = static_cast<uint8_t>(n < g.N ? cbyte : 0u);
+    }
+}
+
 // kBatched = false: one problem (P.count == 1); its arguments stay constant-bank operands,
 // which the batched form's run-time problem index turns into registers (measured: the
 // forward GEMM spilled and lost 4 us in the batched form).
 // kBias: some problem of the launch carries a bias (the instance without one compiles the
 // plain conversion only).
-template <bool kBatched, bool kBias>
+// kQuant: the epilogue also writes the MXFP4 blobs of C (one problem, bf16 through TMA).
+template <bool kBatched, bool kBias, bool kQuant>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ GemmPairBatch P) {
     extern __shared__ uint8_t smem_raw[];
@@ -293,6 +360,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int mt2 = lt % g.tiles_m2, nt = lt / g.tiles_m2;
             const int64_t row0 = static_cast<int64_t>(mt2) * 256 + rank * 128 + q * 32;
             const int64_t col0 = static_cast<int64_t>(nt) * 256 + h * 128;
+            if (kQuant) {
+                // Output quantization (bf16 through TMA stores): the warps of padding rows, up
+                // to M's 128-row padding, still write their zero scale bytes.  The four pieces
+                // are converted to bf16 first, which frees the fp32 accumulator registers.
+                if (row0 >= ((g.M + 127) & ~int64_t{127}) || col0 >= g.N) continue;
+                uint32_t wb[4][16];
+                const uint16_t* const bias = kBias ? g.bias : nullptr;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) convert_piece<false>(v[c], bias, col0 + c * 32, g.N, wb[c]);
+                uint32_t srow = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        sts128(obuf + swz64(lane, j), wb[c][4 * j], wb[c][4 * j + 1], wb[c][4 * j + 2], wb[c][4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < g.M && col0 + c * 32 < g.N) {
+                        tma_store_2d_hint(&P.cmap[pj], static_cast<int32_t>(col0 + c * 32), static_cast<int32_t>(row0),
+                                          obuf, pol);
+                        bulk_commit_group();
+                    }
+                    quantize_out_piece(g, wb[c], obuf, row0, col0 + c * 32, c, q, lane, &srow);
+                }
+                // the row's 4 scale bytes of this 128-column half, one word
+                const int64_t atom = ((row0 + lane) >> 7) * g.kb4o_row + (col0 >> 7);
+                *reinterpret_cast<uint32_t*>(g.so_row + atom * 512 + lane * 16 + q * 4) = srow;
+                continue;
+            }
             if (row0 >= g.M || col0 >= g.N) continue;
             if (g.c_tma) {
                 const int per = g.out_f32 ? 16 : 32;
@@ -361,25 +459,28 @@ int gemm_pair_max_clusters() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev] > 0) return cached[dev];
     const size_t smem = gemm_pair_smem_bytes();
-    if (cudaFuncSetAttribute(gemm_mxf4_pair_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_mxf4_pair_kernel<true, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel<true, true>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel<true, true, false>, &cfg) != cudaSuccess) return 0;
     cached[dev] = n;
     return n;
 }
 
-cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream) {
+cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream, bool quant) {
     const size_t smem = gemm_pair_smem_bytes();
     bool bias = false;
     for (int j = 0; j < b.count; ++j) bias = bias || b.args[j].bias != nullptr;
-    auto kernel = b.count > 1 ? (bias ? gemm_mxf4_pair_kernel<true, true> : gemm_mxf4_pair_kernel<true, false>)
-                              : (bias ? gemm_mxf4_pair_kernel<false, true> : gemm_mxf4_pair_kernel<false, false>);
+    if (quant && (b.count != 1 || b.args[0].out_f32 || !b.args[0].c_tma || b.args[0].qo_row == nullptr))
+        return cudaErrorInvalidValue;
+    auto kernel = quant        ? (bias ? gemm_mxf4_pair_kernel<false, true, true> : gemm_mxf4_pair_kernel<false, false, true>)
+                  : b.count > 1 ? (bias ? gemm_mxf4_pair_kernel<true, true, false> : gemm_mxf4_pair_kernel<true, false, false>)
+                               : (bias ? gemm_mxf4_pair_kernel<false, true, false> : gemm_mxf4_pair_kernel<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];

@@ -65,6 +65,16 @@ struct GemmArgs {
     int32_t c_tma;       // 1: cmap describes C (TMA stores), 0: plain stores
     const uint16_t* bias;  // bf16 bias[N] added to every row (16-byte aligned), or null
     uint32_t* err;
+    // Output quantization (pair kernel, bf16 output through TMA stores): the MXFP4 blobs
+    // of C, scales in the tensor-core layout; qo_col null: row blob only.
+    uint8_t* qo_row;     // [M, Np/2]
+    uint8_t* so_row;     // scales of the row blob, (M, N)
+    uint8_t* qo_col;     // [N, Mp/2]
+    uint8_t* so_col;     // scales of the col blob, (N, M)
+    int64_t ldqo_row;    // Np / 2
+    int64_t ldqo_col;    // Mp / 2
+    int32_t kb4o_row;    // Np / 128: scale atoms along N
+    int32_t kb4o_col;    // Mp / 128: scale atoms along M
 };
 
 size_t gemm_smem_bytes();
@@ -96,7 +106,9 @@ struct GemmPairBatch {
 };
 size_t gemm_pair_smem_bytes();
 int gemm_pair_max_clusters();   // co-resident clusters of the pair kernel, 0 if none
-cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream);
+// quant: one problem (b.count == 1) whose epilogue also writes the MXFP4 blobs of C
+// (GemmArgs::qo_row ..); C in bf16 through TMA stores (c_tma).
+cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream, bool quant = false);
 
 // ---- diagnostics -----------------------------------------------------------------------
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t timeout_ns, cudaStream_t stream);

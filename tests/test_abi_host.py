@@ -86,6 +86,19 @@ def test_argument_checks_precede_any_device_use(lib):
     assert lib.mxfp4_quantize_dual_rht_sr(16, 4, 8, 8, 32, 48, 64, 80, 3, 7, 9, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_quantize_dual_2d(16, 4, 8, 8, 32, 48, None, 64, 1, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_quantize_dual_2d(18, 4, 8, 8, 32, 48, 64, 80, 1, None) == abi.MXFP4_ERR_MISALIGNED
+    ok = (16, 32, 48, 64, 300, 200, 264, None, 80, 200, 96, 112, 128, 144, None)
+    bad = list(ok)
+    bad[9] = 204                                                     # ldc not a multiple of 8
+    assert lib.mxfp4_gemm_quantize(*bad) == abi.MXFP4_ERR_MISALIGNED
+    bad = list(ok)
+    bad[10] = None                                                   # no row blob
+    assert lib.mxfp4_gemm_quantize(*bad) == abi.MXFP4_ERR_INVALID_ARG
+    bad = list(ok)
+    bad[13] = None                                                   # q_col without s_col
+    assert lib.mxfp4_gemm_quantize(*bad) == abi.MXFP4_ERR_INVALID_ARG
+    bad = list(ok)
+    bad[11] = 120                                                    # s_row not 16-byte aligned
+    assert lib.mxfp4_gemm_quantize(*bad) == abi.MXFP4_ERR_MISALIGNED
     G = abi.GemmTask
     g_ok = G(16, 32, 48, 64, 4, 4, 4, 80, 4, 0)
     garr = (G * 5)(*([g_ok] * 5))
@@ -154,6 +167,8 @@ def test_no_usable_device_fails_loudly(lib):
                                           None) in bad
     assert lib.mxfp4_gemm(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x50000, 4, 0, None) in bad
     assert lib.mxfp4_gemm_bias(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x60000, 0x50000, 4, 0, None) in bad
+    assert lib.mxfp4_gemm_quantize(0x10000, 0x20000, 0x30000, 0x40000, 4, 8, 4, None, 0x50000, 8, 0x60000, 0x70000,
+                                   None, None, None) in bad
     assert lib.mxfp4_fp8_quantize_tw(0x10000, 4, 8, 8, 0x20000, None, 0x30000, 0x30004, None) in bad
     assert lib.mxfp4_fp8_gemm(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x50000, 4, 0, None) in bad
     task = (abi.LinearHostTask * 1)(abi.LinearHostTask(0x1000, 0x2000, 0, 0x4000, 0, 0, 4, 8, 16, 0, 0))
