@@ -441,6 +441,13 @@ mxfp4_status mxfp4_gemm_quantize(const void* a_q, const void* a_s, const void* b
     g.ldqo_col = pad128(M) / 2;
     g.kb4o_row = static_cast<int32_t>(pad128(N) / 128);
     g.kb4o_col = static_cast<int32_t>(pad128(M) / 128);
+    if (!encode_2d(&b.qrowmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_row, static_cast<uint64_t>(pad128(N) / 2),
+                   static_cast<uint64_t>(M), static_cast<uint64_t>(pad128(N) / 2), 64, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        (q_col != nullptr &&
+         !encode_2d(&b.qcolmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, q_col, static_cast<uint64_t>(pad128(M) / 2),
+                    static_cast<uint64_t>(N), static_cast<uint64_t>(pad128(M) / 2), 16, 128,
+                    CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return MXFP4_ERR_CUDA;
     const int64_t tiles = b.tile_end[0];
     const int clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
     return mxfp4::launch_gemm_pair(b, clusters, s, true) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;

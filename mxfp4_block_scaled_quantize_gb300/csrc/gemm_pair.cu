@@ -60,6 +60,11 @@ struct PairSmem {
     uint8_t sfa[kStages][kSfaBytes];
     uint8_t sfb[kStages][kSfbBytes];
     uint8_t out[kEpiWarps][kOutBytes];
+    // output quantization: per epilogue warp, the row-blob codes of its 32 rows x 128
+    // columns (32 x 64 bytes, 64-byte swizzle) and the col-blob codes of its 128 columns x 32
+    // rows (128 x 16 bytes), each leaving in one tensor store
+    uint8_t qrow[kEpiWarps][kOutBytes];
+    uint8_t qcol[kEpiWarps][kOutBytes];
     uint64_t full[kStages];               // used in the leader: both CTAs' bytes
     uint64_t empty[kStages];              // each CTA: the leader's MMA commit
     uint64_t tmem_full;                   // each CTA: the leader's commit after a tile
@@ -87,8 +92,21 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                  : "memory");
 }
 
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t j) {
     return r * kOutRowBytes + ((j ^ ((r >> 1) & 3u)) << 4);
+}
+
+// Four 8 x 8 bf16 matrices from shared memory, transposed: lanes 8j .. 8j + 7 give the
+// addresses of the 8 rows (16 bytes each) of matrix j, and lane t receives in d[j] the
+// elements (row 2 (t % 4), column t / 4) (low half) and (row 2 (t % 4) + 1, column t / 4).
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t* d) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(addr));
 }
 
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
@@ -97,17 +115,19 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
     return v;
 }
 
-// Output quantization of one staged 32 x 32 piece of bf16 C (rows row0 .. row0 + 31 of the
-// warp, columns col .. col + 31): w holds this lane's row of the piece (bf16 pairs, even
+// Output quantization of one staged 32 x 32 piece c of bf16 C (rows row0 .. row0 + 31 of
+// the warp, columns col .. col + 31): w holds this lane's row of the piece (bf16 pairs, even
 // column low), `obuf` the same piece in shared memory (swz64 layout).  Row blob: the lane's
-// 32-element block, stored unless the row is past M; its scale byte (0 for a padding row)
-// goes to byte c of *srow.  Col blob (g.qo_col set): column col + lane, read back down the
-// 32 staged rows (rows past M count as 0), stored unless the column is past N, its scale
-// byte written straight into the tensor-core layout (0 for a padding column).  The
-// elements, scales and padding are those the quantizer gives for C's bf16 values.
+// 32-element block, its 16 code bytes staged as chunk c of row `lane` in `qrow` (swz64
+// layout), its scale byte (0 for a padding row) in byte c of *srow.  Col blob (g.qo_col
+// set): column col + lane, read back down the 32 staged rows (rows past M count as 0), its
+// 16 code bytes staged as row 32 c + lane of `qcol`, its scale byte written straight into
+// the tensor-core layout (0 for a padding column).  The elements, scales and padding are
+// those the quantizer gives for C's bf16 values; the tensor stores clip rows past M (row
+// blob) and columns past N (col blob).
 __device__ __forceinline__ void quantize_out_piece(const GemmArgs& g, const uint32_t* w, uint32_t obuf,
-                                                   int64_t row0, int64_t col, int c, int q, uint32_t lane,
-                                                   uint32_t* srow) {
+                                                   uint32_t qrow, uint32_t qcol, int64_t row0, int64_t col, int c,
+                                                   int q, uint32_t lane, uint32_t* srow) {
     const int64_t row = row0 + lane;
     uint32_t m = w[0];
 #pragma unroll
@@ -115,42 +135,81 @@ __device__ __forceinline__ void quantize_out_piece(const GemmArgs& g, const uint
     m = absmax2(m, m >> 16) & 0x7FFFu;   // even and odd columns folded: the block's amax
     const uint32_t rbyte = row < g.M ? scale_byte(m) : 0u;
     *srow |= rbyte << (8 * c);
-    if (row < g.M) {
+    {
         const uint64_t s2 = pack2(inv_scale_bits(rbyte), inv_scale_bits(rbyte));
-        *reinterpret_cast<uint4*>(g.qo_row + row * g.ldqo_row + (col >> 1)) =
-            make_uint4(encode8(w[0], w[1], w[2], w[3], s2), encode8(w[4], w[5], w[6], w[7], s2),
-                       encode8(w[8], w[9], w[10], w[11], s2), encode8(w[12], w[13], w[14], w[15], s2));
+        sts128(qrow + swz64(lane, c), encode8(w[0], w[1], w[2], w[3], s2), encode8(w[4], w[5], w[6], w[7], s2),
+               encode8(w[8], w[9], w[10], w[11], s2), encode8(w[12], w[13], w[14], w[15], s2));
     }
     if (g.qo_col == nullptr) return;
+    const int64_t n_pad = (g.N + 127) & ~int64_t{127};
+    if (row0 + 32 <= g.M) {
+        // The usual case, every row of the block a row of C: four transposing matrix loads
+        // give lane t the row pairs (8 rb + 2 (t % 4), + 1), rb = 0..3, of the piece's columns
+        // 8 cb + t / 4, cb = 0..3.  A column's amax is folded over its four lanes, and its
+        // codes -- lane t % 4 = q' holding bytes 4 rb + q' -- are transposed across those
+        // lanes so that lane q' holds bytes 4 q' .. 4 q' + 3.
+        uint32_t wc[4][4];   // [cb][rb]
+#pragma unroll
+        for (int rb = 0; rb < 4; ++rb) {
+            uint32_t d[4];
+            ldsm_x4_trans(obuf + swz64(8 * rb + (lane & 7u), lane >> 3), d);
+#pragma unroll
+            for (int cb = 0; cb < 4; ++cb) wc[cb][rb] = d[cb];
+        }
+        uint32_t mc[4];
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            const uint32_t m4 = absmax2(absmax2(wc[cb][0], wc[cb][1]), absmax2(wc[cb][2], wc[cb][3]));
+            mc[cb] = absmax2(m4, m4 >> 16) & 0x7FFFu;
+        }
+        uint32_t p01 = mc[0] | (mc[1] << 16), p23 = mc[2] | (mc[3] << 16);
+        p01 = absmax2(p01, __shfl_xor_sync(0xFFFFFFFFu, p01, 1));
+        p23 = absmax2(p23, __shfl_xor_sync(0xFFFFFFFFu, p23, 1));
+        p01 = absmax2(p01, __shfl_xor_sync(0xFFFFFFFFu, p01, 2));
+        p23 = absmax2(p23, __shfl_xor_sync(0xFFFFFFFFu, p23, 2));
+        const uint32_t qq = lane & 3u;
+        const uint32_t sel_a = (qq & 1u) ? 0x3715u : 0x6240u, sel_b = (qq & 2u) ? 0x3276u : 0x5410u;
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            const uint32_t mm = (cb < 2 ? p01 : p23) >> (16 * (cb & 1));
+            const uint32_t cbyte = scale_byte(mm & 0xFFFFu);
+            const uint64_t s2 = pack2(inv_scale_bits(cbyte), inv_scale_bits(cbyte));
+            const uint32_t x = encode8(wc[cb][0], wc[cb][1], wc[cb][2], wc[cb][3], s2);
+            const uint32_t a = __byte_perm(x, __shfl_xor_sync(0xFFFFFFFFu, x, 1), sel_a);
+            const uint32_t y = __byte_perm(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2), sel_b);
+            const int64_t n = col + 8 * cb + (lane >> 2);
+            sts32(qcol + (32 * c + 8 * cb + (lane >> 2)) * 16 + 4 * qq, y);
+            if (qq == 0 && n < n_pad) {
+                const int64_t atom = (n >> 7) * g.kb4o_col + (row0 >> 7);
+                g.so_col[atom * 512 + (n & 31) * 16 + c * 4 + q] = static_cast<uint8_t>(n < g.N ? cbyte : 0u);
+            }
+        }
+        return;
+    }
+    // The block that straddles M: column `lane` read down the staged rows, rows past M as 0.
     const int64_t n = col + lane;
     const uint32_t base = obuf + ((lane & 7u) << 1);
     uint32_t cw[16];
-    if (row0 + 32 <= g.M) {   // the usual case: every row of the block is a row of C
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-            cw[k] = lds_u16(base + swz64(2 * k, lane >> 3)) | (lds_u16(base + swz64(2 * k + 1, lane >> 3)) << 16);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            uint32_t lo = lds_u16(base + swz64(2 * k, lane >> 3));
-            uint32_t hi = lds_u16(base + swz64(2 * k + 1, lane >> 3));
-            if (row0 + 2 * k >= g.M) lo = 0;
-            if (row0 + 2 * k + 1 >= g.M) hi = 0;
-            cw[k] = lo | (hi << 16);
-        }
+    for (int k = 0; k < 16; ++k) {
+        uint32_t lo = lds_u16(base + swz64(2 * k, lane >> 3));
+        uint32_t hi = lds_u16(base + swz64(2 * k + 1, lane >> 3));
+        if (row0 + 2 * k >= g.M) lo = 0;
+        if (row0 + 2 * k + 1 >= g.M) hi = 0;
+        cw[k] = lo | (hi << 16);
     }
     uint32_t mc = cw[0];
 #pragma unroll
     for (int i = 1; i < 16; ++i) mc = absmax2(mc, cw[i]);
     mc = absmax2(mc, mc >> 16) & 0x7FFFu;
     const uint32_t cbyte = scale_byte(mc);
-    if (n < g.N) {
+    {
         const uint64_t s2 = pack2(inv_scale_bits(cbyte), inv_scale_bits(cbyte));
-        *reinterpret_cast<uint4*>(g.qo_col + n * g.ldqo_col + (row0 >> 1)) =
-            make_uint4(encode8(cw[0], cw[1], cw[2], cw[3], s2), encode8(cw[4], cw[5], cw[6], cw[7], s2),
-                       encode8(cw[8], cw[9], cw[10], cw[11], s2), encode8(cw[12], cw[13], cw[14], cw[15], s2));
+        sts128(qcol + (32 * c + lane) * 16, encode8(cw[0], cw[1], cw[2], cw[3], s2),
+               encode8(cw[4], cw[5], cw[6], cw[7], s2), encode8(cw[8], cw[9], cw[10], cw[11], s2),
+               encode8(cw[12], cw[13], cw[14], cw[15], s2));
     }
-    if (n < ((g.N + 127) & ~int64_t{127})) {
+    if (n < n_pad) {
         const int64_t atom = (n >> 7) * g.kb4o_col + (row0 >> 7);
         g.so_col[atom * 512 + lane * 16 + c * 4 + q] = static_cast<uint8_t>(n < g.N ? cbyte : 0u);
     }
@@ -331,11 +390,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int h = (warp - kEpi0) >> 2;
         const uint32_t obuf = smem_addr(sm.out[warp - kEpi0]);
+        const uint32_t qrow_buf = smem_addr(sm.qrow[warp - kEpi0]);
+        const uint32_t qcol_buf = smem_addr(sm.qcol[warp - kEpi0]);
         const uint64_t pol = l2_policy_evict_first();
         const uint32_t leader_tmem_empty = cluster_map(smem_addr(&sm.tmem_empty), 0);
-        if (lane == 0)
+        if (lane == 0) {
             for (int j = 0; j < P.count; ++j)
                 if (P.args[j].c_tma) prefetch_tensormap(&P.cmap[j]);
+            if (kQuant) {
+                prefetch_tensormap(&P.qrowmap);
+                if (P.args[0].qo_col != nullptr) prefetch_tensormap(&P.qcolmap);
+            }
+        }
         int tl = 0;
         for (int t = cluster; t < num_tiles; t += nclusters, ++tl) {
             int okw = 1;
@@ -384,11 +450,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                           obuf, pol);
                         bulk_commit_group();
                     }
-                    quantize_out_piece(g, wb[c], obuf, row0, col0 + c * 32, c, q, lane, &srow);
+                    quantize_out_piece(g, wb[c], obuf, qrow_buf, qcol_buf, row0, col0 + c * 32, c, q, lane, &srow);
                 }
                 // the row's 4 scale bytes of this 128-column half, one word
                 const int64_t atom = ((row0 + lane) >> 7) * g.kb4o_row + (col0 >> 7);
                 *reinterpret_cast<uint32_t*>(g.so_row + atom * 512 + lane * 16 + q * 4) = srow;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (row0 < g.M)
+                        tma_store_2d_hint(&P.qrowmap, static_cast<int32_t>(col0 >> 1), static_cast<int32_t>(row0),
+                                          qrow_buf, pol);
+                    if (g.qo_col != nullptr)
+                        tma_store_2d_hint(&P.qcolmap, static_cast<int32_t>(row0 >> 1), static_cast<int32_t>(col0),
+                                          qcol_buf, pol);
+                    bulk_commit_group();
+                }
                 continue;
             }
             if (row0 >= g.M || col0 >= g.N) continue;

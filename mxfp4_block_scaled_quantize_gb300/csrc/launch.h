@@ -103,6 +103,10 @@ struct GemmPairBatch {
     GemmArgs args[kMaxGemmTasks];
     int32_t tile_end[kMaxGemmTasks];
     int32_t count;
+    // Output quantization of problem 0: its row blob as a 2-D u8 tensor {Np/2, M}, box
+    // {64, 32}, 64-byte swizzle; its col blob {Mp/2, N}, box {16, 128}, no swizzle.
+    CUtensorMap qrowmap;
+    CUtensorMap qcolmap;
 };
 size_t gemm_pair_smem_bytes();
 int gemm_pair_max_clusters();   // co-resident clusters of the pair kernel, 0 if none
