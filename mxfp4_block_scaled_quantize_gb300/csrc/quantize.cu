@@ -43,10 +43,11 @@
 // gradient quantizers): before the columnwise pass quantizes a column, each group of 16
 // consecutive rows becomes (1/4) H16 diag(s) of itself, s a sign mask of the task, computed
 // in fp32 -- signs, butterflies for h = 1, 2, 4, 8, then x 0.25 -- and the 32-row MX block is
-// quantized from these fp32 values.  The thread's rows sit in its registers in the order
-// r ^ 2rb; butterfly partners are XOR pairs in either order, and where the order swaps which
-// partner is the lower one (h = 2, 4, by the bits of rb) the sum and the difference (taken
-// lower minus upper in row order) land in each other's register.
+// quantized from these fp32 values.  For such a task a warp takes one 32-row block and 32
+// consecutive column pairs, so its shared reads are whole tile rows, conflict free in
+// natural row order, and each thread's registers hold its rows in order: the butterflies
+// are plain register pairs, with the difference taken lower minus upper row as the
+// definition has it.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -235,68 +236,102 @@ __device__ __forceinline__ void encode_cols8_sr(const uint32_t* w, float inv0, f
     *q1 = pack_e2m1x8(f1);
 }
 
-// One column of a 32-row block with the Hadamard transform: kHi picks the column of the
-// column pair (high or low halves of w); register i of w holds row (i & ~7) | ((i & 7) ^ 2rb)
-// and bit (i & 15) of psigns is the sign of that row's position in its 16-row group.  Gives
-// the block's scale byte from the transformed values and the codes, word g byte j holding
-// registers 8g + 2j (low nibble) and 8g + 2j + 1, like encode_cols8.  kSR: the scaled
-// transformed elements are stochastically rounded with the col-blob bits of Philox counter
-// (c0 + g, a, 1, 0) for register group g (c0: the block's first row / 8, a: the column).
-template <int kHi, bool kSR>
-__device__ __forceinline__ void rht_column(const uint32_t* w, uint32_t rb, uint32_t psigns, uint32_t* byte,
-                                           uint32_t* q, uint64_t seed, uint32_t c0, uint32_t a) {
-    float f[32];
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ float lo_f(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_f(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
+// The Hadamard transform of the two columns of a column pair over one 32-row block, register
+// i of w holding row i (column c0 in the low halves, c1 in the high halves); bit j of
+// `signs` negates row j of each 16-row group.  Both columns go through every fp32 step
+// together as pairs (packed adds, subtractions and multiplies, each rounding to nearest
+// even per lane, so each column gets exactly its own sequence).  Gives the two blocks'
+// scale bytes from the transformed values and their codes, word g byte j holding rows
+// 8g + 2j (low nibble) and 8g + 2j + 1.  kSR: the scaled transformed elements are
+// stochastically rounded with the col-blob bits of Philox counter (c0 + g, a + column, 1, 0)
+// for row group g (c0: the block's first row / 8, a: the pair's first column).
+template <bool kSR>
+__device__ __forceinline__ void rht_pair(const uint32_t* w, uint32_t signs, uint32_t* byte0, uint32_t* byte1,
+                                         uint32_t* q0, uint32_t* q1, uint64_t seed, uint32_t c0, uint32_t a) {
+    uint64_t f[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const float v = kHi ? bf16_hi(w[i]) : bf16_lo(w[i]);
-        f[i] = ((psigns >> (i & 15)) & 1u) ? -v : v;
+        const uint32_t sb = ((signs >> (i & 15)) & 1u) << 31;
+        f[i] = pack2((w[i] << 16) ^ sb, (w[i] & 0xFFFF0000u) ^ sb);
     }
-    const bool sw2 = (rb & 1u) != 0, sw4 = ((rb >> 1) & 1u) != 0;
 #pragma unroll
     for (int g = 0; g < 32; g += 16) {
 #pragma unroll
         for (int h = 1; h < 16; h <<= 1) {
-            // register order swaps the partners' roles for h = 2 (bit 0 of rb), h = 4 (bit 1)
-            const bool sw = (h == 2 && sw2) || (h == 4 && sw4);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 if (i & h) continue;
-                // lo / hi: the partners in row order (the difference is taken in that order:
-                // x - x is +0, so negating the other order's difference would give -0)
-                const float lo = sw ? f[g + i + h] : f[g + i], hi = sw ? f[g + i] : f[g + i + h];
-                const float s = __fadd_rn(lo, hi), d = __fsub_rn(lo, hi);
-                f[g + i] = sw ? d : s;
-                f[g + i + h] = sw ? s : d;
+                const uint64_t lo = f[g + i], hi = f[g + i + h];
+                f[g + i] = add2(lo, hi);
+                f[g + i + h] = sub2(lo, hi);
             }
         }
     }
-    float amax = 0.0f;
+    const uint64_t quarter = pack2(0x3E800000u, 0x3E800000u);   // 0.25
+    float m0 = 0.0f, m1 = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        f[i] = __fmul_rn(f[i], 0.25f);
-        amax = fmaxf(amax, fabsf(f[i]));
+        f[i] = mul2(f[i], quarter);
+        m0 = fmaxf(m0, fabsf(lo_f(f[i])));
+        m1 = fmaxf(m1, fabsf(hi_f(f[i])));
     }
-    const uint32_t ef = (__float_as_uint(amax) >> 23) & 0xFFu;   // floor(log2) + 127 of a normal amax
-    const uint32_t b = max(ef, 2u) - 2u;
-    *byte = b;
-    const float inv = __uint_as_float(inv_scale_bits(b));
+    // floor(log2) + 127 of a normal amax
+    const uint32_t b0 = max((__float_as_uint(m0) >> 23) & 0xFFu, 2u) - 2u;
+    const uint32_t b1 = max((__float_as_uint(m1) >> 23) & 0xFFu, 2u) - 2u;
+    *byte0 = b0;
+    *byte1 = b1;
+    float g0[8], g1[8];
     if (kSR) {
+        const float inv0 = __uint_as_float(inv_scale_bits(b0)), inv1 = __uint_as_float(inv_scale_bits(b1));
 #pragma unroll
         for (int gw = 0; gw < 4; ++gw) {
-            uint32_t pw[4];
-            words_in_register_order(philox4x32_10(c0 + gw, a, 1u, seed), rb, pw);
+            const uint4 r0 = philox4x32_10(c0 + gw, a, 1u, seed);
+            const uint4 r1 = philox4x32_10(c0 + gw, a + 1u, 1u, seed);
+            const uint32_t p0[4] = {r0.x, r0.y, r0.z, r0.w}, p1[4] = {r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float y = f[8 * gw + i];
-                f[8 * gw + i] = sr_round(__fmul_rn(fabsf(y), inv), y, rnd16(pw[i >> 1], i & 1));
+                const float y0 = lo_f(f[8 * gw + i]), y1 = hi_f(f[8 * gw + i]);
+                g0[i] = sr_round(__fmul_rn(fabsf(y0), inv0), y0, rnd16(p0[i >> 1], i & 1));
+                g1[i] = sr_round(__fmul_rn(fabsf(y1), inv1), y1, rnd16(p1[i >> 1], i & 1));
             }
+            q0[gw] = pack_e2m1x8(g0);
+            q1[gw] = pack_e2m1x8(g1);
         }
     } else {
+        const uint64_t inv2 = pack2(inv_scale_bits(b0), inv_scale_bits(b1));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) f[i] = __fmul_rn(f[i], inv);
+        for (int gw = 0; gw < 4; ++gw) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint64_t y = mul2(f[8 * gw + i], inv2);
+                g0[i] = lo_f(y);
+                g1[i] = hi_f(y);
+            }
+            q0[gw] = pack_e2m1x8(g0);
+            q1[gw] = pack_e2m1x8(g1);
+        }
     }
-#pragma unroll
-    for (int gw = 0; gw < 4; ++gw) q[gw] = pack_e2m1x8(&f[8 * gw]);
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -477,41 +512,36 @@ __global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
         //      read on four disjoint bank groups; the code bytes come out permuted by
         //      XOR rb and one byte permute puts them back.
         if (kDual) {
-            const int pc = 8 * warp + (lane & 7), rb = lane >> 3;
+            // A task with the transform maps threads differently: warp w takes row block
+            // w % 4 and 32 consecutive column pairs, so each shared read is one whole tile row
+            // (conflict free in natural row order) and the butterflies pair registers the way
+            // they pair rows.
+            const bool rht_task = kRecipes && p.rht;
+            const int pc = rht_task ? 32 * (warp >> 2) + lane : 8 * warp + (lane & 7);
+            const int rb = rht_task ? (warp & 3) : (lane >> 3);
+            const int xo = rht_task ? 0 : 2 * rb;   // register k of an 8-row group holds row k ^ xo
             const uint32_t box = tile + (pc >> 5) * kQBoxBytes;
             const int jc = (pc & 31) >> 2;
             const uint32_t inner = (pc & 3) * 4;
-            // Offsets of rows (k ^ 2rb), k = 0..7, of each 8-row group; the group offset is a
+            // Offsets of rows (k ^ xo), k = 0..7, of each 8-row group; the group offset is a
             // compile-time constant of every load.
             uint32_t toff[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const int rr = k ^ (2 * rb);
+                const int rr = k ^ xo;
                 toff[k] = box + rb * 32 * 128 + rr * 128 + ((jc ^ rr) << 4) + inner;
             }
             uint32_t w[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) w[i] = lds32(toff[i & 7] + (i & ~7) * 128);
-            const uint32_t sel = 0x3210u ^ (0x1111u * static_cast<uint32_t>(rb));
+            const uint32_t sel = 0x3210u ^ (0x1111u * static_cast<uint32_t>(xo >> 1));
             const int64_t kc = k0 + 2 * pc;
             uint32_t byte0, byte1;
             uint32_t q0[4], q1[4];
-            if (kRecipes && p.rht) {
-                // sign of register position r of a 16-row group: bit (r & 8) | ((r & 7) ^ 2rb)
-                uint32_t psigns = 0;
-#pragma unroll
-                for (int r2 = 0; r2 < 16; ++r2)
-                    psigns |= ((p.rht_signs >> ((r2 & 8) | ((r2 & 7) ^ (2 * rb)))) & 1u) << r2;
+            if (rht_task) {
+                // natural row order: register i holds row i of the block
                 const uint32_t c0 = static_cast<uint32_t>((m0 + rb * 32) >> 3);
-                rht_column<0, kSR>(w, static_cast<uint32_t>(rb), psigns, &byte0, q0, p.seed, c0,
-                                   static_cast<uint32_t>(kc));
-                rht_column<1, kSR>(w, static_cast<uint32_t>(rb), psigns, &byte1, q1, p.seed, c0,
-                                   static_cast<uint32_t>(kc + 1));
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    q0[j] = __byte_perm(q0[j], 0, sel);
-                    q1[j] = __byte_perm(q1[j], 0, sel);
-                }
+                rht_pair<kSR>(w, p.rht_signs, &byte0, &byte1, q0, q1, p.seed, c0, static_cast<uint32_t>(kc));
             } else {
             if (blk2d) {
                 // both columns lie in block column pc / 16 of row group rb
