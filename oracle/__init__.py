@@ -80,6 +80,10 @@ def _load():
         lib.oracle_quantize_col_rht.restype = ctypes.c_int
         lib.oracle_quantize_col_rht_sr.argtypes = [vp, i64, i64, i64, ctypes.c_uint32, vp, vp, ctypes.c_uint64, vp]
         lib.oracle_quantize_col_rht_sr.restype = ctypes.c_int
+        lib.oracle_qk_norm_rope_fwd.argtypes = [vp, vp, vp, vp, vp, f64, i64, i64, i64, vp, vp]
+        lib.oracle_qk_norm_rope_fwd.restype = None
+        lib.oracle_qk_norm_rope_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, vp]
+        lib.oracle_qk_norm_rope_bwd.restype = None
         _lib = lib
     return _lib
 
@@ -410,3 +414,33 @@ def quantize_col_rht_sr(x_bits, signs, seed, col_ids=None):
                                           int(seed) & (2**64 - 1), None if ids is None else _ptr(ids)):
         raise ValueError("non-finite input or transform")
     return q, s
+
+
+# --- QK RMSNorm + interleaved RoPE backward (the quantizer prologue) -----------------------
+
+def qk_norm_rope_fwd(mixed, wq, wk, cos, sin, H, D, eps=1e-6):
+    """Forward of the norm + RoPE over fp64 mixed[M, H*3*D]: (out [M, H*3*D] with v copied,
+    r [M, H, 2] the saved 1/sqrt(mean(x^2) + eps) of q and k)."""
+    mixed = np.ascontiguousarray(mixed, dtype=np.float64)
+    M = mixed.shape[0]
+    assert mixed.shape[1] == 3 * H * D
+    c = [np.ascontiguousarray(a, dtype=np.float64) for a in (wq, wk, cos, sin)]
+    out = np.empty_like(mixed)
+    r = np.empty((M, H, 2), np.float64)
+    _load().oracle_qk_norm_rope_fwd(_ptr(mixed), *(_ptr(a) for a in c), float(eps), M, H, D, _ptr(out), _ptr(r))
+    return out, r
+
+
+def qk_norm_rope_bwd(g_bits, x_bits, r, wq, wk, cos, sin, H, D):
+    """d(mixed_qkv) [M, H*3*D] in fp64 from bf16 g (the gradient of the norm + RoPE output,
+    v part: the gradient of v) and x (mixed_qkv), the saved r [M, H, 2] and the fp32 norm
+    weights and RoPE tables."""
+    g_bits = np.ascontiguousarray(g_bits, dtype=np.uint16)
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M = g_bits.shape[0]
+    assert g_bits.shape == x_bits.shape == (M, 3 * H * D)
+    f = [np.ascontiguousarray(a, dtype=np.float32) for a in (r, wq, wk, cos, sin)]
+    out = np.empty((M, 3 * H * D), np.float64)
+    _load().oracle_qk_norm_rope_bwd(_ptr(g_bits), _ptr(x_bits), *(_ptr(a) for a in f), M, H, D, _ptr(out))
+    return out
+

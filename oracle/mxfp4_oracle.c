@@ -27,7 +27,7 @@
  *   clamped to the E8M0 range [-127, 127]; an all-zero block gets the byte 0x00;
  *   element = round-to-nearest-even of v / 2^e onto {0, 0.5, 1, 1.5, 2, 3, 4, 6},
  *   saturating at 6.
- * Readings taken where that rule is silent (each is listed in the design notes):
+ * Readings taken where that rule is silent:
  *   - the sign of an element that rounds to zero is kept (-0 encodes as 0x8);
  *   - padding elements are +0, so an all-padding block gets the byte 0x00;
  *   - the low nibble of byte j holds element 2j, the high nibble element 2j+1;
@@ -565,7 +565,7 @@ int oracle_quantize_col_2d(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
  * in primus_turbo_mxfp4_local.py set `colwise_use_rht` for activations and gradients (the
  * weights use 2-D blocks instead).  Those column blobs are exactly the two operands of the
  * wgrad GEMM dW = dY^T . X, whose reduction runs over M.  The pages name the flag only;
- * reading taken (each point listed in the design notes as well):
+ * reading taken:
  *   - T = (1/4) H16 diag(s) is applied to every group of 16 consecutive elements of a
  *     zero-padded column of X (rows 16g .. 16g + 15, g = 0 .. Mp/16 - 1), H16 the Sylvester
  *     Hadamard matrix (H[i][j] = (-1)^popcount(i & j)) and s a sign vector given by the
@@ -650,3 +650,86 @@ int oracle_quantize_col_rht_sr(const uint16_t* x, int64_t M, int64_t K, int64_t 
     free(col);
     return 0;
 }
+
+/* ---------------------------------------------------------------------------------------
+ * QK RMSNorm + interleaved RoPE backward, the producer computed in the quantizer's staging
+ * read: the pages' MXFP6 QKV packer prologue (`MXFP6QKVNormRopeFunction`: "the packer
+ * computes d(mixed_qkv) during its staging read"; fused_norm_rope.py: QK RMSNorm and the
+ * interleaved RoPE rotation, q and k read as strided slices of mixed_qkv at stride 3D, v
+ * copied, never rotated).  Reading taken (the pages name the ops, not their formulas):
+ *   - mixed_qkv[M, H*3*D]: for token m and head h, columns h*3D .. h*3D+D-1 are q, the next
+ *     D are k, the next D are v;
+ *   - forward for p in {q, k}: x = mixed[m, h, p, :]; r = 1/sqrt(mean(x^2) + eps) (saved by
+ *     the forward); n = x r; y = n * w_p (w_q, w_k: the norm weights, [D]); interleaved RoPE
+ *     on pairs (2i, 2i+1) with c = cos[m, i], s = sin[m, i]:
+ *     o[2i] = y[2i] c - y[2i+1] s,  o[2i+1] = y[2i] s + y[2i+1] c;  v passes through;
+ *   - backward, given g = dL/do in the same layout and the saved r:
+ *     dy[2i] = g[2i] c + g[2i+1] s,  dy[2i+1] = -g[2i] s + g[2i+1] c;  dn = dy * w;
+ *     dx = r dn - (r^3 / D) x sum_j(dn_j x_j);  d(mixed) for v is g itself.
+ *     (dx is the derivative of o through n = x r(x); the norm weights' own gradient is a
+ *     separate reduction, not part of d(mixed_qkv).)
+ * The forward is here only to pin the backward (a numerical derivative of it); the product
+ * computes the backward alone.
+ * -------------------------------------------------------------------------------------- */
+
+/* Forward of the norm + RoPE over mixed[M, H*3*D] (fp64 values): out in the same layout (v
+ * copied), r_out[M, H, 2] the saved 1/sqrt(mean(x^2) + eps) of q and k. */
+void oracle_qk_norm_rope_fwd(const double* mixed, const double* wq, const double* wk, const double* cosv,
+                             const double* sinv, double eps, int64_t M, int64_t H, int64_t D, double* out,
+                             double* r_out) {
+    const int64_t ld = 3 * H * D;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t h = 0; h < H; ++h) {
+            for (int p = 0; p < 2; ++p) {
+                const double* x = mixed + m * ld + h * 3 * D + p * D;
+                const double* w = p == 0 ? wq : wk;
+                double* o = out + m * ld + h * 3 * D + p * D;
+                double ss = 0.0;
+                for (int64_t j = 0; j < D; ++j) ss += x[j] * x[j];
+                const double r = 1.0 / sqrt(ss / (double)D + eps);
+                r_out[(m * H + h) * 2 + p] = r;
+                for (int64_t i = 0; i < D / 2; ++i) {
+                    const double c = cosv[m * (D / 2) + i], sn = sinv[m * (D / 2) + i];
+                    const double y0 = x[2 * i] * r * w[2 * i], y1 = x[2 * i + 1] * r * w[2 * i + 1];
+                    o[2 * i] = y0 * c - y1 * sn;
+                    o[2 * i + 1] = y0 * sn + y1 * c;
+                }
+            }
+            for (int64_t j = 0; j < D; ++j) out[m * ld + h * 3 * D + 2 * D + j] = mixed[m * ld + h * 3 * D + 2 * D + j];
+        }
+}
+
+/* Backward: g and x bf16 [M, H*3*D] (x = mixed_qkv, the forward's input), r[M, H, 2] (fp32,
+ * as saved), w_q / w_k [D] and cos / sin [M, D/2] (fp32); out: d(mixed_qkv) [M, H*3*D] in
+ * fp64. */
+void oracle_qk_norm_rope_bwd(const uint16_t* g, const uint16_t* x, const float* r, const float* wq,
+                             const float* wk, const float* cosv, const float* sinv, int64_t M, int64_t H,
+                             int64_t D, double* out) {
+    const int64_t ld = 3 * H * D;
+    double* dn = (double*)malloc((size_t)D * sizeof(double));
+    if (!dn) return;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t h = 0; h < H; ++h) {
+            for (int p = 0; p < 2; ++p) {
+                const int64_t base = m * ld + h * 3 * D + p * D;
+                const float* w = p == 0 ? wq : wk;
+                const double rr = (double)r[(m * H + h) * 2 + p];
+                for (int64_t i = 0; i < D / 2; ++i) {
+                    const double c = (double)cosv[m * (D / 2) + i], sn = (double)sinv[m * (D / 2) + i];
+                    const double g0 = oracle_bf16_to_f64(g[base + 2 * i]), g1 = oracle_bf16_to_f64(g[base + 2 * i + 1]);
+                    dn[2 * i] = (g0 * c + g1 * sn) * (double)w[2 * i];
+                    dn[2 * i + 1] = (-g0 * sn + g1 * c) * (double)w[2 * i + 1];
+                }
+                double dot = 0.0;
+                for (int64_t j = 0; j < D; ++j) dot += dn[j] * oracle_bf16_to_f64(x[base + j]);
+                for (int64_t j = 0; j < D; ++j)
+                    out[base + j] = rr * dn[j] - rr * rr * rr / (double)D * oracle_bf16_to_f64(x[base + j]) * dot;
+            }
+            for (int64_t j = 0; j < D; ++j) {
+                const int64_t k = m * ld + h * 3 * D + 2 * D + j;
+                out[k] = oracle_bf16_to_f64(g[k]);
+            }
+        }
+    free(dn);
+}
+

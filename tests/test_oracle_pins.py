@@ -929,3 +929,68 @@ def test_rht_sr_brute_force_from_the_pinned_parts():
                 want = oracle.e2m1_encode_sr(float(np.ldexp(blk[i], 127 - byte)), r)
                 got = (q[k, m // 2] >> (4 * (m % 2))) & 0xF
                 assert got == want, (k, m)
+
+
+# --- QK RMSNorm + interleaved RoPE backward (the quantizer prologue) ----------------------
+
+def _norm_rope_case(M, H, D, seed):
+    rng = np.random.default_rng(seed)
+    x = oracle.round_to_bf16(rng.standard_normal((M, 3 * H * D)) * 0.7)
+    g = oracle.round_to_bf16(rng.standard_normal((M, 3 * H * D)) * 1e-2)
+    wq = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    wk = rng.uniform(0.5, 1.5, D).astype(np.float32)
+    theta = rng.uniform(-np.pi, np.pi, (M, D // 2))
+    return x, g, wq, wk, np.cos(theta).astype(np.float32), np.sin(theta).astype(np.float32)
+
+
+def test_qk_norm_rope_bwd_is_the_derivative_of_the_forward():
+    # Against central differences of the forward (the function itself, with r recomputed
+    # from the perturbed x): the backward's d(mixed) is the gradient of sum(g * out), along
+    # random directions and along single elements of q, k and v in every head.
+    M, H, D = 3, 2, 16
+    xb, gb, wq, wk, cs, sn = _norm_rope_case(M, H, D, 41)
+    x = f32_bits_to_bf16_values(xb)
+    g = f32_bits_to_bf16_values(gb)
+    _, r = oracle.qk_norm_rope_fwd(x, wq, wk, cs, sn, H, D)
+    dx = oracle.qk_norm_rope_bwd(gb, xb, r.astype(np.float32), wq, wk, cs, sn, H, D)
+
+    def loss(xx):
+        o, _ = oracle.qk_norm_rope_fwd(xx, wq, wk, cs, sn, H, D)
+        return float(np.sum(g * o))
+    h = 1e-5
+    rng = np.random.default_rng(7)
+    for _ in range(6):
+        d = rng.standard_normal(x.shape)
+        num = (loss(x + h * d) - loss(x - h * d)) / (2 * h)
+        assert abs(num - float(np.sum(dx * d))) <= 1e-6 * (abs(num) + 1e-3)
+    for m in range(M):
+        for col in (0, 5, D + 3, 2 * D + 1, 3 * D + 7, 4 * D + 15, 5 * D):
+            d = np.zeros_like(x)
+            d[m, col] = 1.0
+            num = (loss(x + h * d) - loss(x - h * d)) / (2 * h)
+            assert abs(num - dx[m, col]) <= 1e-6 * (abs(num) + 1e-3), (m, col)
+
+
+def test_qk_norm_rope_bwd_special_cases():
+    M, H, D = 2, 3, 8
+    xb, gb, wq, wk, cs, sn = _norm_rope_case(M, H, D, 3)
+    r = np.full((M, H, 2), 1.25, np.float32)
+    # v is passed through exactly
+    dx = oracle.qk_norm_rope_bwd(gb, xb, r, wq, wk, cs, sn, H, D)
+    for h in range(H):
+        v = slice(h * 3 * D + 2 * D, h * 3 * D + 3 * D)
+        assert np.array_equal(dx[:, v], f32_bits_to_bf16_values(gb)[:, v])
+    # no rotation, unit weights, g orthogonal to x: d(mixed) = r g exactly
+    ones, zeros = np.ones(D, np.float32), np.zeros((M, D // 2), np.float32)
+    x = np.zeros((M, 3 * H * D))
+    g = np.zeros((M, 3 * H * D))
+    for h in range(H):
+        for p in range(2):
+            x[:, h * 3 * D + p * D] = 1.0
+            g[:, h * 3 * D + p * D + 1 + p] = 0.5 + h
+    dx = oracle.qk_norm_rope_bwd(oracle.round_to_bf16(g), oracle.round_to_bf16(x), r, ones, ones,
+                                 np.ones((M, D // 2), np.float32), zeros, H, D)
+    for h in range(H):
+        for p in range(2):
+            sl = slice(h * 3 * D + p * D, h * 3 * D + p * D + D)
+            assert np.array_equal(dx[:, sl], 1.25 * g[:, sl])
