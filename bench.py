@@ -488,8 +488,9 @@ def run_extras(args, dev, flush_l2, head_start):
     """Lines for the other Flux configs, timed the same way: the QKV projection forward with
     row-only quantization (X[4608,3072], W[9216,3072]), the quantizer bandwidth sweep
     (dual quantization of M x K bf16 tensors for every M in {4608, 18432, 4600} and K in
-    {3072, 12288, 15360}; the largest, 18432 x 15360, moves 867 MB) and the forward GEMM
-    that quantizes its own output against the GEMM plus a quantizer launch."""
+    {3072, 12288, 15360}; the largest, 18432 x 15360, moves 867 MB), the forward GEMM that
+    quantizes its own output against the GEMM plus a quantizer launch, and the QKV
+    gradient's quantization with the norm + RoPE backward in its staging read."""
     import torch
 
     from mxfp4_block_scaled_quantize_gb300 import abi, workloads
@@ -602,6 +603,51 @@ def run_extras(args, dev, flush_l2, head_start):
     res["shape"] = f"{lin.M}x{lin.N}x{lin.K}"
     out["fwd_gemm_with_output_blobs"] = res
     del aq, a_s, bq, b_s, c, rq, rs, cq, cs
+
+    # The QKV projection's gradient quantization with the QK RMSNorm + interleaved RoPE
+    # backward in the staging read (the pages' QKV packer prologue): Flux QKV, 4608 tokens,
+    # 24 heads of 128 (d(mixed_qkv) [4608, 9216]), against the plain dual quantizer over a
+    # d(mixed_qkv) already in HBM.
+    M, H = 4608, 24
+    K = 3 * H * 128
+    gen.manual_seed(77)
+    g = (torch.randn((M, K), generator=gen, device=dev) * 1e-3).to(torch.bfloat16)
+    x = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
+    rstd = torch.rand((M, H, 2), generator=gen, device=dev) + 0.5
+    wq = torch.rand((128,), generator=gen, device=dev) + 0.5
+    wk = torch.rand((128,), generator=gen, device=dev) + 0.5
+    theta = (torch.rand((M, 64), generator=gen, device=dev) - 0.5) * 6.283
+    cos_t, sin_t = torch.cos(theta).contiguous(), torch.sin(theta).contiguous()
+    rq, rs = abi.alloc_blob(M, K, device=dev)
+    cq, cs = abi.alloc_blob(K, M, device=dev)
+
+    def prolog():
+        abi.mxfp4_quantize_dual_qk_norm_rope_bwd(g, x, M, H, rstd, wq, wk, cos_t, sin_t, rq, rs, cq, cs)
+
+    def plain_dual():
+        abi.mxfp4_quantize_dual(g, M, K, K, rq, rs, cq, cs, abi.MXFP4_SCALE_TC)
+    res = {}
+    for name, fn in (("fused_norm_rope_bwd_quantize", prolog), ("plain_dual_quantize", plain_dual)):
+        for _ in range(3):
+            fn()
+        ms = []
+        for _ in range(n):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ms.append((e0, e1))
+        torch.cuda.synchronize()
+        res[name] = summarize([a.elapsed_time(b) for a, b in ms])
+    # algorithmic bytes of the fused kernel: g read, x read for q and k, both blobs written
+    nb = M * K * (2 + 2 * 2 / 3 + 2 * (0.5 + 1 / 32)) + M * 64 * 8 + M * H * 8
+    gbs = nb / (res["fused_norm_rope_bwd_quantize"]["median_us"] * 1e-6) / 1e9
+    res["fused_gbs"] = round(gbs, 1)
+    res["fused_frac_of_hbm"] = round(gbs / peaks["hbm_gbs"], 4)
+    res["shape"] = f"d(mixed_qkv) {M}x{K}, {H} heads of 128"
+    out["qkv_bwd_quantize_with_norm_rope_prologue"] = res
+    del g, x, rstd, wq, wk, cos_t, sin_t, rq, rs, cq, cs
     if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
         raise RuntimeError("device error word set during the extra lines")
     return out

@@ -164,6 +164,34 @@ mxfp4_status mxfp4_quantize_dual_rht_sr(const void* x, int64_t M, int64_t K, int
                                         mxfp4_scale_layout layout, uint32_t signs, uint64_t seed,
                                         mxfp4_stream_t stream);
 
+/* The gradient quantization of the QKV projection with the QK RMSNorm + interleaved RoPE
+ * backward computed in the quantizer's staging read: the prologue of the pages' QKV packer
+ * (`MXFP6QKVNormRopeFunction`: "the packer computes d(mixed_qkv) during its staging read
+ * instead of the norm+RoPE backward writing it to HBM for the quantizer to read straight
+ * back"; fused_norm_rope.py: q and k read as strided slices of mixed_qkv at stride 3D, the
+ * interleaved rotation, v copied).  Head dimension 128.  With K = 3*H*128:
+ *   g       bf16 [M, K]: the gradient of the norm + RoPE output, per token and head the
+ *           columns h*384 .. h*384+127 for q, the next 128 for k, the next 128 for v (v's
+ *           gradient itself); row pitch K
+ *   x       bf16 [M, K]: mixed_qkv, the projection's output the forward normalized (same
+ *           layout; only its q and k columns are read)
+ *   rstd    fp32 [M, H, 2]: the forward's 1/sqrt(mean(x^2) + eps) of q (0) and k (1)
+ *   wq, wk  fp32 [128]: the norm weights; cos_table, sin_table fp32 [M, 64]: the RoPE angles
+ *           of each token, pair i rotating elements (2i, 2i+1)
+ * What is quantized: d(mixed_qkv)[M, K] with, for q and k, dy = the inverse rotation of g,
+ * dn = dy * w, dx = r dn - (r^3/128) x sum(dn x), computed in fp32 and rounded once to bf16
+ * (to nearest even), and for v the gradient g; the outputs are exactly those of
+ * mxfp4_quantize_dual over that bf16 d(mixed_qkv), which is also written to `dmixed`
+ * (bf16 [M, K], pitch K) when it is not NULL.  Alignment: g, x, cos_table, sin_table and
+ * dmixed 16 bytes, rstd, wq, wk 4 bytes; blobs and layouts as mxfp4_quantize_dual.  H >= 1;
+ * errors as mxfp4_quantize_dual. */
+mxfp4_status mxfp4_quantize_dual_qk_norm_rope_bwd(const void* g, const void* x, int64_t M, int64_t H,
+                                                  const float* rstd, const float* wq, const float* wk,
+                                                  const float* cos_table, const float* sin_table,
+                                                  void* q_row, void* s_row, void* q_col, void* s_col,
+                                                  mxfp4_scale_layout layout, void* dmixed,
+                                                  mxfp4_stream_t stream);
+
 /* Bits of mxfp4_quantize_task::flags. */
 #define MXFP4_QUANT_2D_BLOCKS 1   /* 32 x 32 blocks, as mxfp4_quantize_dual_2d (row-only too) */
 #define MXFP4_QUANT_RHT_COL 2     /* col blob transformed, as mxfp4_quantize_dual_rht (dual only) */

@@ -79,6 +79,7 @@ EXPORTED = (
     "mxfp4_quantize_dual_2d",
     "mxfp4_quantize_dual_rht",
     "mxfp4_quantize_dual_rht_sr",
+    "mxfp4_quantize_dual_qk_norm_rope_bwd",
     "mxfp4_quantize_batch",
     "mxfp4_gemm",
     "mxfp4_gemm_bias",
@@ -125,6 +126,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_quantize_dual_rht.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, ctypes.c_uint32, vp]
     lib.mxfp4_quantize_dual_rht_sr.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, i32, ctypes.c_uint32,
                                                ctypes.c_uint64, vp]
+    lib.mxfp4_quantize_dual_qk_norm_rope_bwd.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                         vp, vp]
     lib.mxfp4_quantize_batch.argtypes = [i32, ctypes.POINTER(QuantizeTask), i32, i32, vp]
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_gemm_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i32, vp]
@@ -223,6 +226,30 @@ def mxfp4_quantize_dual_rht_sr(x, M, K, ldx, q_row, s_row, q_col, s_col, layout=
                                              _ptr(s_col), layout, int(signs) & 0xFFFF, int(seed) & (2**64 - 1),
                                              _stream(stream)),
            "mxfp4_quantize_dual_rht_sr")
+
+
+def mxfp4_quantize_dual_qk_norm_rope_bwd(g, x, M, H, rstd, wq, wk, cos_table, sin_table, q_row, s_row, q_col,
+                                         s_col, layout=MXFP4_SCALE_TC, dmixed=None, stream=None) -> None:
+    _check(load().mxfp4_quantize_dual_qk_norm_rope_bwd(
+        _ptr(g), _ptr(x), M, H, _ptr(rstd), _ptr(wq), _ptr(wk), _ptr(cos_table), _ptr(sin_table), _ptr(q_row),
+        _ptr(s_row), _ptr(q_col), _ptr(s_col), layout, _ptr(dmixed), _stream(stream)),
+        "mxfp4_quantize_dual_qk_norm_rope_bwd")
+
+
+def quantize_qk_norm_rope_bwd(g, x, rstd, wq, wk, cos_table, sin_table, H, layout=MXFP4_SCALE_TC,
+                              with_dmixed=False, stream=None):
+    """Dual blobs of d(mixed_qkv) computed from the gradient g of the QK norm + RoPE output
+    (bf16 [M, H*384], CUDA) in the quantizer's staging read: (row_q, row_s, col_q, col_s) and,
+    with with_dmixed, the bf16 d(mixed_qkv) itself."""
+    import torch
+    M, K = g.shape
+    assert K == 3 * H * 128 and x.shape == g.shape and g.dtype == x.dtype == torch.bfloat16
+    rq, rs = alloc_blob(M, K, layout, g.device)
+    cq, cs = alloc_blob(K, M, layout, g.device)
+    dm = torch.empty_like(g) if with_dmixed else None
+    mxfp4_quantize_dual_qk_norm_rope_bwd(g, x, M, H, rstd, wq, wk, cos_table, sin_table, rq, rs, cq, cs, layout, dm,
+                                         stream)
+    return (rq, rs, cq, cs, dm) if with_dmixed else (rq, rs, cq, cs)
 
 
 def mxfp4_quantize_batch(tasks, dual: bool, layout=MXFP4_SCALE_TC, stream=None) -> None:

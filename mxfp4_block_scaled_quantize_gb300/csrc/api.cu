@@ -365,6 +365,54 @@ mxfp4_status mxfp4_quantize_dual_rht_sr(const void* x, int64_t M, int64_t K, int
                            reinterpret_cast<cudaStream_t>(stream), true, seed, MXFP4_QUANT_RHT_COL, signs);
 }
 
+mxfp4_status mxfp4_quantize_dual_qk_norm_rope_bwd(const void* g, const void* x, int64_t M, int64_t H,
+                                                  const float* rstd, const float* wq, const float* wk,
+                                                  const float* cos_table, const float* sin_table, void* q_row,
+                                                  void* s_row, void* q_col, void* s_col, mxfp4_scale_layout layout,
+                                                  void* dmixed, mxfp4_stream_t stream) {
+    if (H < 1 || H > kMaxDim / (3 * mxfp4::kNormRopeD)) return MXFP4_ERR_INVALID_ARG;
+    const int64_t K = 3 * H * mxfp4::kNormRopeD;
+    mxfp4_status st = quantize_check(g, M, K, K, q_row, s_row, q_col, s_col, layout, true);
+    if (st != MXFP4_OK) return st;
+    if (!x || !rstd || !wq || !wk || !cos_table || !sin_table) return MXFP4_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(cos_table) || !aligned16(sin_table) || (dmixed && !aligned16(dmixed)) ||
+        (reinterpret_cast<uintptr_t>(rstd) & 3u) || (reinterpret_cast<uintptr_t>(wq) & 3u) ||
+        (reinterpret_cast<uintptr_t>(wk) & 3u))
+        return MXFP4_ERR_MISALIGNED;
+    DeviceState* dev = nullptr;
+    st = device_ready(&dev);
+    if (st != MXFP4_OK) return st;
+    mxfp4::QuantBatch b;
+    std::memset(&b, 0, sizeof(b));
+    st = quantize_task(g, M, K, K, q_row, s_row, q_col, s_col, layout, dev, &b, 0);
+    if (st != MXFP4_OK) return st;
+    mxfp4::NormRopeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.gmap = b.maps[0];
+    if (!encode_2d(&a.xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(K) * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MXFP4_ERR_CUDA;
+    a.q = b.args[0];
+    a.rstd = rstd;
+    a.wq = wq;
+    a.wk = wk;
+    a.cosv = cos_table;
+    a.sinv = sin_table;
+    a.dmixed = static_cast<uint16_t*>(dmixed);
+    a.H = static_cast<int32_t>(H);
+    // Units of `span` consecutive tiles of one row block, about one unit per CTA.
+    const int64_t tiles = static_cast<int64_t>(a.q.tiles_m) * a.q.tiles_k;
+    const int64_t cap = static_cast<int64_t>(dev->sms) * mxfp4::quantize_norm_rope_ctas_per_sm();
+    const int64_t span = cdiv(tiles, cap) < a.q.tiles_k ? cdiv(tiles, cap) : a.q.tiles_k;
+    a.span = static_cast<int32_t>(span);
+    a.units_per_row = static_cast<int32_t>(cdiv(a.q.tiles_k, span));
+    a.units = a.q.tiles_m * a.units_per_row;
+    const int grid = static_cast<int>(a.units < cap ? a.units : cap);
+    return mxfp4::launch_quantize_norm_rope(a, grid, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MXFP4_OK
+               : MXFP4_ERR_CUDA;
+}
+
 mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* tasks, int32_t dual,
                                   mxfp4_scale_layout layout, mxfp4_stream_t stream) {
     if (count < 1 || count > MXFP4_MAX_BATCH || tasks == nullptr) return MXFP4_ERR_INVALID_ARG;

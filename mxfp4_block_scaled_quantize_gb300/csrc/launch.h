@@ -41,6 +41,30 @@ struct QuantBatch {
     int32_t count;
 };
 
+// Dual quantization of d(mixed_qkv) computed in the staging read from the gradient of the
+// QK RMSNorm + interleaved RoPE output (the quantizer prologue).  gmap / xmap: the gradient
+// g and mixed_qkv x as bf16 2-D tensors {3*H*128, M} (box {64, 128}, 128-byte swizzle, zero
+// fill); q: the quantization task for d(mixed_qkv) [M, 3*H*128] (dual).
+constexpr int kNormRopeD = 128;   // head dimension
+struct NormRopeArgs {
+    CUtensorMap gmap;
+    CUtensorMap xmap;
+    QuantArgs q;
+    const float* rstd;   // [M, H, 2]: the forward's 1/sqrt(mean(x^2)+eps) of q and k
+    const float* wq;     // [128] norm weights of q and k
+    const float* wk;
+    const float* cosv;   // [M, 64] RoPE tables
+    const float* sinv;
+    uint16_t* dmixed;    // optional bf16 d(mixed_qkv) [M, 3*H*128]
+    int32_t H;
+    int32_t span;           // tiles per unit of work (consecutive tiles of one 128-row block)
+    int32_t units_per_row;  // ceil(tiles_k / span)
+    int32_t units;          // tiles_m * units_per_row
+};
+size_t quantize_norm_rope_smem_bytes();
+int quantize_norm_rope_ctas_per_sm();
+cudaError_t launch_quantize_norm_rope(const NormRopeArgs& a, int grid, cudaStream_t stream);
+
 // Shared memory one quantizer CTA needs, and how many CTAs share an SM.
 size_t quantize_smem_bytes();
 int quantize_ctas_per_sm(bool sr);

@@ -596,10 +596,326 @@ __global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
     }
 }
 
+// ---- the quantizer prologue: QK RMSNorm + interleaved RoPE backward ------------------
+// d(mixed_qkv) of the QKV projection computed in the staging read and quantized, instead of
+// the norm + RoPE backward writing it to HBM for the quantizer to read back.  With head
+// dimension 128 every 128-column tile of d(mixed_qkv) [M, H*3*128] is one (head, part):
+// part 0 = q, 1 = k (computed), 2 = v (the gradient itself).  A CTA takes units of `span`
+// consecutive tiles of one 128-row block, so each thread loads the RoPE cosines and sines
+// of its row and columns once per unit into registers.  For a q / k tile the producer
+// brings the gradient tile g and the tile of mixed_qkv x; each row's two rowwise threads
+// (64 columns each) compute, in fp32, dy = the inverse rotation of g on the pairs
+// (2i, 2i+1) (dy0 = g0 c + g1 s, dy1 = g1 c - g0 s), dn = dy w and their share of
+// sum(dn x); the row's sum over both comes with one shuffle; a second pass recomputes dn and
+// gives dx = r dn - (r^3 / 128) x sum(dn x), rounded to bf16 (to nearest even).  That bf16
+// dx is what gets quantized: by the rowwise pass, and, written back over g in the stage, by
+// the columnwise pass after a barrier of the consumer warps.  One CTA per SM (two 32 KB
+// tiles per stage).
+struct NormRopeSmem {
+    uint8_t tile[kQStages][kQTileBytes];   // g, overwritten by dx for q / k tiles
+    uint8_t xt[kQStages][kQTileBytes];     // mixed_qkv
+    uint64_t full[kQStages];
+    uint64_t empty[kQStages];
+    float w[2][kNormRopeD];
+    int abort;
+};
+
+__device__ __forceinline__ void sts128q(uint32_t a, const uint4& v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& u, int e) {
+    return e == 0 ? u.x : e == 1 ? u.y : e == 2 ? u.z : u.w;
+}
+
+// dn = (the inverse rotation of the 8 gradient elements in gw) * w for columns kk .. kk + 7
+// of a head (kk a multiple of 8), with the row's cosines / sines of pairs kk/2 .. kk/2 + 3.
+__device__ __forceinline__ void norm_rope_dn(const uint4& gw, const float4& cs, const float4& sn, const float* wv,
+                                             int kk, float* dn) {
+    const float cc[4] = {cs.x, cs.y, cs.z, cs.w}, ss[4] = {sn.x, sn.y, sn.z, sn.w};
+    const float4 w0 = *reinterpret_cast<const float4*>(wv + kk), w1 = *reinterpret_cast<const float4*>(wv + kk + 4);
+    const float ww[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t g2 = word_of(gw, e);
+        const float g0 = bf16_lo(g2), g1 = bf16_hi(g2);
+        dn[2 * e] = __fmul_rn(__fadd_rn(__fmul_rn(g0, cc[e]), __fmul_rn(g1, ss[e])), ww[2 * e]);
+        dn[2 * e + 1] = __fmul_rn(__fsub_rn(__fmul_rn(g1, cc[e]), __fmul_rn(g0, ss[e])), ww[2 * e + 1]);
+    }
+}
+
+__global__ void __launch_bounds__(kQThreads, 1) quantize_norm_rope_kernel(const __grid_constant__ NormRopeArgs A) {
+    extern __shared__ uint8_t smem_raw[];
+    NormRopeSmem& sm = *reinterpret_cast<NormRopeSmem*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const QuantArgs& p = A.q;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    uint32_t* const err = p.err;
+
+    if (tid == 0) {
+        for (int s = 0; s < kQStages; ++s) {
+            mbar_init(smem_addr(&sm.full[s]), 1);
+            mbar_init(smem_addr(&sm.empty[s]), kQConsumerWarps);
+        }
+        sm.abort = 0;
+        fence_barrier_init();
+    }
+    if (tid < 2 * kNormRopeD) sm.w[tid / kNormRopeD][tid % kNormRopeD] =
+        __ldg((tid < kNormRopeD ? A.wq : A.wk) + (tid % kNormRopeD));
+    __syncthreads();
+    grid_launch_dependents();
+    grid_wait_prerequisites();
+
+    if (warp == kQConsumerWarps) {
+        if (lane_id() == 0) {
+            prefetch_tensormap(&A.gmap);
+            prefetch_tensormap(&A.xmap);
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < A.units && ok; u += gridDim.x) {
+                const int tm = u / A.units_per_row, tk0 = (u % A.units_per_row) * A.span;
+                const int tk1 = min(tk0 + A.span, p.tiles_k);
+                for (int tk = tk0; tk < tk1; ++tk, ++it) {
+                    const int s = it % kQStages;
+                    const uint32_t ph = (it / kQStages) & 1;
+                    if (!mbar_wait(smem_addr(&sm.empty[s]), ph ^ 1, err, kErrQuantProducer, &sm.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool qk = (tk % 3) != 2;
+                    const uint32_t bar = smem_addr(&sm.full[s]);
+                    mbar_arrive_expect_tx(bar, qk ? 2 * kQTileBytes : kQTileBytes);
+                    tma_load_2d(smem_addr(sm.tile[s]), &A.gmap, tk * kQT, tm * kQT, bar);
+                    tma_load_2d(smem_addr(sm.tile[s]) + kQBoxBytes, &A.gmap, tk * kQT + 64, tm * kQT, bar);
+                    if (qk) {
+                        tma_load_2d(smem_addr(sm.xt[s]), &A.xmap, tk * kQT, tm * kQT, bar);
+                        tma_load_2d(smem_addr(sm.xt[s]) + kQBoxBytes, &A.xmap, tk * kQT + 64, tm * kQT, bar);
+                    }
+                }
+            }
+            const int armed = it < kQStages ? it : kQStages;
+            for (int i = 1; i <= armed; ++i) {
+                const int j = it - i;
+                mbar_wait_quiet(smem_addr(&sm.full[j % kQStages]), (j / kQStages) & 1, kWaitLimitNs);
+            }
+        }
+        return;
+    }
+
+    const uint32_t lane = lane_id();
+    // the rowwise thread mapping of the quantizer: the two lanes that differ in bit 2 share a
+    // row, each with two 32-column blocks b
+    const int L = 4 * warp + (lane & 3);
+    const int Q = lane >> 3;
+    const int r = Q * 32 + L;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < A.units && ok; u += gridDim.x) {
+        const int tm = u / A.units_per_row, tk0 = (u % A.units_per_row) * A.span;
+        const int tk1 = min(tk0 + A.span, p.tiles_k);
+        const int64_t m0 = static_cast<int64_t>(tm) * kQT;
+        const int64_t row = m0 + r;
+        const bool live = row < p.M;
+        const int64_t rrow = live ? row : 0;
+        // this thread's RoPE cosines and sines for the unit: pairs 16 b .. 16 b + 15 of its row
+        float4 cs4[2][4], sn4[2][4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int b = ((lane >> 2) & 1) + 2 * i;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                cs4[i][c] = __ldg(reinterpret_cast<const float4*>(A.cosv + rrow * 64) + 4 * b + c);
+                sn4[i][c] = __ldg(reinterpret_cast<const float4*>(A.sinv + rrow * 64) + 4 * b + c);
+            }
+        }
+        for (int tk = tk0; tk < tk1; ++tk, ++it) {
+            const int s = it % kQStages;
+            const uint32_t ph = (it / kQStages) & 1;
+            int okw = 0;
+            if (lane == 0) okw = mbar_wait(smem_addr(&sm.full[s]), ph, err, kErrQuantConsumer, &sm.abort) ? 1 : 0;
+            // Every consumer warp meets every tile's barrier, with its ok flag: a warp whose
+            // wait ran out skips the tile's work and all leave together.
+            const bool have = __shfl_sync(0xFFFFFFFFu, okw, 0) != 0;
+            const int part = tk % 3, head = tk / 3;
+            const int64_t k0 = static_cast<int64_t>(tk) * kQT;
+            const uint32_t tile = smem_addr(sm.tile[s]);
+            const uint32_t xtile = smem_addr(sm.xt[s]);
+            uint8_t* const atom_row = p.s_row + (static_cast<int64_t>(tm) * (p.kb_row >> 2) + tk) * 512;
+            uint8_t* const atom_col = p.s_col + (static_cast<int64_t>(tk) * (p.kb_col >> 2) + tm) * 512;
+
+            if (have && part != 2) {
+                const float* const wv = sm.w[part];
+                const float rr = live ? __ldg(A.rstd + (rrow * A.H + head) * 2 + part) : 0.0f;
+                float dot = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int b = ((lane >> 2) & 1) + 2 * i;
+                    const uint32_t box = tile + (b >> 1) * kQBoxBytes;
+                    const uint32_t xbox = xtile + (b >> 1) * kQBoxBytes;
+                    const int j0 = (b & 1) * 4;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 xw = lds128(xbox + swz(r, j0 + c));
+                        float dn[8];
+                        norm_rope_dn(lds128(box + swz(r, j0 + c)), cs4[i][c], sn4[i][c], wv, 32 * b + 8 * c, dn);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            dot = __fmaf_rn(dn[2 * e], bf16_lo(word_of(xw, e)), dot);
+                            dot = __fmaf_rn(dn[2 * e + 1], bf16_hi(word_of(xw, e)), dot);
+                        }
+                    }
+                }
+                dot = __fadd_rn(dot, __shfl_xor_sync(0xFFFFFFFFu, dot, 4));
+                const float coef = __fmul_rn(__fmul_rn(__fmul_rn(rr, rr), rr), __fmul_rn(dot, 1.0f / kNormRopeD));
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int b = ((lane >> 2) & 1) + 2 * i;
+                    const uint32_t box = tile + (b >> 1) * kQBoxBytes;
+                    const uint32_t xbox = xtile + (b >> 1) * kQBoxBytes;
+                    const int j0 = (b & 1) * 4;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 xw = lds128(xbox + swz(r, j0 + c));
+                        float dn[8];
+                        norm_rope_dn(lds128(box + swz(r, j0 + c)), cs4[i][c], sn4[i][c], wv, 32 * b + 8 * c, dn);
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t xwd = word_of(xw, e);
+                            const float d0 = __fsub_rn(__fmul_rn(rr, dn[2 * e]), __fmul_rn(coef, bf16_lo(xwd)));
+                            const float d1 = __fsub_rn(__fmul_rn(rr, dn[2 * e + 1]), __fmul_rn(coef, bf16_hi(xwd)));
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(d0, d1);
+                            // rows past M stay +0 padding (a zero gradient can still give -0)
+                            o[e] = live ? *reinterpret_cast<uint32_t*>(&h2) : 0u;
+                        }
+                        sts128q(box + swz(r, j0 + c), make_uint4(o[0], o[1], o[2], o[3]));
+                    }
+                }
+            }
+            if (have) {
+                uint4 v[2][4];
+        #pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int b = ((lane >> 2) & 1) + 2 * i;
+                    const uint32_t box = tile + (b >> 1) * kQBoxBytes;
+                    const int j0 = (b & 1) * 4;
+        #pragma unroll
+                    for (int c = 0; c < 4; ++c) v[i][c] = lds128(box + swz(r, j0 + c));
+                }
+                if (A.dmixed != nullptr && row < p.M) {
+        #pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int b = ((lane >> 2) & 1) + 2 * i;
+        #pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            *reinterpret_cast<uint4*>(A.dmixed + row * p.K + k0 + 32 * b + 8 * c) = v[i][c];
+                    }
+                }
+        #pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int b = ((lane >> 2) & 1) + 2 * i;
+                    uint32_t m = absmax2(absmax2(absmax2(v[i][0].x, v[i][0].y), absmax2(v[i][0].z, v[i][0].w)),
+                                         absmax2(absmax2(v[i][1].x, v[i][1].y), absmax2(v[i][1].z, v[i][1].w)));
+                    m = absmax2(m, absmax2(absmax2(absmax2(v[i][2].x, v[i][2].y), absmax2(v[i][2].z, v[i][2].w)),
+                                           absmax2(absmax2(v[i][3].x, v[i][3].y), absmax2(v[i][3].z, v[i][3].w))));
+                    m = absmax2(m, m >> 16) & 0x7FFFu;
+                    const uint32_t byte = scale_byte(m);
+                    const uint32_t inv = inv_scale_bits(byte);
+                    const uint64_t s2 = pack2(inv, inv);
+                    const uint4 q = make_uint4(encode8(v[i][0].x, v[i][0].y, v[i][0].z, v[i][0].w, s2),
+                                               encode8(v[i][1].x, v[i][1].y, v[i][1].z, v[i][1].w, s2),
+                                               encode8(v[i][2].x, v[i][2].y, v[i][2].z, v[i][2].w, s2),
+                                               encode8(v[i][3].x, v[i][3].y, v[i][3].z, v[i][3].w, s2));
+                    if (row < p.M) {
+                        *reinterpret_cast<uint4*>(p.q_row + row * p.ldq_row + ((k0 + 32 * b) >> 1)) = q;
+                        if (!p.tc_layout) p.s_row[row * p.kb_row + (k0 >> 5) + b] = static_cast<uint8_t>(byte);
+                    }
+                    if (p.tc_layout) atom_row[L * 16 + Q * 4 + b] = static_cast<uint8_t>(row < p.M ? byte : 0u);
+                }
+                // every warp's rows of dx are in the stage before any column is read
+            }
+            if (!named_barrier_and(kBarConsumers, kQConsumers, have)) {
+                ok = false;
+                break;
+            }
+
+            // ---- columnwise, as the quantizer's plain columnwise pass
+            {
+                const int pc = 8 * warp + (lane & 7), rb = lane >> 3;
+                const uint32_t box = tile + (pc >> 5) * kQBoxBytes;
+                const int jc = (pc & 31) >> 2;
+                const uint32_t inner = (pc & 3) * 4;
+                uint32_t toff[8];
+    #pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int rr2 = k ^ (2 * rb);
+                    toff[k] = box + rb * 32 * 128 + rr2 * 128 + ((jc ^ rr2) << 4) + inner;
+                }
+                uint32_t w[32];
+    #pragma unroll
+                for (int i = 0; i < 32; ++i) w[i] = lds32(toff[i & 7] + (i & ~7) * 128);
+                const uint32_t sel = 0x3210u ^ (0x1111u * static_cast<uint32_t>(rb));
+                const int64_t kc = k0 + 2 * pc;
+                uint32_t m = w[0];
+    #pragma unroll
+                for (int i = 1; i < 32; ++i) m = absmax2(m, w[i]);
+                const uint32_t byte0 = scale_byte(m), byte1 = scale_byte(m >> 16);
+                const uint64_t s2 = pack2(inv_scale_bits(byte0), inv_scale_bits(byte1));
+                uint32_t q0[4], q1[4];
+    #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    encode_cols8(&w[8 * j], s2, &q0[j], &q1[j]);
+                    q0[j] = __byte_perm(q0[j], 0, sel);
+                    q1[j] = __byte_perm(q1[j], 0, sel);
+                }
+                const int64_t off = (m0 + rb * 32) >> 1;
+                if (kc < p.K) {
+                    *reinterpret_cast<uint4*>(p.q_col + kc * p.ldq_col + off) = make_uint4(q0[0], q0[1], q0[2], q0[3]);
+                    if (!p.tc_layout) p.s_col[kc * p.kb_col + (m0 >> 5) + rb] = static_cast<uint8_t>(byte0);
+                }
+                if (kc + 1 < p.K) {
+                    *reinterpret_cast<uint4*>(p.q_col + (kc + 1) * p.ldq_col + off) = make_uint4(q1[0], q1[1], q1[2], q1[3]);
+                    if (!p.tc_layout) p.s_col[(kc + 1) * p.kb_col + (m0 >> 5) + rb] = static_cast<uint8_t>(byte1);
+                }
+                const int kl0 = 2 * pc, kl1 = 2 * pc + 1;
+                if (p.tc_layout) {
+                    atom_col[(kl0 & 31) * 16 + (kl0 >> 5) * 4 + rb] = static_cast<uint8_t>(kc < p.K ? byte0 : 0u);
+                    atom_col[(kl1 & 31) * 16 + (kl1 >> 5) * 4 + rb] = static_cast<uint8_t>(kc + 1 < p.K ? byte1 : 0u);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&sm.empty[s]));
+        }
+    }
+}
+
 }  // namespace
 
 size_t quantize_smem_bytes() { return sizeof(QuantSmem) + 1024; }
 int quantize_ctas_per_sm(bool sr) { return sr ? 1 : kQCtasPerSm; }
+
+size_t quantize_norm_rope_smem_bytes() { return sizeof(NormRopeSmem) + 1024; }
+int quantize_norm_rope_ctas_per_sm() { return 1; }
+
+cudaError_t launch_quantize_norm_rope(const NormRopeArgs& a, int grid, cudaStream_t stream) {
+    const size_t smem = quantize_norm_rope_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(quantize_norm_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kQThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_norm_rope_kernel, a);
+}
 
 cudaError_t launch_quantize(const QuantBatch& b, bool dual, bool sr, int grid, cudaStream_t stream) {
     const size_t smem = quantize_smem_bytes();

@@ -83,6 +83,14 @@ def test_argument_checks_precede_any_device_use(lib):
     assert lib.mxfp4_quantize_batch(1, bad, 0, 1, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_quantize_dual_rht(16, 4, 8, 8, 32, 48, None, 64, 1, 7, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_quantize_dual_rht_sr(16, 4, 8, 8, 32, 48, None, 64, 1, 7, 9, None) == abi.MXFP4_ERR_INVALID_ARG
+    nr = [16, 32, 4, 1, 48, 64, 80, 96, 112, 128, 144, 160, 176, 1, None, None]
+    assert lib.mxfp4_quantize_dual_qk_norm_rope_bwd(*nr[:3], 0, *nr[4:]) == abi.MXFP4_ERR_INVALID_ARG  # H
+    bad = list(nr)
+    bad[1] = None                                                    # no mixed_qkv
+    assert lib.mxfp4_quantize_dual_qk_norm_rope_bwd(*bad) == abi.MXFP4_ERR_INVALID_ARG
+    bad = list(nr)
+    bad[7] = 100                                                     # cos table not 16-byte aligned
+    assert lib.mxfp4_quantize_dual_qk_norm_rope_bwd(*bad) == abi.MXFP4_ERR_MISALIGNED
     assert lib.mxfp4_quantize_dual_rht_sr(16, 4, 8, 8, 32, 48, 64, 80, 3, 7, 9, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_quantize_dual_2d(16, 4, 8, 8, 32, 48, None, 64, 1, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_quantize_dual_2d(18, 4, 8, 8, 32, 48, 64, 80, 1, None) == abi.MXFP4_ERR_MISALIGNED
@@ -165,6 +173,9 @@ def test_no_usable_device_fails_loudly(lib):
     assert lib.mxfp4_quantize_dual_rht(0x10000, 4, 8, 8, 0x20000, 0x30000, 0x40000, 0x50000, 1, 7, None) in bad
     assert lib.mxfp4_quantize_dual_rht_sr(0x10000, 4, 8, 8, 0x20000, 0x30000, 0x40000, 0x50000, 1, 7, 9,
                                           None) in bad
+    assert lib.mxfp4_quantize_dual_qk_norm_rope_bwd(0x10000, 0x20000, 4, 1, 0x30000, 0x40000, 0x50000, 0x60000,
+                                                    0x70000, 0x80000, 0x90000, 0xA0000, 0xB0000, 1, None,
+                                                    None) in bad
     assert lib.mxfp4_gemm(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x50000, 4, 0, None) in bad
     assert lib.mxfp4_gemm_bias(0x10000, 0x20000, 0x30000, 0x40000, 4, 4, 4, 0x60000, 0x50000, 4, 0, None) in bad
     assert lib.mxfp4_gemm_quantize(0x10000, 0x20000, 0x30000, 0x40000, 4, 8, 4, None, 0x50000, 8, 0x60000, 0x70000,
