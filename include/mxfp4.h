@@ -166,10 +166,10 @@ mxfp4_status mxfp4_quantize_dual_rht_sr(const void* x, int64_t M, int64_t K, int
 
 /* The gradient quantization of the QKV projection with the QK RMSNorm + interleaved RoPE
  * backward computed in the quantizer's staging read: the prologue of the pages' QKV packer
- * (`MXFP6QKVNormRopeFunction`: "the packer computes d(mixed_qkv) during its staging read
- * instead of the norm+RoPE backward writing it to HBM for the quantizer to read straight
- * back"; fused_norm_rope.py: q and k read as strided slices of mixed_qkv at stride 3D, the
- * interleaved rotation, v copied).  Head dimension 128.  With K = 3*H*128:
+ * (`MXFP6QKVNormRopeFunction`, whose packer produces d(mixed_qkv) while staging its input, so
+ * the norm + RoPE backward never writes it to HBM for the quantizer to read again;
+ * fused_norm_rope.py: per head, q and k are 3D columns apart in mixed_qkv, the rotation acts
+ * on interleaved pairs, v passes through unchanged).  Head dimension 128.  With K = 3*H*128:
  *   g       bf16 [M, K]: the gradient of the norm + RoPE output, per token and head the
  *           columns h*384 .. h*384+127 for q, the next 128 for k, the next 128 for v (v's
  *           gradient itself); row pitch K

@@ -653,10 +653,10 @@ int oracle_quantize_col_rht_sr(const uint16_t* x, int64_t M, int64_t K, int64_t 
 
 /* ---------------------------------------------------------------------------------------
  * QK RMSNorm + interleaved RoPE backward, the producer computed in the quantizer's staging
- * read: the pages' MXFP6 QKV packer prologue (`MXFP6QKVNormRopeFunction`: "the packer
- * computes d(mixed_qkv) during its staging read"; fused_norm_rope.py: QK RMSNorm and the
- * interleaved RoPE rotation, q and k read as strided slices of mixed_qkv at stride 3D, v
- * copied, never rotated).  Reading taken (the pages name the ops, not their formulas):
+ * read: the pages' MXFP6 QKV packer prologue (`MXFP6QKVNormRopeFunction`, whose packer
+ * produces d(mixed_qkv) while staging its input; fused_norm_rope.py: the QK RMSNorm and an
+ * interleaved RoPE rotation, per head q and k 3D columns apart in mixed_qkv, v passed
+ * through unchanged).  Reading taken (the pages name the ops, not their formulas):
  *   - mixed_qkv[M, H*3*D]: for token m and head h, columns h*3D .. h*3D+D-1 are q, the next
  *     D are k, the next D are v;
  *   - forward for p in {q, k}: x = mixed[m, h, p, :]; r = 1/sqrt(mean(x^2) + eps) (saved by
