@@ -199,7 +199,12 @@ mxfp4_status mxfp4_quantize_dual_qk_norm_rope_bwd(const void* g, const void* x, 
 /* One tensor of a batched quantization: bf16 x[rows, k] with row pitch ldx elements and
  * its output buffers, as for mxfp4_quantize / mxfp4_quantize_dual (q_col and s_col are
  * read only for the dual quantizer); flags: 0, MXFP4_QUANT_2D_BLOCKS or
- * MXFP4_QUANT_RHT_COL (not both); rht_signs: the sign mask of MXFP4_QUANT_RHT_COL. */
+ * MXFP4_QUANT_RHT_COL (not both); rht_signs: the sign mask of MXFP4_QUANT_RHT_COL;
+ * amax: NULL, or one fp32 in device memory (4-byte aligned) that the call sets to max |x|
+ * over the tensor, the amax of the tensorwise FP8 quantizer (mxfp4_fp8_quantize_tw), from
+ * the block maxima the rowwise pass takes anyway: the hybrid backward's FP8 quantization of
+ * X and W then skips its own amax pass (mxfp4_fp8_quantize_task::amax_given).  A NaN or
+ * infinity in x makes it non-finite, as there. */
 typedef struct {
     const void* x;
     int64_t rows;
@@ -211,6 +216,7 @@ typedef struct {
     void* s_col;
     int32_t flags;
     uint32_t rht_signs;
+    float* amax;
 } mxfp4_quantize_task;
 
 #define MXFP4_MAX_BATCH 4
@@ -254,7 +260,7 @@ mxfp4_status mxfp4_gemm_bias(const void* a_q, const void* a_s, const void* b_q, 
                              int64_t ldc, mxfp4_out_dtype out_dtype, mxfp4_stream_t stream);
 
 /* A forward GEMM whose epilogue also quantizes its output for the next linear layer: the
- * "GEMM epilogue that emits the next layer's MXFP4 row blob" fusion of the layer chain
+ * fusion that emits the next layer's MXFP4 blobs from the GEMM epilogue, in the layer chain
  * (`MXFP4LinearFunction.forward` of primus_turbo_mxfp4_local.py feeds each layer's output
  * to the next layer, whose forward starts with `_quantize_mxfp4_dual_op` of that output).
  * Writes bf16 C = A . B^T (+ bias), exactly as mxfp4_gemm / mxfp4_gemm_bias with
@@ -316,7 +322,7 @@ mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4
  *              least one of q_row / q_col; both 16-byte aligned
  *   amax, scale_inv   out, one fp32 each in device memory (4-byte aligned); the GEMMs
  *              read scale_inv from there, so no host synchronization is needed.
- * Three launches on `stream`: *amax zeroed, an amax pass, the conversion.  M, K >= 1.
+ * Launches on `stream`: *amax zeroed, an amax pass, the conversion.  M, K >= 1.
  * Inputs must be finite: a NaN or infinity makes amax non-finite, the codes and scale_inv
  * of that tensor are then meaningless, and the conversion records it in the device error
  * word (mxfp4_last_device_error returns MXFP4_ERR_NONFINITE). */
@@ -324,7 +330,10 @@ mxfp4_status mxfp4_fp8_quantize_tw(const void* x, int64_t M, int64_t K, int64_t 
                                    void* q_row, void* q_col, float* amax, float* scale_inv,
                                    mxfp4_stream_t stream);
 
-/* One tensor of a batch: the arguments of mxfp4_fp8_quantize_tw. */
+/* One tensor of a batch: the arguments of mxfp4_fp8_quantize_tw; amax_given nonzero: *amax
+ * already holds max |x| of this tensor (written by an earlier mxfp4_quantize_batch amax
+ * output, in stream order before this call) and the call neither zeroes it nor runs the
+ * amax pass over the tensor. */
 typedef struct {
     const void* x;
     int64_t M;
@@ -334,6 +343,7 @@ typedef struct {
     void* q_col;
     float* amax;
     float* scale_inv;
+    int32_t amax_given;
 } mxfp4_fp8_quantize_task;
 
 /* 1..MXFP4_MAX_BATCH tensors quantized tensorwise with the same three launches (the hybrid

@@ -42,7 +42,7 @@ class QuantizeTask(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("k", ctypes.c_int64),
                 ("ldx", ctypes.c_int64), ("q_row", ctypes.c_void_p), ("s_row", ctypes.c_void_p),
                 ("q_col", ctypes.c_void_p), ("s_col", ctypes.c_void_p), ("flags", ctypes.c_int32),
-                ("rht_signs", ctypes.c_uint32)]
+                ("rht_signs", ctypes.c_uint32), ("amax", ctypes.c_void_p)]
 
 
 MXFP4_QUANT_2D_BLOCKS = 1
@@ -52,7 +52,7 @@ class Fp8QuantizeTask(ctypes.Structure):
     """mxfp4_fp8_quantize_task of include/mxfp4.h."""
     _fields_ = [("x", ctypes.c_void_p), ("M", ctypes.c_int64), ("K", ctypes.c_int64), ("ldx", ctypes.c_int64),
                 ("q_row", ctypes.c_void_p), ("q_col", ctypes.c_void_p), ("amax", ctypes.c_void_p),
-                ("scale_inv", ctypes.c_void_p)]
+                ("scale_inv", ctypes.c_void_p), ("amax_given", ctypes.c_int32)]
 
 
 class Fp8GemmTask(ctypes.Structure):
@@ -253,16 +253,18 @@ def quantize_qk_norm_rope_bwd(g, x, rstd, wq, wk, cos_table, sin_table, H, layou
 
 
 def mxfp4_quantize_batch(tasks, dual: bool, layout=MXFP4_SCALE_TC, stream=None) -> None:
-    """tasks: sequence of (x, rows, k, ldx, q_row, s_row, q_col, s_col[, flags[, rht_signs]]);
-    q_col / s_col may be None for the row-only quantizer; flags 0, MXFP4_QUANT_2D_BLOCKS or
-    MXFP4_QUANT_RHT_COL."""
+    """tasks: sequence of (x, rows, k, ldx, q_row, s_row, q_col, s_col[, flags[, rht_signs[,
+    amax]]]); q_col / s_col may be None for the row-only quantizer; flags 0,
+    MXFP4_QUANT_2D_BLOCKS or MXFP4_QUANT_RHT_COL; amax: None or a one-float CUDA buffer set
+    to max |x| (the tensorwise FP8 amax)."""
     arr = (QuantizeTask * max(1, len(tasks)))()
     for i, t in enumerate(tasks):
         x, rows, k, ldx, q_row, s_row, q_col, s_col = t[:8]
         flags = t[8] if len(t) > 8 else 0
         signs = t[9] if len(t) > 9 else 0
+        amax = t[10] if len(t) > 10 else None
         arr[i] = QuantizeTask(_ptr(x), rows, k, ldx, _ptr(q_row), _ptr(s_row), _ptr(q_col),
-                              _ptr(s_col), flags, int(signs) & 0xFFFF)
+                              _ptr(s_col), flags, int(signs) & 0xFFFF, _ptr(amax))
     _check(load().mxfp4_quantize_batch(len(tasks), arr, int(bool(dual)), layout, _stream(stream)),
            "mxfp4_quantize_batch")
 
@@ -314,11 +316,13 @@ def mxfp4_fp8_quantize_tw(x, M, K, ldx, q_row, q_col, amax, scale_inv, stream=No
 
 
 def mxfp4_fp8_quantize_tw_batch(tasks, stream=None) -> None:
-    """tasks: sequence of (x, M, K, ldx, q_row, q_col, amax, scale_inv); q_row or q_col may
-    be None."""
+    """tasks: sequence of (x, M, K, ldx, q_row, q_col, amax, scale_inv[, amax_given]); q_row
+    or q_col may be None; amax_given: amax already holds max |x| (from mxfp4_quantize_batch)."""
     arr = (Fp8QuantizeTask * max(1, len(tasks)))()
-    for i, (x, M, K, ldx, qr, qc, amax, inv) in enumerate(tasks):
-        arr[i] = Fp8QuantizeTask(_ptr(x), M, K, ldx, _ptr(qr), _ptr(qc), _ptr(amax), _ptr(inv))
+    for i, t in enumerate(tasks):
+        x, M, K, ldx, qr, qc, amax, inv = t[:8]
+        given = int(bool(t[8])) if len(t) > 8 else 0
+        arr[i] = Fp8QuantizeTask(_ptr(x), M, K, ldx, _ptr(qr), _ptr(qc), _ptr(amax), _ptr(inv), given)
     _check(load().mxfp4_fp8_quantize_tw_batch(len(tasks), arr, _stream(stream)), "mxfp4_fp8_quantize_tw_batch")
 
 

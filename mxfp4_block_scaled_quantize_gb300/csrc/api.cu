@@ -425,6 +425,7 @@ mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* task
         if ((t.flags & ~(MXFP4_QUANT_2D_BLOCKS | MXFP4_QUANT_RHT_COL)) != 0 ||
             t.flags == (MXFP4_QUANT_2D_BLOCKS | MXFP4_QUANT_RHT_COL) || ((t.flags & MXFP4_QUANT_RHT_COL) && !d))
             return MXFP4_ERR_INVALID_ARG;
+        if (t.amax != nullptr && (reinterpret_cast<uintptr_t>(t.amax) & 3u)) return MXFP4_ERR_MISALIGNED;
     }
     DeviceState* dev = nullptr;
     mxfp4_status st = device_ready(&dev);
@@ -436,6 +437,7 @@ mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* task
         st = quantize_task(t.x, t.rows, t.k, t.ldx, t.q_row, t.s_row, t.q_col, t.s_col, layout, dev, &b, j,
                            t.flags, t.rht_signs);
         if (st != MXFP4_OK) return st;
+        b.args[j].amax_bits = reinterpret_cast<uint32_t*>(t.amax);
     }
     return launch_batch(b, d, dev, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -568,8 +570,9 @@ mxfp4_status mxfp4_fp8_quantize_tw_batch(int32_t count, const mxfp4_fp8_quantize
     int64_t rows = 0, tiles = 0;
     for (int j = 0; j < count; ++j) {
         const mxfp4_fp8_quantize_task& t = tasks[j];
-        b.t[j] = mxfp4::Fp8QuantArgs{t.x, t.M, t.K, t.ldx, t.q_row, pad16(t.K), t.q_col, pad16(t.M), t.amax,
-                                     t.scale_inv};
+        b.t[j] = mxfp4::Fp8QuantArgs{t.x,        t.M,        t.K,    t.ldx,         t.q_row,
+                                     pad16(t.K), t.q_col,    pad16(t.M), t.amax, t.scale_inv,
+                                     t.amax_given != 0 ? 1 : 0};
         rows += t.M;
         tiles += cdiv(t.M, 64) * cdiv(t.K, 64);
         b.row_end[j] = rows;

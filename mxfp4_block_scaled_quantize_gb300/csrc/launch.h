@@ -26,6 +26,7 @@ struct QuantArgs {
     int32_t block_2d;    // 1: 32 x 32 blocks (one scale per block in both packings)
     int32_t rht;         // 1: Hadamard transform of 16-row groups before the column pass
     uint32_t rht_signs;  // its sign mask (bit j: row j of a group is negated)
+    uint32_t* amax_bits; // or null: raised (atomic max) to max |x| as fp32 bits, zeroed before the launch
     uint32_t* err;       // device error word
 };
 

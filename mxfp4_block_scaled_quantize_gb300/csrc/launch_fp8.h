@@ -21,6 +21,7 @@ struct Fp8QuantArgs {
     int64_t ldc;
     float* amax;
     float* scale_inv;
+    int32_t amax_given;  // *amax already holds max |x|: no zeroing, no amax pass
 };
 
 // Up to kMaxFp8Tasks tensors in one pass of each kernel: row_end / tile_end are the

@@ -414,6 +414,7 @@ __global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
 
     // ------------------------------------------------------------------ consumers
     const uint32_t lane = lane_id();
+    uint32_t amx[kMaxQuantTasks] = {0u, 0u, 0u, 0u};   // per task: this lane's max |x| so far
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
         const int s = it % kQStages;
@@ -423,7 +424,8 @@ __global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
         if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
 
         int lt;
-        const QuantArgs& p = P.args[task_of(t, &lt)];
+        const int pj = task_of(t, &lt);
+        const QuantArgs& p = P.args[pj];
         const int tm = lt / p.tiles_k, tk = lt % p.tiles_k;
         const int64_t m0 = static_cast<int64_t>(tm) * kQT;
         const int64_t k0 = static_cast<int64_t>(tk) * kQT;
@@ -475,6 +477,12 @@ __global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
                 for (int w = 0; w < kQConsumerWarps; ++w) m = max(m, sm.part[par][w][Q * 4 + b]);
                 bm[i] = m;
             }
+        }
+        if (p.amax_bits != nullptr) {   // running max |x| per task, folded in once at exit
+            const uint32_t m2 = max(bm[0], bm[1]);
+#pragma unroll
+            for (int k = 0; k < kMaxQuantTasks; ++k)
+                if (k == pj) amx[k] = max(amx[k], m2);
         }
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -593,6 +601,13 @@ __global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
         // This warp is done with the stage.
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.empty[s]));
+    }
+    // The tasks' max |x| (bf16 magnitude bits -> fp32 bits): one atomic per warp and task.
+#pragma unroll
+    for (int k = 0; k < kMaxQuantTasks; ++k) {
+        if (k >= P.count || P.args[k].amax_bits == nullptr) continue;
+        const uint32_t m2 = __reduce_max_sync(0xFFFFFFFFu, amx[k]);
+        if (lane == 0 && m2 != 0) atomicMax(P.args[k].amax_bits, m2 << 16);
     }
 }
 
@@ -917,8 +932,20 @@ cudaError_t launch_quantize_norm_rope(const NormRopeArgs& a, int grid, cudaStrea
     return cudaLaunchKernelEx(&cfg, quantize_norm_rope_kernel, a);
 }
 
+__global__ void amax_zero_kernel(const __grid_constant__ QuantBatch B) {
+    if (static_cast<int>(threadIdx.x) < B.count && B.args[threadIdx.x].amax_bits != nullptr)
+        *B.args[threadIdx.x].amax_bits = 0u;
+}
+
 cudaError_t launch_quantize(const QuantBatch& b, bool dual, bool sr, int grid, cudaStream_t stream) {
     const size_t smem = quantize_smem_bytes();
+    bool any_amax = false;
+    for (int j = 0; j < b.count; ++j) any_amax = any_amax || b.args[j].amax_bits != nullptr;
+    if (any_amax) {   // a plain launch: the quantizer's dependency wait covers it
+        amax_zero_kernel<<<1, 32, 0, stream>>>(b);
+        const cudaError_t ez = cudaGetLastError();
+        if (ez != cudaSuccess) return ez;
+    }
     if (sr && !dual) return cudaErrorInvalidValue;
     bool recipes = false, any_2d = false;
     for (int j = 0; j < b.count; ++j) {

@@ -9,7 +9,8 @@
 //
 // Up to four tensors per call: the amax words are zeroed, then for each tensor an amax
 // pass (each warp folds its maxima into the tensor's amax word with one atomicMax on the
-// fp32 bit pattern, which orders like the value for non-negative floats) and a conversion
+// fp32 bit pattern, which orders like the value for non-negative floats; skipped, and the
+// word left alone, for a tensor whose amax an earlier MXFP4 quantization wrote) and a conversion
 // pass over 64 x 64 tiles that writes the row copy (X's codes, row pitch
 // ldr bytes) and/or the column copy (X^T's codes, row pitch ldc bytes) through a shared
 // transpose, so both copies leave in 16-byte row pieces.  The column copies are what keep
@@ -29,7 +30,7 @@ constexpr int kFt = 64;            // tile edge
 constexpr int kFThreads = 256;     // 4 threads per tile row, 16 elements each
 
 __global__ void fp8_zero_kernel(const __grid_constant__ Fp8QuantBatch B) {
-    if (static_cast<int>(threadIdx.x) < B.count) *B.t[threadIdx.x].amax = 0.0f;
+    if (static_cast<int>(threadIdx.x) < B.count && !B.t[threadIdx.x].amax_given) *B.t[threadIdx.x].amax = 0.0f;
 }
 
 // 16 bytes through the read-only path with an L2 eviction-priority policy.
@@ -232,12 +233,14 @@ cudaError_t launch_fp8_quantize(const Fp8QuantBatch& b, int sms, cudaStream_t st
         one.t[0] = b.t[j];
         one.row_end[0] = b.row_end[j] - (j > 0 ? b.row_end[j - 1] : 0);
         one.tile_end[0] = b.tile_end[j] - (j > 0 ? b.tile_end[j - 1] : 0);
-        const int64_t rows = one.row_end[0];
-        const int64_t want = (rows + 7) / 8;   // 8 warps per CTA, one row each
-        const int grid1 = static_cast<int>(want < int64_t{sms} * 8 ? want : int64_t{sms} * 8);
-        fp8_amax_kernel<<<grid1 > 0 ? grid1 : 1, 256, 0, stream>>>(one);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        if (!one.t[0].amax_given) {
+            const int64_t rows = one.row_end[0];
+            const int64_t want = (rows + 7) / 8;   // 8 warps per CTA, one row each
+            const int grid1 = static_cast<int>(want < int64_t{sms} * 8 ? want : int64_t{sms} * 8);
+            fp8_amax_kernel<<<grid1 > 0 ? grid1 : 1, 256, 0, stream>>>(one);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
         const int64_t tiles = one.tile_end[0];
         const int grid2 = static_cast<int>(tiles < int64_t{sms} * 8 ? tiles : int64_t{sms} * 8);
         fp8_quantize_kernel<<<grid2, kFThreads, 0, stream>>>(one);

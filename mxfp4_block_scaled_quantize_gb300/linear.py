@@ -136,6 +136,12 @@ class MXFP4Linear:
             xf = abi.MXFP4_QUANT_RHT_COL if self.rht_signs is not None else 0
             tasks = [(x, M, K, x.stride(0), *self.x_row, *self.x_col, xf, self.rht_signs or 0),
                      (w, N, K, w.stride(0), *self.w_row, *self.w_col, wf)]
+        elif self.fp8_backward:
+            # the row-only forward quantization also gives X's and W's tensorwise amax, so the
+            # hybrid backward's FP8 quantization of them skips its own amax pass
+            sc = self.f8_scalars
+            tasks = [(x, M, K, x.stride(0), *self.x_row, None, None, 0, 0, sc[2:3]),
+                     (w, N, K, w.stride(0), *self.w_row, None, None, wf, 0, sc[4:5])]
         else:
             tasks = [(x, M, K, x.stride(0), *self.x_row, None, None),
                      (w, N, K, w.stride(0), *self.w_row, None, None, wf)]
@@ -157,13 +163,14 @@ class MXFP4Linear:
     # -- hybrid FP8 backward ----------------------------------------------------------------
     def quantize_fp8_bwd(self, dy, stream=None):
         """`_quantize_fp8_tw` of dY (row and column copies), X and W (column copies: the
-        K-major operands of the two TN GEMMs)."""
+        K-major operands of the two TN GEMMs); X's and W's amax come from the forward's
+        quantization."""
         x, w = self._saved
         sc = self.f8_scalars
         abi.mxfp4_fp8_quantize_tw_batch([
             (dy, self.M, self.N, dy.stride(0), self.dy_f8, self.dy_f8_col, sc[0:1], sc[1:2]),
-            (x, self.M, self.K, x.stride(0), None, self.x_f8_col, sc[2:3], sc[3:4]),
-            (w, self.N, self.K, w.stride(0), None, self.w_f8_col, sc[4:5], sc[5:6]),
+            (x, self.M, self.K, x.stride(0), None, self.x_f8_col, sc[2:3], sc[3:4], True),
+            (w, self.N, self.K, w.stride(0), None, self.w_f8_col, sc[4:5], sc[5:6], True),
         ], stream)
 
     def fp8_bwd_gemms(self, stream=None):
@@ -272,12 +279,15 @@ class MXFP4Block:
         out = []
         for name, L, t, b in zip(self.names, self.layers, inputs, bias):
             kind = "row" if (not self.train or L.fp8_backward) else "dual"
-            out.append((f"{name}.quant_{kind}_XW", lambda L=L, t=t: L.quantize_xw(t["X"], t["W"]), 1))
+            # the hybrid forward's quantizer also zeroes and fills the X / W amax words
+            out.append((f"{name}.quant_{kind}_XW", lambda L=L, t=t: L.quantize_xw(t["X"], t["W"]),
+                        2 if L.fp8_backward else 1))
             out.append((f"{name}.gemm_fwd", lambda L=L, b=b: L.fwd_gemm(bias=b), 1))
         if self.train:
             for name, L, t in reversed(list(zip(self.names, self.layers, inputs))):
                 if L.fp8_backward:
-                    out.append((f"{name}.quant_fp8_dY_X_W", lambda L=L, t=t: L.quantize_fp8_bwd(t["dY"]), 3))
+                    # zero, dY's amax and conversion, X's and W's conversions
+                    out.append((f"{name}.quant_fp8_dY_X_W", lambda L=L, t=t: L.quantize_fp8_bwd(t["dY"]), 5))
                     out.append((f"{name}.gemm_fp8_dgrad_wgrad", lambda L=L: L.fp8_bwd_gemms(), 1))
                 else:
                     out.append((f"{name}.quant_dual_dY",

@@ -204,3 +204,31 @@ def test_fp8_non_finite_input_is_reported(bad):
     assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
     want_qr, want_qc, want_amax, want_inv = oracle.fp8_quantize_tw(workloads.bf16_bits(y))
     assert_bytes_equal(qr.cpu().numpy(), want_qr, "finite tensor after a non-finite one")
+
+
+def test_quantize_batch_amax_output_feeds_the_fp8_quantizer():
+    # The MXFP4 quantizer's tensor amax equals the FP8 quantizer's own amax pass (bit for
+    # bit), and the FP8 quantization with amax_given gives the same codes and scale_inv.
+    from mxfp4_block_scaled_quantize_gb300 import workloads
+    for M, K, seed in ((300, 520, 1), (4608, 3072, 2), (77, 40, 3)):
+        x = workloads.student_t3((M, K), 0.3, seed)
+        ld = (K + 7) // 8 * 8
+        xg = torch.zeros((M, ld), dtype=torch.bfloat16, device="cuda")
+        xg[:, :K] = x.cuda()
+        xg = xg[:, :K]
+        rq, rs = abi.alloc_blob(M, K)
+        amax = torch.full((1,), 123.0, dtype=torch.float32, device="cuda")   # zeroed by the call
+        abi.mxfp4_quantize_batch([(xg, M, K, ld, rq, rs, None, None, 0, 0, amax)], False)
+        p = abi.fp8_pitch
+        qa = torch.empty((K, p(M)), dtype=torch.uint8, device="cuda")
+        qb = torch.empty_like(qa)
+        sa = torch.zeros(2, dtype=torch.float32, device="cuda")
+        sb = torch.zeros(2, dtype=torch.float32, device="cuda")
+        sb[0] = amax[0]
+        abi.mxfp4_fp8_quantize_tw_batch([(xg, M, K, ld, None, qa, sa[0:1], sa[1:2])])
+        abi.mxfp4_fp8_quantize_tw_batch([(xg, M, K, ld, None, qb, sb[0:1], sb[1:2], True)])
+        torch.cuda.synchronize()
+        assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+        want = x.float().abs().max().item()
+        assert amax.item() == want and sa[0].item() == want
+        assert torch.equal(qa, qb) and torch.equal(sa, sb)
