@@ -403,7 +403,8 @@ mxfp4_status mxfp4_quantize_dual_qk_norm_rope_bwd(const void* g, const void* x, 
     // Units of `span` consecutive tiles of one row block, about one unit per CTA.
     const int64_t tiles = static_cast<int64_t>(a.q.tiles_m) * a.q.tiles_k;
     const int64_t cap = static_cast<int64_t>(dev->sms) * mxfp4::quantize_norm_rope_ctas_per_sm();
-    const int64_t span = cdiv(tiles, cap) < a.q.tiles_k ? cdiv(tiles, cap) : a.q.tiles_k;
+    int64_t span = cdiv(tiles, cap) < a.q.tiles_k ? cdiv(tiles, cap) : a.q.tiles_k;
+    if (span > 3 * mxfp4::kNormRopeMaxUnitHeads - 2) span = 3 * mxfp4::kNormRopeMaxUnitHeads - 2;
     a.span = static_cast<int32_t>(span);
     a.units_per_row = static_cast<int32_t>(cdiv(a.q.tiles_k, span));
     a.units = a.q.tiles_m * a.units_per_row;

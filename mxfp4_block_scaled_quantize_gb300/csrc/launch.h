@@ -47,6 +47,7 @@ struct QuantBatch {
 // g and mixed_qkv x as bf16 2-D tensors {3*H*128, M} (box {64, 128}, 128-byte swizzle, zero
 // fill); q: the quantization task for d(mixed_qkv) [M, 3*H*128] (dual).
 constexpr int kNormRopeD = 128;   // head dimension
+constexpr int kNormRopeMaxUnitHeads = 16;   // a unit of work touches at most this many heads
 struct NormRopeArgs {
     CUtensorMap gmap;
     CUtensorMap xmap;

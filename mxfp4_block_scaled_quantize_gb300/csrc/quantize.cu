@@ -626,12 +626,14 @@ __global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
 // dx is what gets quantized: by the rowwise pass, and, written back over g in the stage, by
 // the columnwise pass after a barrier of the consumer warps.  One CTA per SM (two 32 KB
 // tiles per stage).
+
 struct NormRopeSmem {
     uint8_t tile[kQStages][kQTileBytes];   // g, overwritten by dx for q / k tiles
     uint8_t xt[kQStages][kQTileBytes];     // mixed_qkv
     uint64_t full[kQStages];
     uint64_t empty[kQStages];
     float w[2][kNormRopeD];
+    float rs[kQT][kNormRopeMaxUnitHeads * 2];   // the unit's saved r of each row, (head, part)
     int abort;
 };
 
@@ -745,6 +747,12 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_norm_rope_kernel(const 
                 sn4[i][c] = __ldg(reinterpret_cast<const float4*>(A.sinv + rrow * 64) + 4 * b + c);
             }
         }
+        // and the row's saved r of every (head, part) of the unit, into shared memory: the two
+        // lanes of the row split the loads, so each tile reads its value without a global load
+        const int h0 = tk0 / 3, nh = (tk1 - 1) / 3 - h0 + 1;
+        for (int k = static_cast<int>((lane >> 2) & 1); k < 2 * nh; k += 2)
+            sm.rs[r][k] = live ? __ldg(A.rstd + (rrow * A.H + h0) * 2 + k) : 0.0f;
+        __syncwarp();
         for (int tk = tk0; tk < tk1; ++tk, ++it) {
             const int s = it % kQStages;
             const uint32_t ph = (it / kQStages) & 1;
@@ -762,7 +770,7 @@ __global__ void __launch_bounds__(kQThreads, 1) quantize_norm_rope_kernel(const 
 
             if (have && part != 2) {
                 const float* const wv = sm.w[part];
-                const float rr = live ? __ldg(A.rstd + (rrow * A.H + head) * 2 + part) : 0.0f;
+                const float rr = sm.rs[r][(head - tk0 / 3) * 2 + part];
                 float dot = 0.0f;
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
