@@ -200,11 +200,12 @@ mxfp4_status mxfp4_quantize_dual_qk_norm_rope_bwd(const void* g, const void* x, 
  * its output buffers, as for mxfp4_quantize / mxfp4_quantize_dual (q_col and s_col are
  * read only for the dual quantizer); flags: 0, MXFP4_QUANT_2D_BLOCKS or
  * MXFP4_QUANT_RHT_COL (not both); rht_signs: the sign mask of MXFP4_QUANT_RHT_COL;
- * amax: NULL, or one fp32 in device memory (4-byte aligned) that the call sets to max |x|
- * over the tensor, the amax of the tensorwise FP8 quantizer (mxfp4_fp8_quantize_tw), from
- * the block maxima the rowwise pass takes anyway: the hybrid backward's FP8 quantization of
- * X and W then skips its own amax pass (mxfp4_fp8_quantize_task::amax_given).  A NaN or
- * infinity in x makes it non-finite, as there. */
+ * amax (row-only batches, dual == 0; MXFP4_ERR_INVALID_ARG otherwise): NULL, or one fp32
+ * in device memory (4-byte aligned) that the call sets to max |x| over the tensor, the amax
+ * of the tensorwise FP8 quantizer (mxfp4_fp8_quantize_tw), from the block maxima the
+ * rowwise pass takes anyway: the hybrid backward's FP8 quantization of X and W, whose
+ * forward is row-only, then skips its own amax pass (mxfp4_fp8_quantize_task::amax_given).
+ * A NaN or infinity in x makes it non-finite, as there. */
 typedef struct {
     const void* x;
     int64_t rows;

@@ -426,6 +426,7 @@ mxfp4_status mxfp4_quantize_batch(int32_t count, const mxfp4_quantize_task* task
         if ((t.flags & ~(MXFP4_QUANT_2D_BLOCKS | MXFP4_QUANT_RHT_COL)) != 0 ||
             t.flags == (MXFP4_QUANT_2D_BLOCKS | MXFP4_QUANT_RHT_COL) || ((t.flags & MXFP4_QUANT_RHT_COL) && !d))
             return MXFP4_ERR_INVALID_ARG;
+        if (t.amax != nullptr && d) return MXFP4_ERR_INVALID_ARG;   // row-only batches only
         if (t.amax != nullptr && (reinterpret_cast<uintptr_t>(t.amax) & 3u)) return MXFP4_ERR_MISALIGNED;
     }
     DeviceState* dev = nullptr;

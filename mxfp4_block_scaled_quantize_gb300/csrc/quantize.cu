@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
 
     // ------------------------------------------------------------------ consumers
     const uint32_t lane = lane_id();
-    uint32_t amx[kMaxQuantTasks] = {0u, 0u, 0u, 0u};   // per task: this lane's max |x| so far
+    uint32_t amx[kMaxQuantTasks] = {0u, 0u, 0u, 0u};   // row-only: per task, this lane's max |x| so far
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
         const int s = it % kQStages;
@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
                 bm[i] = m;
             }
         }
-        if (p.amax_bits != nullptr) {   // running max |x| per task, folded in once at exit
+        if (!kDual && p.amax_bits != nullptr) {   // running max |x| per task, folded in once at exit
             const uint32_t m2 = max(bm[0], bm[1]);
 #pragma unroll
             for (int k = 0; k < kMaxQuantTasks; ++k)
@@ -605,7 +605,7 @@ __global__ void __launch_bounds__(kQThreads, kSR ? 1 : kQCtasPerSm)
     // The tasks' max |x| (bf16 magnitude bits -> fp32 bits): one atomic per warp and task.
 #pragma unroll
     for (int k = 0; k < kMaxQuantTasks; ++k) {
-        if (k >= P.count || P.args[k].amax_bits == nullptr) continue;
+        if (kDual || k >= P.count || P.args[k].amax_bits == nullptr) continue;
         const uint32_t m2 = __reduce_max_sync(0xFFFFFFFFu, amx[k]);
         if (lane == 0 && m2 != 0) atomicMax(P.args[k].amax_bits, m2 << 16);
     }

@@ -107,6 +107,11 @@ def test_argument_checks_precede_any_device_use(lib):
     bad = list(ok)
     bad[11] = 120                                                    # s_row not 16-byte aligned
     assert lib.mxfp4_gemm_quantize(*bad) == abi.MXFP4_ERR_MISALIGNED
+    T2 = abi.QuantizeTask
+    amax_dual = (T2 * 1)(T2(16, 4, 8, 8, 32, 48, 64, 80, 0, 0, 96))     # amax with the dual quantizer
+    assert lib.mxfp4_quantize_batch(1, amax_dual, 1, 1, None) == abi.MXFP4_ERR_INVALID_ARG
+    amax_odd = (T2 * 1)(T2(16, 4, 8, 8, 32, 48, None, None, 0, 0, 98))  # amax not 4-byte aligned
+    assert lib.mxfp4_quantize_batch(1, amax_odd, 0, 1, None) == abi.MXFP4_ERR_MISALIGNED
     G = abi.GemmTask
     g_ok = G(16, 32, 48, 64, 4, 4, 4, 80, 4, 0)
     garr = (G * 5)(*([g_ok] * 5))
