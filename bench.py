@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--cpu-baseline-seconds S] [--no-extras]
-                    [--sr | --fp8-backward] [--bias]
+                    [--sr | --fp8-backward] [--recipes] [--bias] [--extra NAME]
 
 One step is one training step of every MXFP4 linear of the workload, in the order of a
 block's training step: each linear's forward (X and W quantized in one launch, then
@@ -15,8 +15,10 @@ Prints one JSON line (rank 0).  `value` is the step's GEMM work divided by the d
 of the whole step, quantizers included, summed over all ranks' steps.  With it: per-kernel
 medians and means, the GEMM roofline, the quantizer bandwidth, the same step replayed as a
 CUDA graph, an end-to-end step from pinned host buffers through the library's host-step
-entry point, and (N = 1, `extras`) the Flux QKV forward with row-only quantization and the
-quantizer bandwidth sweep.  Under torchrun each rank runs its own replica of the step on
+entry point, and (N = 1, `extras`) the Flux QKV forward with row-only quantization, the
+quantizer bandwidth sweep, the forward GEMM that writes its output's MXFP4 blobs and the QKV
+gradient's quantization with the norm + RoPE backward in its read (`--extra NAME` runs one
+of these alone and prints only its line).  Under torchrun each rank runs its own replica of the step on
 its own GPU (the path has no exchange step), so scaling is weak.  `--impl reference`
 times the CPU oracle on a bounded sample of the same workload instead.
 """
@@ -484,23 +486,44 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-def run_extras(args, dev, flush_l2, head_start):
+EXTRAS = ("qkv_fwd", "quant_sweep", "fwd_gemm_with_output_blobs", "qkv_bwd_norm_rope")
+
+
+def run_extras(args, dev, flush_l2, head_start, only=None):
     """Lines for the other Flux configs, timed the same way: the QKV projection forward with
     row-only quantization (X[4608,3072], W[9216,3072]), the quantizer bandwidth sweep
     (dual quantization of M x K bf16 tensors for every M in {4608, 18432, 4600} and K in
     {3072, 12288, 15360}; the largest, 18432 x 15360, moves 867 MB), the forward GEMM that
     quantizes its own output against the GEMM plus a quantizer launch, and the QKV
-    gradient's quantization with the norm + RoPE backward in its staging read."""
+    gradient's quantization with the norm + RoPE backward in its staging read.  `only`
+    names one of them (`EXTRAS`) to run it alone."""
     import torch
 
-    from mxfp4_block_scaled_quantize_gb300 import abi, workloads
-    from mxfp4_block_scaled_quantize_gb300.linear import MXFP4Block
+    from mxfp4_block_scaled_quantize_gb300 import abi
 
     peaks = load_peaks()
     stream = torch.cuda.current_stream(dev)
-    out = {}
     n = max(5, min(args.steps, 50))
+    ctx = (dev, stream, flush_l2, head_start, peaks, n)
+    parts = {"qkv_fwd": _extra_qkv_fwd, "quant_sweep": _extra_quant_sweep,
+             "fwd_gemm_with_output_blobs": _extra_fwd_gemm_output_blobs,
+             "qkv_bwd_norm_rope": _extra_qkv_bwd_norm_rope}
+    out = {}
+    for name in EXTRAS:
+        if only is None or only == name:
+            out.update(parts[name](*ctx))
+    if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
+        raise RuntimeError("device error word set during the extra lines")
+    return out
 
+
+def _extra_qkv_fwd(dev, stream, flush_l2, head_start, peaks, n):
+    import torch
+
+    from mxfp4_block_scaled_quantize_gb300 import workloads
+    from mxfp4_block_scaled_quantize_gb300.linear import MXFP4Block
+
+    out = {}
     # QKV forward (row-only X, W, then the forward GEMM)
     wl = workloads.FLUX_QKV_FWD
     lin = wl.linears[0]
@@ -529,6 +552,13 @@ def run_extras(args, dev, flush_l2, head_start):
         "step_tflops": round(lin.flops_fwd / ((statistics.mean(q_ms) + statistics.mean(g_ms)) * 1e-3) / 1e12, 1),
     }
     del blk, t
+    return out
+
+
+def _extra_quant_sweep(dev, stream, flush_l2, head_start, peaks, n):
+    import torch
+
+    from mxfp4_block_scaled_quantize_gb300 import abi, workloads
 
     # quantizer sweep: dual quantization, inputs drawn on the device from a seed (the values
     # do not change the work; the bit-exact sweep lives in the parity tests)
@@ -556,7 +586,13 @@ def run_extras(args, dev, flush_l2, head_start):
                                  "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
                                  "frac_of_spec_8tbs": round(gbs / SPEC_HBM_GBS, 4)}
             del x, outs
-    out["quant_dual_sweep"] = sweep
+    return {"quant_dual_sweep": sweep}
+
+
+def _extra_fwd_gemm_output_blobs(dev, stream, flush_l2, head_start, peaks, n):
+    import torch
+
+    from mxfp4_block_scaled_quantize_gb300 import abi, workloads
 
     # The forward GEMM whose epilogue writes its output's dual MXFP4 blobs (what the next
     # layer's forward would quantize), against the GEMM followed by the dual quantizer over
@@ -601,8 +637,14 @@ def run_extras(args, dev, flush_l2, head_start):
         ms = [a.elapsed_time(b) for a, b in ms]
         res[name] = dict(summarize(ms), tflops=round(lin.flops_fwd / (statistics.median(ms) * 1e-3) / 1e12, 1))
     res["shape"] = f"{lin.M}x{lin.N}x{lin.K}"
-    out["fwd_gemm_with_output_blobs"] = res
     del aq, a_s, bq, b_s, c, rq, rs, cq, cs
+    return {"fwd_gemm_with_output_blobs": res}
+
+
+def _extra_qkv_bwd_norm_rope(dev, stream, flush_l2, head_start, peaks, n):
+    import torch
+
+    from mxfp4_block_scaled_quantize_gb300 import abi
 
     # The QKV projection's gradient quantization with the QK RMSNorm + interleaved RoPE
     # backward in the staging read (the pages' QKV packer prologue): Flux QKV, 4608 tokens,
@@ -610,6 +652,7 @@ def run_extras(args, dev, flush_l2, head_start):
     # d(mixed_qkv) already in HBM.
     M, H = 4608, 24
     K = 3 * H * 128
+    gen = torch.Generator(device=dev)
     gen.manual_seed(77)
     g = (torch.randn((M, K), generator=gen, device=dev) * 1e-3).to(torch.bfloat16)
     x = torch.randn((M, K), generator=gen, device=dev).to(torch.bfloat16)
@@ -646,11 +689,35 @@ def run_extras(args, dev, flush_l2, head_start):
     res["fused_gbs"] = round(gbs, 1)
     res["fused_frac_of_hbm"] = round(gbs / peaks["hbm_gbs"], 4)
     res["shape"] = f"d(mixed_qkv) {M}x{K}, {H} heads of 128"
-    out["qkv_bwd_quantize_with_norm_rope_prologue"] = res
     del g, x, rstd, wq, wk, cos_t, sin_t, rq, rs, cq, cs
-    if abi.mxfp4_last_device_error() != abi.MXFP4_OK:
-        raise RuntimeError("device error word set during the extra lines")
-    return out
+    return {"qkv_bwd_quantize_with_norm_rope_prologue": res}
+
+
+def run_extra_alone(args):
+    """One extra line alone (`--extra NAME`), on the first GPU: what a profiler capture of
+    one of those kernels runs, without the step and the CPU baseline around it."""
+    import torch
+
+    from mxfp4_block_scaled_quantize_gb300 import abi
+    import __graft_entry__
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    __graft_entry__.build()
+    abi.load()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_src = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        flush_src.sum()
+
+    def head_start():
+        if hasattr(torch.cuda, "_sleep"):
+            torch.cuda._sleep(HEAD_START_CYCLES)
+    res = run_extras(args, dev, flush_l2, head_start, only=args.extra)
+    return {"extra": args.extra, "n_gpus": 1, "steps": max(5, min(args.steps, 50)),
+            "device": torch.cuda.get_device_name(dev), "result": res}
 
 
 # ---------------------------------------------------------------------------------------
@@ -817,6 +884,8 @@ def main():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the QKV-forward and quantizer-sweep lines")
+    ap.add_argument("--extra", choices=EXTRAS, default=None,
+                    help="run only this extra line (one GPU, no step, no CPU baseline)")
     ap.add_argument("--sr", action="store_true",
                     help="dY is quantized with stochastic rounding (the gradient quantizer's "
                          "`use_sr`), a new Philox seed every step")
@@ -834,6 +903,12 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     rank, world, local_rank = dist_env()
+
+    if args.extra is not None:
+        if args.impl != "ours" or world > 1:
+            raise SystemExit("--extra runs our arm on one GPU")
+        print(json.dumps(run_extra_alone(args)), flush=True)
+        return
 
     if args.impl == "reference":
         line = run_reference(args, rank, world)

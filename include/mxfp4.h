@@ -305,6 +305,24 @@ typedef struct {
  * failing task's status is returned and nothing is launched. */
 mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4_stream_t stream);
 
+/* Output tile width of the CTA-pair GEMM launches (problems of more than one 128-row tile)
+ * made by the calls that follow, process-wide:
+ *   MXFP4_TILES_AUTO    (the default) each launch takes the width whose modelled time is
+ *                       lower: the tiles dealt round-robin to the co-resident CTA pairs,
+ *                       each costing its K steps and an accumulator hand-over;
+ *   MXFP4_TILES_NARROW  256 x 256 tiles;
+ *   MXFP4_TILES_WIDE    256 x 384 tiles (a sixth fewer operand bytes per flop and a third
+ *                       fewer hand-overs, at a coarser tile grid) wherever the launch
+ *                       allows them: every pair problem of the launch with bf16 output and
+ *                       a pitch that is a multiple of 8 elements; other launches narrow.
+ * The width changes no result: the same bits come out either way (the tests check this).
+ * mxfp4_gemm_quantize always runs narrow tiles.  An unknown policy returns
+ * MXFP4_ERR_INVALID_ARG and changes nothing. */
+#define MXFP4_TILES_AUTO 0
+#define MXFP4_TILES_NARROW 1
+#define MXFP4_TILES_WIDE 2
+mxfp4_status mxfp4_gemm_set_tile_policy(int32_t policy);
+
 /* ---- hybrid FP8 backward --------------------------------------------------------------
  * `MXFP4LinearFunction.backward` in primus_turbo_mxfp4_local.py, when the layer's
  * `mxfp4_backward_precision` is "fp8" (`backward_is_fp8`): dY, X and W are quantized

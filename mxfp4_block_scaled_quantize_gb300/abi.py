@@ -28,6 +28,10 @@ MXFP4_OUT_F32 = 1
 
 MXFP4_MAX_BATCH = 4
 
+MXFP4_TILES_AUTO = 0
+MXFP4_TILES_NARROW = 1
+MXFP4_TILES_WIDE = 2
+
 
 class GemmTask(ctypes.Structure):
     """mxfp4_gemm_task of include/mxfp4.h."""
@@ -85,6 +89,7 @@ EXPORTED = (
     "mxfp4_gemm_bias",
     "mxfp4_gemm_quantize",
     "mxfp4_gemm_batch",
+    "mxfp4_gemm_set_tile_policy",
     "mxfp4_fp8_quantize_tw",
     "mxfp4_fp8_quantize_tw_batch",
     "mxfp4_fp8_gemm",
@@ -132,6 +137,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_gemm.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, i64, i32, vp]
     lib.mxfp4_gemm_bias.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, i32, vp]
     lib.mxfp4_gemm_batch.argtypes = [i32, ctypes.POINTER(GemmTask), vp]
+    lib.mxfp4_gemm_set_tile_policy.argtypes = [i32]
     lib.mxfp4_gemm_quantize.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i64, vp, vp, vp, vp, vp]
     lib.mxfp4_fp8_quantize_tw.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp]
     lib.mxfp4_fp8_quantize_tw_batch.argtypes = [i32, ctypes.POINTER(Fp8QuantizeTask), vp]
@@ -308,6 +314,11 @@ def mxfp4_gemm_batch(tasks, stream=None) -> None:
         bias = t[10] if len(t) > 10 else None
         arr[i] = GemmTask(_ptr(a_q), _ptr(a_s), _ptr(b_q), _ptr(b_s), M, N, K, _ptr(c), ldc, od, _ptr(bias))
     _check(load().mxfp4_gemm_batch(len(tasks), arr, _stream(stream)), "mxfp4_gemm_batch")
+
+
+def mxfp4_gemm_set_tile_policy(policy) -> None:
+    """MXFP4_TILES_AUTO / _NARROW / _WIDE for the CTA-pair GEMM launches that follow."""
+    _check(load().mxfp4_gemm_set_tile_policy(policy), "mxfp4_gemm_set_tile_policy")
 
 
 def mxfp4_fp8_quantize_tw(x, M, K, ldx, q_row, q_col, amax, scale_inv, stream=None) -> None:

@@ -3,6 +3,7 @@
 // synchronizes, except mxfp4_last_device_error, whose job is to synchronize.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -18,6 +19,12 @@ __device__ uint32_t g_error_word;
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 512;  // keeps tile coordinates in int32
+// Modelled cost of a CTA-pair K step (cycles of one cluster) and of a tile's accumulator
+// hand-over, for the choice of tile width.
+constexpr double kPairNarrowStepCost = 512.0;
+constexpr double kPairWideStepCost = 768.0;
+constexpr double kPairHandoverCost = 1500.0;
+std::atomic<int> g_tile_policy{MXFP4_TILES_AUTO};   // mxfp4_gemm_set_tile_policy
 
 struct DeviceState {
     int state = 0;  // 0 unknown, 1 supported, 2 unsupported
@@ -225,25 +232,87 @@ mxfp4_status gemm_fill(const mxfp4_gemm_task& t, DeviceState* dev, mxfp4::GemmAr
     return MXFP4_OK;
 }
 
-// Appends a checked GEMM to the CTA-pair batch (B box 128 rows, scale maps).
-mxfp4_status gemm_fill_pair(const mxfp4_gemm_task& t, DeviceState* dev, mxfp4::GemmPairBatch* b) {
+// Appends a checked GEMM to the CTA-pair batch (B box 128 rows, scale maps; wide tiles: the
+// 64-row B map too, and three scale groups of B per box).
+mxfp4_status gemm_fill_pair(const mxfp4_gemm_task& t, DeviceState* dev, mxfp4::GemmPairBatch* b, bool wide) {
     const int j = b->count;
     mxfp4::GemmArgs& g = b->args[j];
     mxfp4_status st = gemm_fill(t, dev, &g, &b->amap[j], &b->bmap[j], &b->cmap[j], 128);
     if (st != MXFP4_OK) return st;
+    const int64_t kp = pad128(t.K);
     if (!encode_2d(&b->sfamap[j], CU_TENSOR_MAP_DATA_TYPE_UINT64, t.a_s, static_cast<uint64_t>(g.kb4) * 64,
                    static_cast<uint64_t>(cdiv(t.M, 128)), static_cast<uint64_t>(g.kb4) * 512, 128, 1,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&b->sfbmap[j], CU_TENSOR_MAP_DATA_TYPE_UINT64, t.b_s, static_cast<uint64_t>(g.kb4) * 64,
-                   static_cast<uint64_t>(cdiv(t.N, 128)), static_cast<uint64_t>(g.kb4) * 512, 128, 2,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+                   static_cast<uint64_t>(cdiv(t.N, 128)), static_cast<uint64_t>(g.kb4) * 512, 128, wide ? 3 : 2,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        (wide && !encode_2d(&b->bmap2[j], CU_TENSOR_MAP_DATA_TYPE_UINT8, t.b_q, static_cast<uint64_t>(kp / 2),
+                            static_cast<uint64_t>(t.N), static_cast<uint64_t>(kp / 2), 128, 64,
+                            CU_TENSOR_MAP_SWIZZLE_128B)))
         return MXFP4_ERR_CUDA;
+    if (wide) {
+        if (!g.c_tma || g.out_f32) return MXFP4_ERR_INVALID_ARG;
+        g.tiles_n = static_cast<int32_t>(cdiv(t.N, mxfp4::kPairTileNWide));
+    }
     const int64_t before = j > 0 ? b->tile_end[j - 1] : 0;
     const int64_t end = before + static_cast<int64_t>(g.tiles_m2) * g.tiles_n;
     if (end > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;
     b->tile_end[j] = static_cast<int32_t>(end);
     b->count = j + 1;
     return MXFP4_OK;
+}
+
+// Tile width of a CTA-pair launch.  Wide tiles (256 x 384) need every problem's output in
+// bf16 through TMA stores.  Otherwise the launch takes the width with the lower modelled
+// time: the tiles are dealt round-robin to the clusters, as the kernel walks them; a tile
+// costs its K steps times its width (the MMA time, in units of 128 columns) times the
+// width's measured efficiency, plus a fixed accumulator hand-over; the busiest cluster sets
+// the time.
+double pair_time_model(const mxfp4_gemm_task* tasks, const bool* on_pair, int count, int clusters, int tile_n) {
+    if (clusters <= 0) return 1e300;
+    const double per_step = (tile_n == mxfp4::kPairTileNWide ? kPairWideStepCost : kPairNarrowStepCost);
+    double busiest = 0.0;
+    // tiles of each problem occupy a contiguous range of launch tile indices
+    int64_t begin[MXFP4_MAX_BATCH], ntiles[MXFP4_MAX_BATCH];
+    double cost[MXFP4_MAX_BATCH];
+    int64_t at = 0;
+    int n = 0;
+    for (int j = 0; j < count; ++j) {
+        if (!on_pair[j]) continue;
+        const int64_t kp = pad128(tasks[j].K);
+        begin[n] = at;
+        ntiles[n] = cdiv(tasks[j].M, 256) * cdiv(tasks[j].N, tile_n);
+        cost[n] = static_cast<double>(cdiv(kp, 256)) * per_step + kPairHandoverCost;
+        at += ntiles[n];
+        ++n;
+    }
+    const int64_t used = at < clusters ? at : clusters;
+    for (int64_t c = 0; c < used; ++c) {
+        double sum = 0.0;
+        for (int p = 0; p < n; ++p) {
+            // launch tiles t in [begin, begin + ntiles) with t = c (mod clusters)
+            const int64_t lo = begin[p], hi = begin[p] + ntiles[p];
+            const int64_t first = lo + ((c - lo % clusters) % clusters + clusters) % clusters;
+            if (first < hi) sum += static_cast<double>((hi - 1 - first) / clusters + 1) * cost[p];
+        }
+        busiest = sum > busiest ? sum : busiest;
+    }
+    return busiest;
+}
+
+bool pair_use_wide(const mxfp4_gemm_task* tasks, const bool* on_pair, int count, int narrow_clusters,
+                   int wide_clusters) {
+    bool any = false;
+    for (int j = 0; j < count; ++j) {
+        if (!on_pair[j]) continue;
+        any = true;
+        if (tasks[j].out_dtype != MXFP4_OUT_BF16 || (tasks[j].ldc * 2) % 16 != 0) return false;
+    }
+    if (!any || wide_clusters <= 0) return false;
+    const int policy = g_tile_policy.load(std::memory_order_relaxed);
+    if (policy != MXFP4_TILES_AUTO) return policy == MXFP4_TILES_WIDE;
+    return pair_time_model(tasks, on_pair, count, wide_clusters, mxfp4::kPairTileNWide) <
+           pair_time_model(tasks, on_pair, count, narrow_clusters, 256);
 }
 
 // ---- hybrid FP8 backward ------------------------------------------------------------
@@ -472,7 +541,7 @@ mxfp4_status mxfp4_gemm_quantize(const void* a_q, const void* a_s, const void* b
     st = device_ready(&dev);
     if (st != MXFP4_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int max_clusters = mxfp4::gemm_pair_max_clusters();
+    const int max_clusters = mxfp4::gemm_pair_max_clusters(false);
     if (M <= mxfp4::kGemmBM || max_clusters <= 0) {
         // One 128-row tile: the one-CTA GEMM, then the quantizer over C (same bytes).
         st = mxfp4_gemm_batch(1, &t, stream);
@@ -481,7 +550,7 @@ mxfp4_status mxfp4_gemm_quantize(const void* a_q, const void* a_s, const void* b
     }
     mxfp4::GemmPairBatch b;
     std::memset(&b, 0, sizeof(b));
-    st = gemm_fill_pair(t, dev, &b);
+    st = gemm_fill_pair(t, dev, &b, false);
     if (st != MXFP4_OK) return st;
     mxfp4::GemmArgs& g = b.args[0];
     if (!g.c_tma) return MXFP4_ERR_CUDA;
@@ -502,7 +571,7 @@ mxfp4_status mxfp4_gemm_quantize(const void* a_q, const void* a_s, const void* b
         return MXFP4_ERR_CUDA;
     const int64_t tiles = b.tile_end[0];
     const int clusters = static_cast<int>(tiles < max_clusters ? tiles : max_clusters);
-    return mxfp4::launch_gemm_pair(b, clusters, s, true) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+    return mxfp4::launch_gemm_pair(b, clusters, s, true, false) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
 
 mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4_stream_t stream) {
@@ -519,7 +588,11 @@ mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4
     // Problems of more than one 128-row tile share one CTA-pair launch; the others run on
     // the one-CTA kernel, one launch each.  Every task's arguments and tensor maps are
     // prepared before the first launch, so a failing task leaves nothing enqueued.
-    const int max_clusters = mxfp4::gemm_pair_max_clusters();
+    const int max_clusters = mxfp4::gemm_pair_max_clusters(false);
+    bool on_pair[MXFP4_MAX_BATCH];
+    for (int j = 0; j < count; ++j) on_pair[j] = tasks[j].M > mxfp4::kGemmBM && max_clusters > 0;
+    const int wide_clusters = mxfp4::gemm_pair_max_clusters(true);
+    const bool wide = pair_use_wide(tasks, on_pair, count, max_clusters, wide_clusters);
     mxfp4::GemmPairBatch b;
     std::memset(&b, 0, sizeof(b));
     struct Single {
@@ -530,8 +603,8 @@ mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4
     int n_single = 0;
     for (int j = 0; j < count; ++j) {
         const mxfp4_gemm_task& t = tasks[j];
-        if (t.M > mxfp4::kGemmBM && max_clusters > 0) {
-            st = gemm_fill_pair(t, dev, &b);
+        if (on_pair[j]) {
+            st = gemm_fill_pair(t, dev, &b, wide);
         } else {
             Single& o = singles[n_single++];
             st = gemm_fill(t, dev, &o.g, &o.amap, &o.bmap, &o.cmap, mxfp4::kGemmBN);
@@ -546,8 +619,16 @@ mxfp4_status mxfp4_gemm_batch(int32_t count, const mxfp4_gemm_task* tasks, mxfp4
     }
     if (b.count == 0) return MXFP4_OK;
     const int64_t pair_tiles = b.tile_end[b.count - 1];
-    const int clusters = static_cast<int>(pair_tiles < max_clusters ? pair_tiles : max_clusters);
-    return mxfp4::launch_gemm_pair(b, clusters, s) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+    const int cmax = wide ? wide_clusters : max_clusters;
+    const int clusters = static_cast<int>(pair_tiles < cmax ? pair_tiles : cmax);
+    return mxfp4::launch_gemm_pair(b, clusters, s, false, wide) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
+mxfp4_status mxfp4_gemm_set_tile_policy(int32_t policy) {
+    if (policy != MXFP4_TILES_AUTO && policy != MXFP4_TILES_NARROW && policy != MXFP4_TILES_WIDE)
+        return MXFP4_ERR_INVALID_ARG;
+    g_tile_policy.store(policy, std::memory_order_relaxed);
+    return MXFP4_OK;
 }
 
 mxfp4_status mxfp4_fp8_quantize_tw_batch(int32_t count, const mxfp4_fp8_quantize_task* tasks,

@@ -7,7 +7,7 @@
 // and one 256 x 256 x 64 MMA issued by the even CTA reads both CTAs' shared memory.  Per
 // SM that is 35 KB of operands per 256-element K step instead of 51 KB for a 128 x 256
 // tile on one SM, so the same shared memory holds five stages instead of four and L2
-// feeds a third fewer bytes per flop.
+// feeds a third fewer bytes per flop.  The wide instances own 256 x 384 tiles (PairCfg).
 //
 // Layout facts this relies on (measured on the part: each CTA's scale copy lands in its
 // own TMEM from its own shared memory, and each SM reads all N B-scales from its own TMEM):
@@ -17,12 +17,14 @@
 //
 // Roles (both CTAs run the same code; `leader` is the even CTA):
 //   warp 0      producer, both CTAs: per K step, its A half (128 rows x 128 bytes), its B
-//               half (128 x 128), its A scales (1 KB) and all B scales (2 KB) by TMA.
+//               half (128 x 128; wide: and 64 more rows), its A scales (1 KB) and all B
+//               scales (2 KB; wide 3 KB) by TMA.
 //   warp 1      TMEM allocation for the pair (512 columns, same address in both CTAs); in
 //               the leader, the MMA issuer (one elected lane of a converged warp).
 //   warp 2      leader only: waits on the barriers for the MMA warp, named-barrier hand-over.
-//   warps 3..10 epilogue, both CTAs: the CTA's own 128 accumulator rows, as in gemm.cu;
-//               each warp reports the accumulator read to the leader's `tmem_empty`.
+//   warps 3..   epilogue, both CTAs (8 warps; wide 12): the CTA's own 128 accumulator
+//               rows, a lane quarter x 128 columns per warp; each warp reports the
+//               accumulator read to the leader's `tmem_empty`.
 // Every mbarrier wait is bounded; on a timeout the CTA stops its loops, and both CTAs
 // still meet at the final cluster barrier, so neither leaves while the other may touch
 // its shared memory.
@@ -37,36 +39,58 @@ namespace mxfp4 {
 namespace {
 
 constexpr int BKB = 128;                  // bytes of K per stage (256 FP4 elements)
-constexpr int kStages = 5;
 constexpr int kABytes = 128 * BKB;        // this CTA's 128 A rows
-constexpr int kBBytes = 128 * BKB;        // this CTA's 128 of the tile's 256 B rows
 constexpr int kSfaBytes = 2 * 512;        // 2 scale atoms of this CTA's rows
-constexpr int kSfbBytes = 2 * 2 * 512;    // 2 atoms x both 128-row groups of B
-constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
-constexpr int kEpiWarps = 8;
 constexpr int kEpi0 = 3;
-constexpr int kThreads = (kEpi0 + kEpiWarps) * 32;
 constexpr uint32_t kBarHandoff = 1;
 constexpr uint32_t kBarEpilogue = 2;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfTmemBase = 256;
-constexpr uint32_t kSfTmemPerStage = 24;
 constexpr int kOutRowBytes = 64;
 constexpr int kOutBytes = 32 * kOutRowBytes;
 
+// Tile shapes.  Narrow: 256 x 256 tiles, one N 256 MMA per K slice, five stages.  Wide:
+// 256 x 384 tiles, per K slice an N 256 MMA (tile columns 0..255, accumulator columns
+// 0..255) and an N 128 MMA (tile columns 256..383, accumulator columns 256..383) on the
+// same A; each CTA stages B rows [128 r, 128 r + 128) and [256 + 64 r, 256 + 64 r + 64) of
+// the tile (r its rank), the halves the two MMAs take from it.  Per SM that is 44 KB of
+// operands for 1.5x the flops of a narrow K step (a sixth fewer bytes per flop), four stages,
+// and one accumulator hand-over per 1.5x the work; the 384 accumulator columns and four
+// stages of 32 scale columns fill the 512 TMEM columns.  12 epilogue warps.
+template <bool kWide>
+struct PairCfg {
+    static constexpr int kTileN = kWide ? 384 : 256;
+    static constexpr int kStages = kWide ? 4 : 5;
+    static constexpr int kBRows = kWide ? 192 : 128;   // this CTA's B rows per stage
+    static constexpr int kBBytes = kBRows * BKB;
+    static constexpr int kBGroups = kTileN / 128;      // 128-row scale groups of the tile's B
+    static constexpr int kSfbBytes = kBGroups * 2 * 512;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+    static constexpr int kEpiWarps = kTileN / 32;      // 4 lane quarters x 128-column groups
+    static constexpr int kThreads = (kEpi0 + kEpiWarps) * 32;
+    static constexpr uint32_t kSfTmemBase = kTileN;    // after the accumulator
+    static constexpr uint32_t kSfTmemPerStage = 4 * (2 + 2 * kBGroups);
+    static constexpr int kQuantWarps = kWide ? 1 : kEpiWarps;   // output quantization: narrow only
+};
+static_assert(PairCfg<false>::kSfTmemBase + PairCfg<false>::kStages * PairCfg<false>::kSfTmemPerStage <= kTmemCols,
+              "narrow TMEM budget");
+static_assert(PairCfg<true>::kSfTmemBase + PairCfg<true>::kStages * PairCfg<true>::kSfTmemPerStage <= kTmemCols,
+              "wide TMEM budget");
+
+template <bool kWide>
 struct PairSmem {
-    uint8_t a[kStages][kABytes];          // 1024-byte aligned (128-byte swizzle atoms)
-    uint8_t b[kStages][kBBytes];
-    uint8_t sfa[kStages][kSfaBytes];
-    uint8_t sfb[kStages][kSfbBytes];
-    uint8_t out[kEpiWarps][kOutBytes];
+    using C = PairCfg<kWide>;
+    uint8_t a[C::kStages][kABytes];       // 1024-byte aligned (128-byte swizzle atoms)
+    uint8_t b[C::kStages][C::kBBytes];
+    uint8_t sfa[C::kStages][kSfaBytes];
+    uint8_t sfb[C::kStages][C::kSfbBytes];
+    uint8_t out[C::kEpiWarps][kOutBytes];
     // output quantization: per epilogue warp, the row-blob codes of its 32 rows x 128
     // columns (32 x 64 bytes, 64-byte swizzle) and the col-blob codes of its 128 columns x 32
     // rows (128 x 16 bytes), each leaving in one tensor store
-    uint8_t qrow[kEpiWarps][kOutBytes];
-    uint8_t qcol[kEpiWarps][kOutBytes];
-    uint64_t full[kStages];               // used in the leader: both CTAs' bytes
-    uint64_t empty[kStages];              // each CTA: the leader's MMA commit
+    uint8_t qrow[C::kQuantWarps][kOutBytes];
+    uint8_t qcol[C::kQuantWarps][kOutBytes];
+    uint64_t full[C::kStages];            // used in the leader: both CTAs' bytes
+    uint64_t empty[C::kStages];           // each CTA: the leader's MMA commit
     uint64_t tmem_full;                   // each CTA: the leader's commit after a tile
     uint64_t tmem_empty;                  // used in the leader: 2 x kEpiWarps arrivals
     uint64_t drain;
@@ -74,13 +98,13 @@ struct PairSmem {
     int abort;
 };
 
-// tcgen05.mma kind::mxf4 instruction descriptor, M = 256 (the pair), N = 256.
-__device__ __forceinline__ uint32_t pair_idesc(uint32_t sf_id) {
+// tcgen05.mma kind::mxf4 instruction descriptor, M = 256 (the pair), N = n.
+__device__ __forceinline__ uint32_t pair_idesc(uint32_t sf_id, uint32_t n) {
     uint32_t d = 0;
     d |= sf_id << 4;
     d |= 1u << 7;
     d |= 1u << 10;
-    d |= static_cast<uint32_t>(256 >> 3) << 17;
+    d |= (n >> 3) << 17;
     d |= 1u << 23;
     d |= static_cast<uint32_t>(256 >> 4) << 24;
     d |= sf_id << 29;
@@ -221,11 +245,16 @@ __device__ __forceinline__ void quantize_out_piece(const GemmArgs& g, const uint
 // kBias: some problem of the launch carries a bias (the instance without one compiles the
 // plain conversion only).
 // kQuant: the epilogue also writes the MXFP4 blobs of C (one problem, bf16 through TMA).
-template <bool kBatched, bool kBias, bool kQuant>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// kWide: 256 x 384 tiles (PairCfg); every problem bf16 out through TMA stores, no kQuant.
+template <bool kBatched, bool kBias, bool kQuant, bool kWide>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kWide>::kThreads, 1)
     gemm_mxf4_pair_kernel(const __grid_constant__ GemmPairBatch P) {
+    using C = PairCfg<kWide>;
+    static_assert(!(kWide && kQuant), "output quantization runs on narrow tiles");
+    constexpr int kStages = C::kStages;
+    constexpr int kEpiWarps = C::kEpiWarps;
     extern __shared__ uint8_t smem_raw[];
-    PairSmem& sm = *reinterpret_cast<PairSmem*>(
+    PairSmem<kWide>& sm = *reinterpret_cast<PairSmem<kWide>*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
     const int tid = threadIdx.x;
@@ -290,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const GemmArgs& g = P.args[j];
                 const int mt2 = lt % g.tiles_m2, nt = lt / g.tiles_m2;
                 const int arow = mt2 * 256 + static_cast<int>(rank) * 128;
-                const int brow = nt * 256 + static_cast<int>(rank) * 128;
+                const int brow = nt * C::kTileN + static_cast<int>(rank) * 128;
                 for (int ks = 0; ks < g.k_stages; ++ks, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
@@ -298,14 +327,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (leader) mbar_arrive_expect_tx(smem_addr(&sm.full[s]), 2 * kStageBytes);
+                    if (leader) mbar_arrive_expect_tx(smem_addr(&sm.full[s]), 2 * C::kStageBytes);
                     const uint32_t bar = cluster_map(smem_addr(&sm.full[s]), 0);
                     tma_load_2d_pair(smem_addr(sm.a[s]), &P.amap[j], ks * BKB, arow, bar, pol);
                     tma_load_2d_pair(smem_addr(sm.b[s]), &P.bmap[j], ks * BKB, brow, bar, pol);
+                    if (kWide)
+                        tma_load_2d_pair(smem_addr(sm.b[s]) + 128 * BKB, &P.bmap2[j], ks * BKB,
+                                         nt * C::kTileN + 256 + static_cast<int>(rank) * 64, bar, pol);
                     // Scale maps count 8-byte units: 2 atoms = 128 units per K step.
                     tma_load_2d_pair(smem_addr(sm.sfa[s]), &P.sfamap[j], ks * 128, 2 * mt2 + static_cast<int>(rank),
                                      bar, pol);
-                    tma_load_2d_pair(smem_addr(sm.sfb[s]), &P.sfbmap[j], ks * 128, 2 * nt, bar, pol);
+                    tma_load_2d_pair(smem_addr(sm.sfb[s]), &P.sfbmap[j], ks * 128, C::kBGroups * nt, bar, pol);
                 }
             }
             // Drain (leader): every armed stage, both CTAs' bytes, has landed.
@@ -334,21 +366,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         tc_fence_after_sync();
                         const int s = it % kStages;
                         const int natoms = min(2, g.kb4 - 2 * ks);
-                        const uint32_t sf = tmem + kSfTmemBase + s * kSfTmemPerStage;
+                        // TMEM scale slot of the stage: A atoms a at columns 4a, then per atom a
+                        // the B groups gb at 8 + 4 (kBGroups a + gb)
+                        const uint32_t sf = tmem + C::kSfTmemBase + s * C::kSfTmemPerStage;
                         const uint32_t sfa_s = smem_addr(sm.sfa[s]);
                         const uint32_t sfb_s = smem_addr(sm.sfb[s]);
                         for (int a = 0; a < natoms; ++a) {
                             tc_cp_32x128b_warpx4_pair(sf + a * 4, smem_desc(sfa_s + a * 512, 0, 128, 0));
-                            tc_cp_32x128b_warpx4_pair(sf + 8 + a * 8, smem_desc(sfb_s + a * 512, 0, 128, 0));
-                            tc_cp_32x128b_warpx4_pair(sf + 8 + a * 8 + 4,
-                                                      smem_desc(sfb_s + 1024 + a * 512, 0, 128, 0));
+#pragma unroll
+                            for (int gb = 0; gb < C::kBGroups; ++gb)
+                                tc_cp_32x128b_warpx4_pair(sf + 8 + (a * C::kBGroups + gb) * 4,
+                                                          smem_desc(sfb_s + gb * 1024 + a * 512, 0, 128, 0));
                         }
                         const uint64_t adesc = smem_desc(smem_addr(sm.a[s]), 16, 1024, 2);
                         const uint64_t bdesc = smem_desc(smem_addr(sm.b[s]), 16, 1024, 2);
+                        const uint64_t bdesc2 = smem_desc(smem_addr(sm.b[s]) + 128 * BKB, 16, 1024, 2);
                         for (int j = 0; j < natoms * 2; ++j) {
                             const uint32_t sf_id = (j & 1) * 2;
-                            tc_mma_mxf4_pair(tmem, adesc + 2 * j, bdesc + 2 * j, pair_idesc(sf_id),
-                                             sf + (j >> 1) * 4, sf + 8 + (j >> 1) * 8, (ks | j) != 0);
+                            const uint32_t sfb = sf + 8 + (j >> 1) * 4 * C::kBGroups;
+                            tc_mma_mxf4_pair(tmem, adesc + 2 * j, bdesc + 2 * j, pair_idesc(sf_id, 256),
+                                             sf + (j >> 1) * 4, sfb, (ks | j) != 0);
+                            if (kWide)
+                                tc_mma_mxf4_pair(tmem + 256, adesc + 2 * j, bdesc2 + 2 * j, pair_idesc(sf_id, 128),
+                                                 sf + (j >> 1) * 4, sfb + 8, (ks | j) != 0);
                         }
                         tc_commit_pair_multicast(smem_addr(&sm.empty[s]), 3);
                         if (ks == g.k_stages - 1) tc_commit_pair_multicast(smem_addr(&sm.tmem_full), 3);
@@ -390,8 +430,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int h = (warp - kEpi0) >> 2;
         const uint32_t obuf = smem_addr(sm.out[warp - kEpi0]);
-        const uint32_t qrow_buf = smem_addr(sm.qrow[warp - kEpi0]);
-        const uint32_t qcol_buf = smem_addr(sm.qcol[warp - kEpi0]);
+        const uint32_t qrow_buf = kQuant ? smem_addr(sm.qrow[warp - kEpi0]) : 0u;
+        const uint32_t qcol_buf = kQuant ? smem_addr(sm.qcol[warp - kEpi0]) : 0u;
         const uint64_t pol = l2_policy_evict_first();
         const uint32_t leader_tmem_empty = cluster_map(smem_addr(&sm.tmem_empty), 0);
         if (lane == 0) {
@@ -409,8 +449,59 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 okw = mbar_wait(smem_addr(&sm.tmem_full), tl & 1, err, kErrGemmEpilogue, &sm.abort);
             if (!named_barrier_and(kBarEpilogue, kEpiWarps * 32, __shfl_sync(0xFFFFFFFFu, okw, 0) != 0)) break;
             tc_fence_after_sync();
-            uint32_t v[4][32];
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128;
+            if (kWide) {
+                // bf16 through TMA stores.  The accumulator is read in two halves of 64
+                // columns, the first converted to bf16 pairs while the second is read, so no
+                // more than 64 fp32 values are live (the 480-thread CTA has 136 registers a
+                // thread); the accumulator is released as soon as the second half is in.
+                int lt;
+                const int pj = task_of(t, &lt);
+                const GemmArgs& g = P.args[pj];
+                const int mt2 = lt % g.tiles_m2, nt = lt / g.tiles_m2;
+                const int64_t row0 = static_cast<int64_t>(mt2) * 256 + rank * 128 + q * 32;
+                const int64_t col0 = static_cast<int64_t>(nt) * C::kTileN + h * 128;
+                const uint16_t* const bias = kBias ? g.bias : nullptr;
+                uint32_t wb[4][16];
+                {
+                    uint32_t v0[32], v1[32];
+                    tc_ld_32x32b_x32(taddr + 0, v0);
+                    tc_ld_32x32b_x32(taddr + 32, v1);
+                    tc_wait_ld();
+                    convert_piece<false>(v0, bias, col0, g.N, wb[0]);
+                    convert_piece<false>(v1, bias, col0 + 32, g.N, wb[1]);
+                    // the first half's bf16 pairs exist before the second half is read
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(wb[0][i]), "+r"(wb[1][i]));
+                    tc_ld_32x32b_x32(taddr + 64, v0);
+                    tc_ld_32x32b_x32(taddr + 96, v1);
+                    tc_wait_ld();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster_relaxed(leader_tmem_empty);
+                    convert_piece<false>(v0, bias, col0 + 64, g.N, wb[2]);
+                    convert_piece<false>(v1, bias, col0 + 96, g.N, wb[3]);
+                }
+                if (row0 >= g.M || col0 >= g.N) continue;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (col0 + c * 32 >= g.N) break;
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        sts128(obuf + swz64(lane, j), wb[c][4 * j], wb[c][4 * j + 1], wb[c][4 * j + 2], wb[c][4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d_hint(&P.cmap[pj], static_cast<int32_t>(col0 + c * 32), static_cast<int32_t>(row0),
+                                          obuf, pol);
+                        bulk_commit_group();
+                    }
+                }
+                continue;
+            }
+            uint32_t v[4][32];
             tc_ld_32x32b_x32(taddr + 0, v[0]);
             tc_ld_32x32b_x32(taddr + 32, v[1]);
             tc_ld_32x32b_x32(taddr + 64, v[2]);
@@ -528,36 +619,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-size_t gemm_pair_smem_bytes() { return sizeof(PairSmem) + 1024; }
+size_t gemm_pair_smem_bytes(bool wide) {
+    return (wide ? sizeof(PairSmem<true>) : sizeof(PairSmem<false>)) + 1024;
+}
 
-int gemm_pair_max_clusters() {
-    static int cached[64] = {0};
+int gemm_pair_max_clusters(bool wide) {
+    static int cached[2][64] = {{0}};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached[dev] > 0) return cached[dev];
-    const size_t smem = gemm_pair_smem_bytes();
-    if (cudaFuncSetAttribute(gemm_mxf4_pair_kernel<true, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-        return 0;
+    if (cached[wide][dev] > 0) return cached[wide][dev];
+    const size_t smem = gemm_pair_smem_bytes(wide);
+    auto kernel = wide ? gemm_mxf4_pair_kernel<true, true, false, true> : gemm_mxf4_pair_kernel<true, true, false, false>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(wide ? PairCfg<true>::kThreads : PairCfg<false>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_mxf4_pair_kernel<true, true, false>, &cfg) != cudaSuccess) return 0;
-    cached[dev] = n;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return 0;
+    cached[wide][dev] = n;
     return n;
 }
 
-cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream, bool quant) {
-    const size_t smem = gemm_pair_smem_bytes();
+cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream, bool quant, bool wide) {
+    const size_t smem = gemm_pair_smem_bytes(wide);
     bool bias = false;
     for (int j = 0; j < b.count; ++j) bias = bias || b.args[j].bias != nullptr;
-    if (quant && (b.count != 1 || b.args[0].out_f32 || !b.args[0].c_tma || b.args[0].qo_row == nullptr))
+    if (quant && (wide || b.count != 1 || b.args[0].out_f32 || !b.args[0].c_tma || b.args[0].qo_row == nullptr))
         return cudaErrorInvalidValue;
-    auto kernel = quant        ? (bias ? gemm_mxf4_pair_kernel<false, true, true> : gemm_mxf4_pair_kernel<false, false, true>)
-                  : b.count > 1 ? (bias ? gemm_mxf4_pair_kernel<true, true, false> : gemm_mxf4_pair_kernel<true, false, false>)
-                               : (bias ? gemm_mxf4_pair_kernel<false, true, false> : gemm_mxf4_pair_kernel<false, false, false>);
+    if (wide)
+        for (int j = 0; j < b.count; ++j)
+            if (b.args[j].out_f32 || !b.args[j].c_tma) return cudaErrorInvalidValue;
+    using K = void (*)(GemmPairBatch);
+    K kernel;
+    if (quant)
+        kernel = bias ? gemm_mxf4_pair_kernel<false, true, true, false> : gemm_mxf4_pair_kernel<false, false, true, false>;
+    else if (wide)
+        kernel = b.count > 1 ? (bias ? gemm_mxf4_pair_kernel<true, true, false, true> : gemm_mxf4_pair_kernel<true, false, false, true>)
+                             : (bias ? gemm_mxf4_pair_kernel<false, true, false, true> : gemm_mxf4_pair_kernel<false, false, false, true>);
+    else
+        kernel = b.count > 1 ? (bias ? gemm_mxf4_pair_kernel<true, true, false, false> : gemm_mxf4_pair_kernel<true, false, false, false>)
+                             : (bias ? gemm_mxf4_pair_kernel<false, true, false, false> : gemm_mxf4_pair_kernel<false, false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
@@ -565,7 +667,7 @@ cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(wide ? PairCfg<true>::kThreads : PairCfg<false>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;

@@ -113,16 +113,19 @@ constexpr int kGemmBN = 256;
 cudaError_t launch_gemm(const CUtensorMap& amap, const CUtensorMap& bmap, const CUtensorMap& cmap,
                         const GemmArgs& g, int grid, cudaStream_t stream);
 
-// The CTA-pair kernel (gemm_pair.cu): 256 x 256 tiles on clusters of two CTAs, over up to
-// kMaxGemmTasks independent problems in one launch (tile t belongs to the first problem j
-// with t < tile_end[j]).  Per problem: amap / bmap as for launch_gemm but with a B box of
-// 128 rows; sfamap / sfbmap: the A / B scale blobs as 2-D u64 tensors
-// {Kp/128 * 64, ceil(rows/128)} (one row per 128-row group of atoms), boxes {128, 1} /
-// {128, 2}; cmap as for launch_gemm.  `clusters` CTA pairs.
+// The CTA-pair kernel (gemm_pair.cu): 256 x 256 (narrow) or 256 x 384 (wide) tiles on
+// clusters of two CTAs, over up to kMaxGemmTasks independent problems in one launch (tile t
+// belongs to the first problem j with t < tile_end[j]; GemmArgs::tiles_n counts the
+// launch's tile width).  Per problem: amap / bmap as for launch_gemm but with a B box of
+// 128 rows; bmap2 (wide only): B with a box of 64 rows; sfamap / sfbmap: the A / B scale
+// blobs as 2-D u64 tensors {Kp/128 * 64, ceil(rows/128)} (one row per 128-row group of
+// atoms), boxes {128, 1} / {128, 2 | 3 (wide)}; cmap as for launch_gemm.  `clusters` CTA
+// pairs.
 constexpr int kMaxGemmTasks = 4;
 struct GemmPairBatch {
     CUtensorMap amap[kMaxGemmTasks];
     CUtensorMap bmap[kMaxGemmTasks];
+    CUtensorMap bmap2[kMaxGemmTasks];
     CUtensorMap cmap[kMaxGemmTasks];
     CUtensorMap sfamap[kMaxGemmTasks];
     CUtensorMap sfbmap[kMaxGemmTasks];
@@ -134,11 +137,13 @@ struct GemmPairBatch {
     CUtensorMap qrowmap;
     CUtensorMap qcolmap;
 };
-size_t gemm_pair_smem_bytes();
-int gemm_pair_max_clusters();   // co-resident clusters of the pair kernel, 0 if none
+constexpr int kPairTileNWide = 384;
+size_t gemm_pair_smem_bytes(bool wide);
+int gemm_pair_max_clusters(bool wide);   // co-resident clusters of the pair kernel, 0 if none
 // quant: one problem (b.count == 1) whose epilogue also writes the MXFP4 blobs of C
-// (GemmArgs::qo_row ..); C in bf16 through TMA stores (c_tma).
-cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream, bool quant = false);
+// (GemmArgs::qo_row ..); C in bf16 through TMA stores (c_tma); narrow tiles.
+// wide: 256 x 384 tiles; every problem bf16 out through TMA stores (c_tma).
+cudaError_t launch_gemm_pair(const GemmPairBatch& b, int clusters, cudaStream_t stream, bool quant, bool wide);
 
 // ---- diagnostics -----------------------------------------------------------------------
 cudaError_t launch_selftest_wait(uint32_t* err, uint64_t timeout_ns, cudaStream_t stream);

@@ -400,3 +400,105 @@ def test_step_with_both_recipes(shape, sr_seed, out_dtype):
     check_gemm(dx, c, cabs, f"recipes dgrad {shape}")
     c, cabs = oracle.gemm(*dyc, *xc)
     check_gemm(dw, c, cabs, f"recipes wgrad {shape}")
+
+
+@pytest.fixture
+def tile_policy():
+    """Set the CTA-pair tile width for one test; AUTO again afterwards."""
+    yield abi.mxfp4_gemm_set_tile_policy
+    abi.mxfp4_gemm_set_tile_policy(abi.MXFP4_TILES_AUTO)
+
+
+@pytest.mark.parametrize("M,N,K", [(384, 768, 640), (300, 520, 1000), (513, 1000, 2048), (257, 385, 128),
+                                   (1000, 1152, 384), (640, 2304, 4608), (2048, 383, 256)])
+def test_wide_tiles_match_oracle_and_narrow_tiles(M, N, K, tile_policy):
+    # 256 x 384 tiles (one N 256 and one N 128 MMA per K slice, ragged M, N and K edges,
+    # tile grids of one to several waves) against the oracle, and bit for bit against the
+    # 256 x 256 tiles.
+    a = workloads.student_t3((M, K), 1.0, 11 + M + 3 * N + 7 * K)
+    b = workloads.normal((N, K), 0.5, 13 + M + 5 * N + 11 * K)
+    tile_policy(abi.MXFP4_TILES_WIDE)
+    wide = gpu_gemm_from_bf16(a, b, torch.bfloat16)
+    tile_policy(abi.MXFP4_TILES_NARROW)
+    narrow = gpu_gemm_from_bf16(a, b, torch.bfloat16)
+    c, cabs = oracle_gemm_from_bf16(a, b)
+    check_gemm(wide, c, cabs, f"wide gemm {M}x{N}x{K}")
+    assert torch.equal(wide.view(torch.uint8).cpu(), narrow.view(torch.uint8).cpu())
+
+
+@pytest.mark.parametrize("M,N,K", [(384, 768, 640), (513, 1000, 2048)])
+def test_wide_tiles_with_bias(M, N, K, tile_policy):
+    a = workloads.student_t3((M, K), 1.0, 41 + M + 3 * N + 7 * K)
+    b = workloads.normal((N, K), 0.5, 43 + M + 5 * N + 11 * K)
+    bits, bias = bias_bf16(N, 47 + M + N + K)
+    aq, a_s = abi.quantize(pitched(a), dual=False)
+    bq, b_s = abi.quantize(pitched(b), dual=False)
+    tile_policy(abi.MXFP4_TILES_WIDE)
+    out = abi.gemm(aq, a_s, bq, b_s, M, N, K, out_dtype=torch.bfloat16, bias=bias)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    c, cabs = oracle_gemm_from_bf16(a, b)
+    check_gemm_bias(out, c, cabs, bits, f"wide gemm+bias {M}x{N}x{K}")
+
+
+def test_wide_policy_batch_equals_narrow_singles(tile_policy):
+    # A batch under the wide policy (bf16 pair problems, a one-CTA problem beside them, a
+    # pitched output) gives each problem the bytes of its own narrow call; a batch holding an
+    # fp32 pair problem runs narrow tiles and gives the same bytes too.
+    probs = [(384, 768, 640, torch.bfloat16, 776), (513, 1000, 2048, torch.bfloat16, 1000),
+             (64, 1000, 4600, torch.bfloat16, 1000), (300, 520, 1000, torch.float32, 520)]
+    ins, singles = [], []
+    tile_policy(abi.MXFP4_TILES_NARROW)
+    for i, (M, N, K, od, ldc) in enumerate(probs):
+        a = workloads.student_t3((M, K), 1.0, 601 + i)
+        b = workloads.normal((N, K), 0.5, 701 + i)
+        aq, a_s = abi.quantize(pitched(a), dual=False)
+        bq, b_s = abi.quantize(pitched(b), dual=False)
+        code = abi.MXFP4_OUT_F32 if od == torch.float32 else abi.MXFP4_OUT_BF16
+        ins.append((aq, a_s, bq, b_s, M, N, K, code))
+        ref = torch.full((M, ldc), float("nan"), dtype=od, device="cuda")
+        abi.mxfp4_gemm(aq, a_s, bq, b_s, M, N, K, ref, ldc, code)
+        singles.append(ref)
+    torch.cuda.synchronize()
+    tile_policy(abi.MXFP4_TILES_WIDE)
+    for sel in ((0, 1, 2), (0, 3)):
+        outs, tasks = [], []
+        for i in sel:
+            aq, a_s, bq, b_s, M, N, K, code = ins[i]
+            out = torch.full(singles[i].shape, float("nan"), dtype=singles[i].dtype, device="cuda")
+            tasks.append((aq, a_s, bq, b_s, M, N, K, out, out.stride(0), code))
+            outs.append(out)
+        abi.mxfp4_gemm_batch(tasks)
+        torch.cuda.synchronize()
+        assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+        for i, out in zip(sel, outs):
+            assert torch.equal(out.view(torch.uint8).cpu(), singles[i].view(torch.uint8).cpu())
+
+
+def test_flux_linear1_step_wide_tiles_sampled(tile_policy):
+    # The single-stream block's linear1 training step at full size on 256 x 384 tiles: the
+    # forward 4608 x 21504 x 3072, and dgrad 4608 x 3072 x 21504 with wgrad 21504 x 3072 x
+    # 4608 in one launch, as the step runs them; sampled rows against the oracle.
+    wl = workloads.FLUX_SINGLE_BLOCK
+    lin = wl.linears[0]
+    t = wl.tensors(0)
+    tile_policy(abi.MXFP4_TILES_WIDE)
+    layer = MXFP4Linear(lin.M, lin.N, lin.K, train=True)
+    y, dx, dw = layer.step(t["X"].cuda(), t["W"].cuda(), t["dY"].cuda())
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    xb, wb, dyb = (workloads.bf16_bits(t[k]) for k in ("X", "W", "dY"))
+    rows = _sample_rows(lin.M, 6, 3)
+    aq, a_s = oracle.quantize_row(np.ascontiguousarray(xb[rows]))
+    wq, ws = oracle.quantize_row(wb)
+    c, cabs = oracle.gemm(aq, a_s, wq, ws)
+    check_gemm(y[torch.as_tensor(rows, device="cuda")], c, cabs, "linear1 fwd (wide)")
+    aq, a_s = oracle.quantize_row(np.ascontiguousarray(dyb[rows]))
+    wcq, wcs = oracle.quantize_col(wb)
+    c, cabs = oracle.gemm(aq, a_s, wcq, wcs)
+    check_gemm(dx[torch.as_tensor(rows, device="cuda")], c, cabs, "linear1 dgrad (wide)")
+    nrows = _sample_rows(lin.N, 6, 4)
+    aq, a_s = oracle.quantize_col(np.ascontiguousarray(dyb[:, nrows]))
+    xcq, xcs = oracle.quantize_col(xb)
+    c, cabs = oracle.gemm(aq, a_s, xcq, xcs)
+    check_gemm(dw[torch.as_tensor(nrows, device="cuda")], c, cabs, "linear1 wgrad (wide)")
