@@ -24,6 +24,13 @@ constexpr int64_t kMaxDim = (int64_t{1} << 31) - 512;  // keeps tile coordinates
 constexpr double kPairNarrowStepCost = 512.0;
 constexpr double kPairWideStepCost = 768.0;
 constexpr double kPairHandoverCost = 1500.0;
+// Tile order of the pair kernel: problems of up to kPairGroupAllRows row tiles walk all of
+// them fastest (the co-resident clusters cover every A row tile, each B column tile is read
+// once); taller ones walk groups of kPairGroupM row tiles, so A streams once instead of once
+// per column tile (measured on the Flux wgrad, M 21504: 187.9 -> 180.1 us for dgrad + wgrad;
+// a grouped order on the 18-row-tile forward cost 5-7 %).
+constexpr int32_t kPairGroupAllRows = 24;
+constexpr int32_t kPairGroupM = 8;
 std::atomic<int> g_tile_policy{MXFP4_TILES_AUTO};   // mxfp4_gemm_set_tile_policy
 
 struct DeviceState {
@@ -254,6 +261,7 @@ mxfp4_status gemm_fill_pair(const mxfp4_gemm_task& t, DeviceState* dev, mxfp4::G
         if (!g.c_tma || g.out_f32) return MXFP4_ERR_INVALID_ARG;
         g.tiles_n = static_cast<int32_t>(cdiv(t.N, mxfp4::kPairTileNWide));
     }
+    g.group_m = g.tiles_m2 <= kPairGroupAllRows ? g.tiles_m2 : kPairGroupM;
     const int64_t before = j > 0 ? b->tile_end[j - 1] : 0;
     const int64_t end = before + static_cast<int64_t>(g.tiles_m2) * g.tiles_n;
     if (end > (int64_t{1} << 31) - 1) return MXFP4_ERR_INVALID_ARG;

@@ -239,6 +239,19 @@ __device__ __forceinline__ void quantize_out_piece(const GemmArgs& g, const uint
     }
 }
 
+// Row tile mt2 and column tile nt of a problem's tile lt.  The tiles are walked in groups of
+// g.group_m row tiles, the row tile fastest within a group: the clusters at work at one time
+// share a few A row tiles and the group's B tiles, which L2 keeps.
+__device__ __forceinline__ void pair_tile_coords(int lt, const GemmArgs& g, int* mt2, int* nt) {
+    const int per_group = g.group_m * g.tiles_n;
+    const int grp = lt / per_group;
+    const int first = grp * g.group_m;
+    const int gm = min(g.tiles_m2 - first, g.group_m);
+    const int r = lt - grp * per_group;
+    *mt2 = first + r % gm;
+    *nt = r / gm;
+}
+
 // kBatched = false: one problem (P.count == 1); its arguments stay constant-bank operands,
 // which the batched form's run-time problem index turns into registers (measured: the
 // forward GEMM spilled and lost 4 us in the batched form).
@@ -317,7 +330,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kWide>::kThr
                 int lt;
                 const int j = task_of(t, &lt);
                 const GemmArgs& g = P.args[j];
-                const int mt2 = lt % g.tiles_m2, nt = lt / g.tiles_m2;
+                int mt2, nt;
+                pair_tile_coords(lt, g, &mt2, &nt);
                 const int arow = mt2 * 256 + static_cast<int>(rank) * 128;
                 const int brow = nt * C::kTileN + static_cast<int>(rank) * 128;
                 for (int ks = 0; ks < g.k_stages; ++ks, ++it) {
@@ -458,7 +472,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kWide>::kThr
                 int lt;
                 const int pj = task_of(t, &lt);
                 const GemmArgs& g = P.args[pj];
-                const int mt2 = lt % g.tiles_m2, nt = lt / g.tiles_m2;
+                int mt2, nt;
+                pair_tile_coords(lt, g, &mt2, &nt);
                 const int64_t row0 = static_cast<int64_t>(mt2) * 256 + rank * 128 + q * 32;
                 const int64_t col0 = static_cast<int64_t>(nt) * C::kTileN + h * 128;
                 const uint16_t* const bias = kBias ? g.bias : nullptr;
@@ -514,7 +529,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kWide>::kThr
             int lt;
             const int pj = task_of(t, &lt);
             const GemmArgs& g = P.args[pj];
-            const int mt2 = lt % g.tiles_m2, nt = lt / g.tiles_m2;
+            int mt2, nt;
+            pair_tile_coords(lt, g, &mt2, &nt);
             const int64_t row0 = static_cast<int64_t>(mt2) * 256 + rank * 128 + q * 32;
             const int64_t col0 = static_cast<int64_t>(nt) * 256 + h * 128;
             if (kQuant) {

@@ -80,6 +80,7 @@ struct GemmArgs {
     int32_t tiles_m;     // ceil(M / 128)
     int32_t tiles_n;     // ceil(N / 256)
     int32_t tiles_m2;    // ceil(M / 256): row tiles of the CTA-pair kernel
+    int32_t group_m;     // pair kernel: row tiles per group of its tile order (1..tiles_m2)
     int32_t k_stages;    // ceil(Kp / 256): 256-element (128-byte) K steps
     int32_t kb4;         // Kp / 128: 4-block scale groups per row (scale atoms along K)
     int32_t groups_b;    // ceil(N / 128): 128-row scale groups of B
