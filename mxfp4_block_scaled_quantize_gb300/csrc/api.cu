@@ -258,7 +258,12 @@ mxfp4_status gemm_fill_pair(const mxfp4_gemm_task& t, DeviceState* dev, mxfp4::G
                             CU_TENSOR_MAP_SWIZZLE_128B)))
         return MXFP4_ERR_CUDA;
     if (wide) {
-        if (!g.c_tma || g.out_f32) return MXFP4_ERR_INVALID_ARG;
+        // C as bf16 {N, M}, box {32 columns, 128 rows}: a column group's four epilogue warps
+        // store their 128 rows together
+        if (!g.c_tma || g.out_f32 ||
+            !encode_2d(&b->cmap[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, t.c, static_cast<uint64_t>(t.N),
+                       static_cast<uint64_t>(t.M), static_cast<uint64_t>(t.ldc * 2), 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+            return MXFP4_ERR_INVALID_ARG;
         g.tiles_n = static_cast<int32_t>(cdiv(t.N, mxfp4::kPairTileNWide));
     }
     g.group_m = g.tiles_m2 <= kPairGroupAllRows ? g.tiles_m2 : kPairGroupM;

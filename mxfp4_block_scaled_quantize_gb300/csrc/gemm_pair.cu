@@ -44,6 +44,7 @@ constexpr int kSfaBytes = 2 * 512;        // 2 scale atoms of this CTA's rows
 constexpr int kEpi0 = 3;
 constexpr uint32_t kBarHandoff = 1;
 constexpr uint32_t kBarEpilogue = 2;
+constexpr uint32_t kBarStore0 = 3;        // wide: + column group h, the group's four warps
 constexpr uint32_t kTmemCols = 512;
 constexpr int kOutRowBytes = 64;
 constexpr int kOutBytes = 32 * kOutRowBytes;
@@ -467,14 +468,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kWide>::kThr
             if (kWide) {
                 // bf16 through TMA stores.  The accumulator is read in two halves of 64
                 // columns, the first converted to bf16 pairs while the second is read, so no
-                // more than 64 fp32 values are live (the 480-thread CTA has 136 registers a
+                // more than 64 fp32 values are live (the 480-thread CTA has 128 registers a
                 // thread); the accumulator is released as soon as the second half is in.
                 int lt;
                 const int pj = task_of(t, &lt);
                 const GemmArgs& g = P.args[pj];
                 int mt2, nt;
                 pair_tile_coords(lt, g, &mt2, &nt);
-                const int64_t row0 = static_cast<int64_t>(mt2) * 256 + rank * 128 + q * 32;
+                const int64_t rowblk = static_cast<int64_t>(mt2) * 256 + rank * 128;
                 const int64_t col0 = static_cast<int64_t>(nt) * C::kTileN + h * 128;
                 const uint16_t* const bias = kBias ? g.bias : nullptr;
                 uint32_t wb[4][16];
@@ -497,22 +498,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kWide>::kThr
                     convert_piece<false>(v0, bias, col0 + 64, g.N, wb[2]);
                     convert_piece<false>(v1, bias, col0 + 96, g.N, wb[3]);
                 }
-                if (row0 >= g.M || col0 >= g.N) continue;
+                // The four warps of column group h (one per lane quarter) stage their 32 x 32
+                // pieces side by side, in row order, and one of them stores the 128-row column
+                // strip with one tensor store (a quarter of the store operations).
+                if (rowblk >= g.M || col0 >= g.N) continue;   // the same for the group's warps
+                const uint32_t gbuf = smem_addr(sm.out[4 * h]);
+                const bool issuer = ((warp - kEpi0) & 3) == 0;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if (col0 + c * 32 >= g.N) break;
-                    if (lane == 0) bulk_wait_read_all();
-                    __syncwarp();
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        sts128(obuf + swz64(lane, j), wb[c][4 * j], wb[c][4 * j + 1], wb[c][4 * j + 2], wb[c][4 * j + 3]);
+                        sts128(gbuf + q * kOutBytes + swz64(lane, j), wb[c][4 * j], wb[c][4 * j + 1], wb[c][4 * j + 2],
+                               wb[c][4 * j + 3]);
                     fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_2d_hint(&P.cmap[pj], static_cast<int32_t>(col0 + c * 32), static_cast<int32_t>(row0),
-                                          obuf, pol);
+                    named_barrier(kBarStore0 + h, 128);
+                    if (issuer && lane == 0) {
+                        tma_store_2d_hint(&P.cmap[pj], static_cast<int32_t>(col0 + c * 32), static_cast<int32_t>(rowblk),
+                                          gbuf, pol);
                         bulk_commit_group();
+                        bulk_wait_read_all();
                     }
+                    named_barrier(kBarStore0 + h, 128);
                 }
                 continue;
             }
