@@ -504,3 +504,32 @@ def test_flux_linear1_step_wide_tiles_sampled(tile_policy):
     xcq, xcs = oracle.quantize_col(xb)
     c, cabs = oracle.gemm(aq, a_s, xcq, xcs)
     check_gemm(dw[torch.as_tensor(nrows, device="cuda")], c, cabs, "linear1 wgrad (wide)")
+
+
+def test_wide_batch_with_bias_equals_narrow_singles(tile_policy):
+    # The batched wide instance with a bias (two bf16 CTA-pair problems, one with a bias and
+    # one without) gives each problem the bytes of its own narrow call.
+    probs = [(384, 768, 640, True), (513, 1000, 2048, False), (640, 1152, 384, True)]
+    tasks, outs, refs = [], [], []
+    for i, (M, N, K, with_bias) in enumerate(probs):
+        a = workloads.student_t3((M, K), 1.0, 801 + i)
+        b = workloads.normal((N, K), 0.5, 901 + i)
+        aq, a_s = abi.quantize(pitched(a), dual=False)
+        bq, b_s = abi.quantize(pitched(b), dual=False)
+        bias = bias_bf16(N, 1001 + i)[1] if with_bias else None
+        tile_policy(abi.MXFP4_TILES_NARROW)
+        ref = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        if with_bias:
+            abi.mxfp4_gemm_bias(aq, a_s, bq, b_s, M, N, K, bias, ref, N, abi.MXFP4_OUT_BF16)
+        else:
+            abi.mxfp4_gemm(aq, a_s, bq, b_s, M, N, K, ref, N, abi.MXFP4_OUT_BF16)
+        out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+        tasks.append((aq, a_s, bq, b_s, M, N, K, out, N, abi.MXFP4_OUT_BF16, bias))
+        outs.append(out)
+        refs.append(ref)
+    tile_policy(abi.MXFP4_TILES_WIDE)
+    abi.mxfp4_gemm_batch(tasks)
+    torch.cuda.synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    for out, ref in zip(outs, refs):
+        assert torch.equal(out.view(torch.uint8).cpu(), ref.view(torch.uint8).cpu())
