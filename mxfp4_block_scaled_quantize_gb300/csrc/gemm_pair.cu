@@ -386,24 +386,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<kWide>::kThr
                         const uint32_t sf = tmem + C::kSfTmemBase + s * C::kSfTmemPerStage;
                         const uint32_t sfa_s = smem_addr(sm.sfa[s]);
                         const uint32_t sfb_s = smem_addr(sm.sfb[s]);
+                        const uint64_t adesc = smem_desc(smem_addr(sm.a[s]), 16, 1024, 2);
+                        const uint64_t bdesc = smem_desc(smem_addr(sm.b[s]), 16, 1024, 2);
+                        const uint64_t bdesc2 = smem_desc(smem_addr(sm.b[s]) + 128 * BKB, 16, 1024, 2);
+                        // per scale atom (128 elements of K): its copies, then the two K-64
+                        // slices that read them, so a tile's first MMA waits for one atom's
+                        // copies only
                         for (int a = 0; a < natoms; ++a) {
                             tc_cp_32x128b_warpx4_pair(sf + a * 4, smem_desc(sfa_s + a * 512, 0, 128, 0));
 #pragma unroll
                             for (int gb = 0; gb < C::kBGroups; ++gb)
                                 tc_cp_32x128b_warpx4_pair(sf + 8 + (a * C::kBGroups + gb) * 4,
                                                           smem_desc(sfb_s + gb * 1024 + a * 512, 0, 128, 0));
-                        }
-                        const uint64_t adesc = smem_desc(smem_addr(sm.a[s]), 16, 1024, 2);
-                        const uint64_t bdesc = smem_desc(smem_addr(sm.b[s]), 16, 1024, 2);
-                        const uint64_t bdesc2 = smem_desc(smem_addr(sm.b[s]) + 128 * BKB, 16, 1024, 2);
-                        for (int j = 0; j < natoms * 2; ++j) {
-                            const uint32_t sf_id = (j & 1) * 2;
-                            const uint32_t sfb = sf + 8 + (j >> 1) * 4 * C::kBGroups;
-                            tc_mma_mxf4_pair(tmem, adesc + 2 * j, bdesc + 2 * j, pair_idesc(sf_id, 256),
-                                             sf + (j >> 1) * 4, sfb, (ks | j) != 0);
-                            if (kWide)
-                                tc_mma_mxf4_pair(tmem + 256, adesc + 2 * j, bdesc2 + 2 * j, pair_idesc(sf_id, 128),
-                                                 sf + (j >> 1) * 4, sfb + 8, (ks | j) != 0);
+                            const uint32_t sfb = sf + 8 + a * 4 * C::kBGroups;
+#pragma unroll
+                            for (int jj = 0; jj < 2; ++jj) {
+                                const int j = 2 * a + jj;
+                                const uint32_t sf_id = jj * 2;
+                                tc_mma_mxf4_pair(tmem, adesc + 2 * j, bdesc + 2 * j, pair_idesc(sf_id, 256), sf + a * 4,
+                                                 sfb, (ks | j) != 0);
+                                if (kWide)
+                                    tc_mma_mxf4_pair(tmem + 256, adesc + 2 * j, bdesc2 + 2 * j, pair_idesc(sf_id, 128),
+                                                     sf + a * 4, sfb + 8, (ks | j) != 0);
+                            }
                         }
                         tc_commit_pair_multicast(smem_addr(&sm.empty[s]), 3);
                         if (ks == g.k_stages - 1) tc_commit_pair_multicast(smem_addr(&sm.tmem_full), 3);
