@@ -221,30 +221,51 @@ __global__ void __launch_bounds__(kFThreads) fp8_quantize_kernel(const __grid_co
 }  // namespace
 
 cudaError_t launch_fp8_quantize(const Fp8QuantBatch& b, int sms, cudaStream_t stream) {
-    fp8_zero_kernel<<<1, 32, 0, stream>>>(b);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // Tensor by tensor, the amax pass then the conversion pass: the conversion re-reads a
-    // tensor the amax pass has just streamed through L2, instead of one the amax pass over
-    // all tensors has long evicted.
+    bool any_amax = false;
+    for (int j = 0; j < b.count; ++j) any_amax = any_amax || !b.t[j].amax_given;
+    cudaError_t e;
+    if (any_amax) {
+        fp8_zero_kernel<<<1, 32, 0, stream>>>(b);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    auto convert = [&](const Fp8QuantBatch& sub) {
+        const int64_t tiles = sub.tile_end[sub.count - 1];
+        const int grid2 = static_cast<int>(tiles < int64_t{sms} * 8 ? tiles : int64_t{sms} * 8);
+        fp8_quantize_kernel<<<grid2, kFThreads, 0, stream>>>(sub);
+        return cudaGetLastError();
+    };
+    // A tensor whose amax is still to be found: its amax pass, then its conversion pass right
+    // away, which re-reads the tensor the amax pass has just streamed through L2 instead of
+    // one the amax pass over all tensors has long evicted.
+    Fp8QuantBatch given = b;
+    given.count = 0;
     for (int j = 0; j < b.count; ++j) {
+        const int64_t rows = b.row_end[j] - (j > 0 ? b.row_end[j - 1] : 0);
+        const int64_t tiles = b.tile_end[j] - (j > 0 ? b.tile_end[j - 1] : 0);
+        if (b.t[j].amax_given) {
+            // the tensors whose amax is known convert together, in one launch, last
+            const int k = given.count++;
+            given.t[k] = b.t[j];
+            given.row_end[k] = (k > 0 ? given.row_end[k - 1] : 0) + rows;
+            given.tile_end[k] = (k > 0 ? given.tile_end[k - 1] : 0) + tiles;
+            continue;
+        }
         Fp8QuantBatch one = b;
         one.count = 1;
         one.t[0] = b.t[j];
-        one.row_end[0] = b.row_end[j] - (j > 0 ? b.row_end[j - 1] : 0);
-        one.tile_end[0] = b.tile_end[j] - (j > 0 ? b.tile_end[j - 1] : 0);
-        if (!one.t[0].amax_given) {
-            const int64_t rows = one.row_end[0];
-            const int64_t want = (rows + 7) / 8;   // 8 warps per CTA, one row each
-            const int grid1 = static_cast<int>(want < int64_t{sms} * 8 ? want : int64_t{sms} * 8);
-            fp8_amax_kernel<<<grid1 > 0 ? grid1 : 1, 256, 0, stream>>>(one);
-            e = cudaGetLastError();
-            if (e != cudaSuccess) return e;
-        }
-        const int64_t tiles = one.tile_end[0];
-        const int grid2 = static_cast<int>(tiles < int64_t{sms} * 8 ? tiles : int64_t{sms} * 8);
-        fp8_quantize_kernel<<<grid2, kFThreads, 0, stream>>>(one);
+        one.row_end[0] = rows;
+        one.tile_end[0] = tiles;
+        const int64_t want = (rows + 7) / 8;   // 8 warps per CTA, one row each
+        const int grid1 = static_cast<int>(want < int64_t{sms} * 8 ? want : int64_t{sms} * 8);
+        fp8_amax_kernel<<<grid1 > 0 ? grid1 : 1, 256, 0, stream>>>(one);
         e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        e = convert(one);
+        if (e != cudaSuccess) return e;
+    }
+    if (given.count > 0) {
+        e = convert(given);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -249,7 +249,9 @@ class MXFP4Linear:
     @property
     def launches_per_step(self) -> int:
         if self.fp8_backward:
-            return 2 + 3 + 1   # X+W, fwd; FP8 quantization of dY, X, W (zero, amax, convert); the GEMMs
+            # X+W (amax zeroing, row-only quantization), fwd; FP8 quantization of dY, X, W
+            # (zeroing, dY's amax, dY's conversion, X's and W's conversion); the FP8 GEMMs
+            return 2 + 1 + 4 + 1
         return 4 if self.train else 2
 
 
@@ -287,7 +289,7 @@ class MXFP4Block:
             for name, L, t in reversed(list(zip(self.names, self.layers, inputs))):
                 if L.fp8_backward:
                     # zero, dY's amax and conversion, X's and W's conversions
-                    out.append((f"{name}.quant_fp8_dY_X_W", lambda L=L, t=t: L.quantize_fp8_bwd(t["dY"]), 5))
+                    out.append((f"{name}.quant_fp8_dY_X_W", lambda L=L, t=t: L.quantize_fp8_bwd(t["dY"]), 4))
                     out.append((f"{name}.gemm_fp8_dgrad_wgrad", lambda L=L: L.fp8_bwd_gemms(), 1))
                 else:
                     out.append((f"{name}.quant_dual_dY",
