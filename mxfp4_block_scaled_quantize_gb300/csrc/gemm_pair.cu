@@ -11,7 +11,7 @@
 //
 // Layout facts this relies on (measured on the part: each CTA's scale copy lands in its
 // own TMEM from its own shared memory, and each SM reads all N B-scales from its own TMEM):
-//   - every CTA loads the A scales of its own rows and the B scales of all 256 tile rows;
+//   - every CTA loads the A scales of its own rows and the B scales of all the tile's rows;
 //   - all loads of a stage, from both CTAs, complete on the even CTA's `full` barrier;
 //   - the MMA's commit arrives on `empty` / `tmem_full` in both CTAs (multicast).
 //
