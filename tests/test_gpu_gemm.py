@@ -411,12 +411,14 @@ def tile_policy():
 
 @pytest.mark.parametrize("M,N,K", [(384, 768, 640), (300, 520, 1000), (513, 1000, 2048), (257, 385, 128),
                                    (1000, 1152, 384), (640, 2304, 4608), (2048, 383, 256),
-                                   (6500, 520, 256)])
+                                   (6500, 520, 256), (256, 384, 256), (300, 64, 256), (1024, 136, 512),
+                                   (129, 392, 96)])
 def test_wide_tiles_match_oracle_and_narrow_tiles(M, N, K, tile_policy):
     # 256 x 384 tiles (one N 256 and one N 128 MMA per K slice, ragged M, N and K edges,
     # tile grids of one to several waves) against the oracle, and bit for bit against the
     # 256 x 256 tiles.  M 6500 has 26 row tiles: its tiles are walked in groups of 8 row
-    # tiles, the last group holding 2.
+    # tiles, the last group holding 2.  N 64 and 136 leave the N 128 MMA's rows (and part of
+    # the N 256 one's) wholly past N; M 129 leaves the odd CTA's rows wholly past M.
     a = workloads.student_t3((M, K), 1.0, 11 + M + 3 * N + 7 * K)
     b = workloads.normal((N, K), 0.5, 13 + M + 5 * N + 11 * K)
     tile_policy(abi.MXFP4_TILES_WIDE)
