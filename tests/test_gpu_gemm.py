@@ -418,7 +418,7 @@ def test_wide_tiles_match_oracle_and_narrow_tiles(M, N, K, tile_policy):
     # tile grids of one to several waves) against the oracle, and bit for bit against the
     # 256 x 256 tiles.  M 6500 has 26 row tiles: its tiles are walked in groups of 8 row
     # tiles, the last group holding 2.  N 64 and 136 leave the N 128 MMA's rows (and part of
-    # the N 256 one's) wholly past N; M 129 leaves the odd CTA's rows wholly past M.
+    # the N 256 one's) wholly past N; M 129 leaves the odd CTA one row, K 96 one scale atom.
     a = workloads.student_t3((M, K), 1.0, 11 + M + 3 * N + 7 * K)
     b = workloads.normal((N, K), 0.5, 13 + M + 5 * N + 11 * K)
     tile_policy(abi.MXFP4_TILES_WIDE)
