@@ -449,6 +449,32 @@ mxfp4_status mxfp4_linear_workspace_bytes(int32_t count, const mxfp4_linear_host
 mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task* tasks,
                                     void* workspace, size_t workspace_bytes, mxfp4_stream_t stream);
 
+/* Pipelined form of mxfp4_linear_step_host for a loop of steps: the same copies, kernels
+ * and results, but consecutive calls overlap.  Each refill of a device input waits only for
+ * the previous step's quantizer of that input, the results of consecutive steps leave from
+ * two output sets used alternately, and when the call returns `stream` is ordered after the
+ * step's kernels and copies in but NOT after its copies out, so the next step's copies in
+ * and kernels run while this step's results are still being copied out.
+ *   workspace  at least mxfp4_linear_pipelined_workspace_bytes (the plain step's workspace
+ *              and a second output set), 256-byte aligned; keep the same workspace and
+ *              tasks' shapes from one call to the next
+ * The host results of a step are in host memory once mxfp4_linear_host_wait(stream) has
+ * been called after it and `stream` has been synchronized.  A host input buffer may be
+ * rewritten once `stream` has passed the call (its copies in are done); a host output
+ * buffer is written by every call that names it, in call order.  Errors as for
+ * mxfp4_linear_step_host.  A plain mxfp4_linear_step_host call between pipelined ones is
+ * allowed (it waits for everything before it, as always). */
+mxfp4_status mxfp4_linear_pipelined_workspace_bytes(int32_t count, const mxfp4_linear_host_task* tasks,
+                                                    size_t* bytes);
+mxfp4_status mxfp4_linear_step_host_pipelined(int32_t count, const mxfp4_linear_host_task* tasks,
+                                              void* workspace, size_t workspace_bytes,
+                                              mxfp4_stream_t stream);
+
+/* Orders `stream` after every copy (in and out) of every host step enqueued on the current
+ * device so far: synchronizing `stream` afterwards makes all their results visible in host
+ * memory. */
+mxfp4_status mxfp4_linear_host_wait(mxfp4_stream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the device error word of the current
  * device: MXFP4_ERR_TIMEOUT if a bounded wait in any kernel of this library ran out
  * since the last call, else MXFP4_ERR_NONFINITE if a tensorwise FP8 quantization met a

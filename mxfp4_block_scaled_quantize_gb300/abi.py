@@ -96,6 +96,9 @@ EXPORTED = (
     "mxfp4_fp8_gemm_batch",
     "mxfp4_linear_workspace_bytes",
     "mxfp4_linear_step_host",
+    "mxfp4_linear_pipelined_workspace_bytes",
+    "mxfp4_linear_step_host_pipelined",
+    "mxfp4_linear_host_wait",
     "mxfp4_last_device_error",
     "mxfp4_selftest_bounded_wait",
     "mxfp4_status_string",
@@ -146,6 +149,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mxfp4_linear_workspace_bytes.argtypes = [i32, ctypes.POINTER(LinearHostTask),
                                                  ctypes.POINTER(ctypes.c_size_t)]
     lib.mxfp4_linear_step_host.argtypes = [i32, ctypes.POINTER(LinearHostTask), vp, ctypes.c_size_t, vp]
+    lib.mxfp4_linear_pipelined_workspace_bytes.argtypes = [i32, ctypes.POINTER(LinearHostTask),
+                                                           ctypes.POINTER(ctypes.c_size_t)]
+    lib.mxfp4_linear_step_host_pipelined.argtypes = [i32, ctypes.POINTER(LinearHostTask), vp, ctypes.c_size_t, vp]
+    lib.mxfp4_linear_host_wait.argtypes = [vp]
     lib.mxfp4_last_device_error.argtypes = [vp]
     lib.mxfp4_selftest_bounded_wait.argtypes = [i64, vp]
     lib.mxfp4_status_string.argtypes = [i32]
@@ -371,6 +378,23 @@ def mxfp4_linear_workspace_bytes(tasks) -> int:
 def mxfp4_linear_step_host(tasks, workspace, workspace_bytes: int, stream=None) -> None:
     _check(load().mxfp4_linear_step_host(len(tasks), _host_tasks(tasks), _ptr(workspace),
                                          workspace_bytes, _stream(stream)), "mxfp4_linear_step_host")
+
+
+def mxfp4_linear_pipelined_workspace_bytes(tasks) -> int:
+    n = ctypes.c_size_t()
+    _check(load().mxfp4_linear_pipelined_workspace_bytes(len(tasks), _host_tasks(tasks), ctypes.byref(n)),
+           "mxfp4_linear_pipelined_workspace_bytes")
+    return n.value
+
+
+def mxfp4_linear_step_host_pipelined(tasks, workspace, workspace_bytes: int, stream=None) -> None:
+    _check(load().mxfp4_linear_step_host_pipelined(len(tasks), _host_tasks(tasks), _ptr(workspace),
+                                                   workspace_bytes, _stream(stream)),
+           "mxfp4_linear_step_host_pipelined")
+
+
+def mxfp4_linear_host_wait(stream=None) -> None:
+    _check(load().mxfp4_linear_host_wait(_stream(stream)), "mxfp4_linear_host_wait")
 
 
 def mxfp4_last_device_error(stream=None) -> int:

@@ -4,6 +4,9 @@
 // entry points on the caller's stream, and copies every result out on a second stream as
 // soon as the kernel that writes it is done.  Events order the three streams, so each
 // quantization waits only for its own inputs and the result copies overlap later kernels.
+// The pipelined form (mxfp4_linear_step_host_pipelined) also lets consecutive steps
+// overlap: a step's results leave from one of two output sets while the next step's inputs
+// come in and its kernels run.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -22,6 +25,15 @@ struct CopyStreams {
     cudaStream_t h2d = nullptr;
     cudaStream_t d2h = nullptr;
     cudaEvent_t ev[kEventsPerStep] = {};
+    // Across calls: the last step's quantizers are done with each linear's device inputs
+    // (X and W; dY), so the next step may refill them; and the copies out of the last step
+    // that wrote each output set are done, so a step may write that set again.
+    cudaEvent_t consumed_xw[MXFP4_MAX_BATCH] = {};
+    cudaEvent_t consumed_dy[MXFP4_MAX_BATCH] = {};
+    cudaEvent_t slot_free[2] = {};
+    bool consumed_valid = false;
+    bool slot_valid[2] = {false, false};
+    int slot = 0;
 };
 
 std::mutex g_host_mutex;
@@ -44,6 +56,24 @@ struct Carve {
 
 size_t blob_q(int64_t rows, int64_t k) { return static_cast<size_t>(rows) * static_cast<size_t>(pad128(k) / 2); }
 size_t blob_s(int64_t rows, int64_t k) { return static_cast<size_t>(pad128(rows)) * static_cast<size_t>(pad128(k) / 32); }
+
+// Lays out one task's output buffers (Y; dX, dW) from `base` (nullptr: only measures) over
+// the ones `carve` placed.  Returns the bytes used.
+size_t carve_outputs(const mxfp4_linear_host_task& t, uint8_t* base, Carve* c) {
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        uint8_t* p = base ? base + off : nullptr;
+        off += align256(n);
+        return p;
+    };
+    const size_t es = t.out_dtype == MXFP4_OUT_F32 ? 4 : 2;
+    c->y = take(static_cast<size_t>(t.M) * t.N * es);
+    if (t.train) {
+        c->dx = take(static_cast<size_t>(t.M) * t.K * es);
+        c->dw = take(static_cast<size_t>(t.N) * t.K * es);
+    }
+    return off;
+}
 
 // Lays out one task's buffers from `base` (nullptr: only measures).  Returns the bytes used.
 size_t carve(const mxfp4_linear_host_task& t, uint8_t* base, Carve* c) {
@@ -100,6 +130,14 @@ size_t total_bytes(int32_t count, const mxfp4_linear_host_task* tasks) {
     return n;
 }
 
+// The pipelined step's workspace: the plain step's, then a second set of outputs.
+size_t pipelined_bytes(int32_t count, const mxfp4_linear_host_task* tasks) {
+    size_t n = total_bytes(count, tasks);
+    Carve c = {};
+    for (int i = 0; i < count; ++i) n += carve_outputs(tasks[i], nullptr, &c);
+    return n;
+}
+
 // bf16 rows of `cols` elements from dense host rows into device rows of pitch round8(cols).
 cudaError_t copy_in(uint8_t* dst, const void* src, int64_t rows, int64_t cols, cudaStream_t s) {
     const size_t w = static_cast<size_t>(cols) * 2;
@@ -123,6 +161,12 @@ mxfp4_status copy_streams(CopyStreams** out) {
             return MXFP4_ERR_CUDA;
         for (auto& e : c.ev)
             if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return MXFP4_ERR_CUDA;
+        for (int i = 0; i < MXFP4_MAX_BATCH; ++i)
+            if (cudaEventCreateWithFlags(&c.consumed_xw[i], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&c.consumed_dy[i], cudaEventDisableTiming) != cudaSuccess)
+                return MXFP4_ERR_CUDA;
+        for (auto& e : c.slot_free)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return MXFP4_ERR_CUDA;
         c.ready = true;
     }
     *out = &c;
@@ -141,19 +185,18 @@ mxfp4_status copy_streams(CopyStreams** out) {
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-mxfp4_status mxfp4_linear_workspace_bytes(int32_t count, const mxfp4_linear_host_task* tasks, size_t* bytes) {
-    MX_TRY_ST(check_tasks(count, tasks, false));
-    if (bytes == nullptr) return MXFP4_ERR_INVALID_ARG;
-    *bytes = total_bytes(count, tasks);
-    return MXFP4_OK;
-}
-
-mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task* tasks, void* workspace,
-                                    size_t workspace_bytes, mxfp4_stream_t stream) {
+// One step from host buffers to host buffers (both entry points).  Pipelined: the
+// workspace holds two output sets used alternately, each refill of a device input waits
+// only for the previous step's quantizer of that input, and the caller's stream is not
+// ordered after the copies out (mxfp4_linear_host_wait does that).
+mxfp4_status step_host(int32_t count, const mxfp4_linear_host_task* tasks, void* workspace, size_t workspace_bytes,
+                       mxfp4_stream_t stream, bool pipelined) {
     MX_TRY_ST(check_tasks(count, tasks, true));
-    if (workspace == nullptr || workspace_bytes < total_bytes(count, tasks)) return MXFP4_ERR_INVALID_ARG;
+    if (workspace == nullptr ||
+        workspace_bytes < (pipelined ? pipelined_bytes(count, tasks) : total_bytes(count, tasks)))
+        return MXFP4_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MXFP4_ERR_MISALIGNED;
     std::lock_guard<std::mutex> lock(g_host_mutex);
     CopyStreams* cs = nullptr;
@@ -172,15 +215,25 @@ mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task*
     Carve c[MXFP4_MAX_BATCH] = {};
     uint8_t* base = static_cast<uint8_t*>(workspace);
     for (int i = 0; i < count; ++i) base += carve(tasks[i], base, &c[i]);
+    const int slot = pipelined ? cs->slot : 0;
+    if (slot == 1)   // the second output set, after the first layout
+        for (int i = 0; i < count; ++i) base += carve_outputs(tasks[i], base, &c[i]);
+    const bool wait_inputs = pipelined && cs->consumed_valid;
 
-    // The previous step's kernels are done with the input buffers before they refill.
+    // The previous step's kernels are done with the input buffers before they refill
+    // (pipelined: each input waits only for the quantizer that read it).
     MX_TRY(cudaEventRecord(ev_start, comp));
-    MX_TRY(cudaStreamWaitEvent(cs->h2d, ev_start, 0));
+    if (!pipelined) MX_TRY(cudaStreamWaitEvent(cs->h2d, ev_start, 0));
     MX_TRY(cudaStreamWaitEvent(cs->d2h, ev_start, 0));
+    // The output set is free: the copies out of the step that last wrote it are done (a
+    // plain step after pipelined ones waits for all their copies out).
+    if (pipelined && cs->slot_valid[slot]) MX_TRY(cudaStreamWaitEvent(comp, cs->slot_free[slot], 0));
+    if (!pipelined && (cs->slot_valid[0] || cs->slot_valid[1])) MX_TRY(cudaStreamWaitEvent(comp, ev_d2h_done, 0));
     // Inputs in the order the kernels read them: X, W of each forward, then dY of each
     // backward (reverse task order).
     for (int i = 0; i < count; ++i) {
         const mxfp4_linear_host_task& t = tasks[i];
+        if (wait_inputs) MX_TRY(cudaStreamWaitEvent(cs->h2d, cs->consumed_xw[i], 0));
         MX_TRY(copy_in(c[i].xd, t.x, t.M, t.K, cs->h2d));
         MX_TRY(copy_in(c[i].wd, t.w, t.N, t.K, cs->h2d));
         MX_TRY(cudaEventRecord(ev_xw(i), cs->h2d));
@@ -188,6 +241,7 @@ mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task*
     for (int i = count - 1; i >= 0; --i) {
         const mxfp4_linear_host_task& t = tasks[i];
         if (!t.train) continue;
+        if (wait_inputs) MX_TRY(cudaStreamWaitEvent(cs->h2d, cs->consumed_dy[i], 0));
         MX_TRY(copy_in(c[i].dyd, t.dy, t.M, t.N, cs->h2d));
         MX_TRY(cudaEventRecord(ev_dy(i), cs->h2d));
     }
@@ -204,6 +258,7 @@ mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task*
             {b.wd, t.N, t.K, ldk, b.wrq, b.wrs, b.wcq, b.wcs, 0, 0},
         };
         MX_TRY_ST(mxfp4_quantize_batch(2, q, t.train, MXFP4_SCALE_TC, stream));
+        MX_TRY(cudaEventRecord(cs->consumed_xw[i], comp));
         MX_TRY_ST(mxfp4_gemm(b.xrq, b.xrs, b.wrq, b.wrs, t.M, t.N, t.K, b.y, t.N, t.out_dtype, stream));
         MX_TRY(cudaEventRecord(ev_y(i), comp));
         MX_TRY(cudaStreamWaitEvent(cs->d2h, ev_y(i), 0));
@@ -217,6 +272,7 @@ mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task*
         MX_TRY(cudaStreamWaitEvent(comp, ev_dy(i), 0));
         MX_TRY_ST(mxfp4_quantize_dual(b.dyd, t.M, t.N, round8(t.N), b.drq, b.drs, b.dcq, b.dcs, MXFP4_SCALE_TC,
                                       stream));
+        MX_TRY(cudaEventRecord(cs->consumed_dy[i], comp));
         const mxfp4_gemm_task g[2] = {
             {b.drq, b.drs, b.wcq, b.wcs, t.M, t.K, t.N, b.dx, t.K, t.out_dtype, nullptr},
             {b.dcq, b.dcs, b.xcq, b.xcs, t.N, t.K, t.M, b.dw, t.K, t.out_dtype, nullptr},
@@ -229,9 +285,61 @@ mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task*
         MX_TRY(copy_out(t.dx, b.dx, t.M, t.K, es, cs->d2h));
     }
     MX_TRY(cudaEventRecord(ev_d2h_done, cs->d2h));
-    // The caller's stream is ordered after every copy of the step.
     MX_TRY(cudaStreamWaitEvent(comp, ev_h2d_done, 0));
-    MX_TRY(cudaStreamWaitEvent(comp, ev_d2h_done, 0));
+    if (pipelined) {
+        // The caller's stream runs on; the next step writes the other output set.
+        MX_TRY(cudaEventRecord(cs->slot_free[slot], cs->d2h));
+        cs->slot_valid[slot] = true;
+        cs->slot = slot ^ 1;
+        cs->consumed_valid = true;
+    } else {
+        // The caller's stream is ordered after every copy of the step, so nothing of it is
+        // in flight when the next step starts.
+        MX_TRY(cudaStreamWaitEvent(comp, ev_d2h_done, 0));
+        cs->slot_valid[0] = cs->slot_valid[1] = false;
+        cs->slot = 0;
+        cs->consumed_valid = false;
+    }
+    return MXFP4_OK;
+}
+
+
+}  // namespace
+
+extern "C" {
+
+mxfp4_status mxfp4_linear_workspace_bytes(int32_t count, const mxfp4_linear_host_task* tasks, size_t* bytes) {
+    MX_TRY_ST(check_tasks(count, tasks, false));
+    if (bytes == nullptr) return MXFP4_ERR_INVALID_ARG;
+    *bytes = total_bytes(count, tasks);
+    return MXFP4_OK;
+}
+
+mxfp4_status mxfp4_linear_step_host(int32_t count, const mxfp4_linear_host_task* tasks, void* workspace,
+                                    size_t workspace_bytes, mxfp4_stream_t stream) {
+    return step_host(count, tasks, workspace, workspace_bytes, stream, false);
+}
+
+mxfp4_status mxfp4_linear_pipelined_workspace_bytes(int32_t count, const mxfp4_linear_host_task* tasks,
+                                                    size_t* bytes) {
+    MX_TRY_ST(check_tasks(count, tasks, false));
+    if (bytes == nullptr) return MXFP4_ERR_INVALID_ARG;
+    *bytes = pipelined_bytes(count, tasks);
+    return MXFP4_OK;
+}
+
+mxfp4_status mxfp4_linear_step_host_pipelined(int32_t count, const mxfp4_linear_host_task* tasks,
+                                              void* workspace, size_t workspace_bytes, mxfp4_stream_t stream) {
+    return step_host(count, tasks, workspace, workspace_bytes, stream, true);
+}
+
+mxfp4_status mxfp4_linear_host_wait(mxfp4_stream_t stream) {
+    std::lock_guard<std::mutex> lock(g_host_mutex);
+    CopyStreams* cs = nullptr;
+    MX_TRY_ST(copy_streams(&cs));
+    cudaStream_t comp = reinterpret_cast<cudaStream_t>(stream);
+    MX_TRY(cudaStreamWaitEvent(comp, cs->ev[kEventsPerStep - 2], 0));
+    MX_TRY(cudaStreamWaitEvent(comp, cs->ev[kEventsPerStep - 1], 0));
     return MXFP4_OK;
 }
 

@@ -272,6 +272,7 @@ class MXFP4Block:
                                    backward=backward, weight_2d=weight_2d, rht_signs=rht_signs)
                        for _, M, N, K in shapes]
         self._ws = None
+        self._pws = None   # the pipelined host step's workspace (two output sets)
 
     def ops(self, inputs, bias=None, sr_seed=None):
         """One step as a list of (name, callable, launches): each callable enqueues one
@@ -323,6 +324,22 @@ class MXFP4Block:
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(need, dtype=torch.uint8, device=self.layers[0].y.device)
         abi.mxfp4_linear_step_host(tasks, self._ws, self._ws.numel(), stream)
+
+    def step_host_pipelined(self, host_inputs, host_outputs, stream=None):
+        """step_host for a loop of steps (mxfp4_linear_step_host_pipelined): consecutive
+        calls overlap one step's copies out with the next step's copies in and kernels.
+        Call host_wait() and synchronize the stream before reading the host outputs."""
+        assert not any(L.fp8_backward or L.weight_2d or L.rht_signs is not None for L in self.layers), \
+            "the host step runs the plain MXFP4 recipe"
+        tasks = self.host_tasks(host_inputs, host_outputs)
+        need = abi.mxfp4_linear_pipelined_workspace_bytes(tasks)
+        if self._pws is None or self._pws.numel() < need:
+            self._pws = torch.empty(need, dtype=torch.uint8, device=self.layers[0].y.device)
+        abi.mxfp4_linear_step_host_pipelined(tasks, self._pws, self._pws.numel(), stream)
+
+    def host_wait(self, stream=None):
+        """Orders the stream after every copy of the host steps enqueued so far."""
+        abi.mxfp4_linear_host_wait(stream)
 
     @property
     def launches_per_step(self) -> int:

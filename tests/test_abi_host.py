@@ -115,6 +115,8 @@ def test_argument_checks_precede_any_device_use(lib):
     G = abi.GemmTask
     g_ok = G(16, 32, 48, 64, 4, 4, 4, 80, 4, 0)
     garr = (G * 5)(*([g_ok] * 5))
+    assert lib.mxfp4_linear_step_host_pipelined(0, None, None, 0, None) == abi.MXFP4_ERR_INVALID_ARG
+    assert lib.mxfp4_linear_pipelined_workspace_bytes(1, None, None) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_gemm_set_tile_policy(3) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_gemm_set_tile_policy(-1) == abi.MXFP4_ERR_INVALID_ARG
     assert lib.mxfp4_gemm_set_tile_policy(abi.MXFP4_TILES_AUTO) == abi.MXFP4_OK

@@ -133,6 +133,58 @@ def test_block_host_step_matches_device_step():
                 assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
 
 
+def test_pipelined_host_steps_match_device_steps():
+    # Five consecutive host-buffer steps of two linears (one training with bf16 outputs, one
+    # forward-only with fp32 outputs), each step with inputs of its own: four through the
+    # pipelined entry point (the two output sets each used twice, the inputs refilled while
+    # the previous step's results are still being copied out) and a plain call in the middle.
+    # Every step's host results are the bytes of the device step on that step's inputs.
+    shapes = [(300, 520, 200, True, torch.bfloat16), (257, 136, 1001, False, torch.float32)]
+    steps = 5
+    host_in, want = [], []
+    for k in range(steps):
+        hin, wk = [], []
+        for i, (M, N, K, train, od) in enumerate(shapes):
+            t = {"X": workloads.student_t3((M, K), 1.0, 1000 + 10 * k + i),
+                 "W": workloads.normal((N, K), 0.3, 2000 + 10 * k + i)}
+            if train:
+                t["dY"] = workloads.normal((M, N), 0.01, 3000 + 10 * k + i)
+            hin.append({n: v.pin_memory() for n, v in t.items()})
+            ref = MXFP4Linear(M, N, K, train=train, out_dtype=od)
+            outs = ref.step(pitched(t["X"]), pitched(t["W"]), pitched(t["dY"]) if train else None)
+            wk.append([o.cpu() for o in outs])
+        host_in.append(hin)
+        want.append(wk)
+    torch.cuda.synchronize()
+    got = []
+    tasks_of = []
+    for k in range(steps):
+        tasks, gk = [], []
+        for (M, N, K, train, od), hi, w_ in zip(shapes, host_in[k], want[k]):
+            code = abi.MXFP4_OUT_F32 if od == torch.float32 else abi.MXFP4_OUT_BF16
+            outs = [torch.full(o.shape, float("nan"), dtype=o.dtype).pin_memory() for o in w_]
+            outs3 = outs + [None] * (3 - len(outs))
+            tasks.append((hi["X"], hi["W"], hi.get("dY"), *outs3, M, N, K, train, code))
+            gk.append(outs)
+        tasks_of.append(tasks)
+        got.append(gk)
+    need = abi.mxfp4_linear_pipelined_workspace_bytes(tasks_of[0])
+    assert need > abi.mxfp4_linear_workspace_bytes(tasks_of[0])
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    for k in range(steps):
+        if k == 2:
+            abi.mxfp4_linear_step_host(tasks_of[k], ws, need)
+        else:
+            abi.mxfp4_linear_step_host_pipelined(tasks_of[k], ws, need)
+    abi.mxfp4_linear_host_wait()
+    torch.cuda.current_stream().synchronize()
+    assert abi.mxfp4_last_device_error() == abi.MXFP4_OK
+    for k in range(steps):
+        for g_, w_ in zip(got[k], want[k]):
+            for a, b in zip(g_, w_):
+                assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f"step {k}"
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (1, 8, 32), (200, 300, 40), (129, 257, 384),
                                    (128, 256, 256), (300, 520, 1000), (64, 1000, 4600),
                                    (256, 128, 128), (384, 768, 640), (513, 255, 2048)])
